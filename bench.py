@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark of the fused linear cross entropy forward+backward on GB300.
+
+One step = one flce_fwd_bwd call over one batch of synthetic inputs (all stages: row
+compaction, logits GEMM with online logsumexp, finalize, gradient formation, dX GEMM, dW
+GEMM, reductions). Default workload: the Llama-3.1-8B-shaped head (BT=8192, H=4096,
+V=128256, bf16, 16 sequences of 512 rows with the last row of each ignored, mean, z-loss
+1e-4, dX and fp32 dW).
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--labelled-fraction F]
+  python bench.py --impl reference ...   # the float64 CPU oracle on a bounded row sample
+
+Prints one JSON line (rank 0). Under torchrun each rank runs an independent replica on its
+own GPU (the op has no exchange step); value = all ranks' tokens / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from linear_cross_entropy_logits_gb300 import inputs as I  # noqa: E402
+
+METRIC = "FLCE fwd+bwd tokens/s and ms at 1 GB300; % of dense bf16 tensor peak"
+UNIT = "tokens/s"
+WORKLOAD_TITLES = {
+    "tiny_fp32": "tiny fp32 FLCE",
+    "llama1b": "Llama-3.2-1B-shaped head",
+    "llama8b": "Llama-3.1-8B-shaped head",
+    "large_vocab": "large-vocab long-context head",
+    "frozen_head": "frozen-head (LoRA) variant",
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="llama8b", choices=list(I.WORKLOADS))
+    p.add_argument("--labelled-fraction", type=float, default=None)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def workload_spec(args):
+    ov = {}
+    if args.labelled_fraction is not None:
+        ov["labelled_fraction"] = args.labelled_fraction
+    return I.spec(args.workload, **ov)
+
+
+def config_of(sp, n_lab, extra=None):
+    c = {"workload": f"{WORKLOAD_TITLES[sp['name']]} ({sp['name']})", "BT": sp["BT"], "H": sp["H"],
+         "V": sp["V"], "input_dtype": sp["dtype"], "n_labelled": int(n_lab),
+         "reduction": sp["reduction"], "z_loss_scale": sp.get("z", 0.0),
+         "bias": sp.get("bias_std") is not None, "dW": bool(sp["want_dW"]),
+         "targets": sp.get("targets", "uniform"), "ignored_rows": sp.get("ignore", "none")}
+    if sp.get("ignore") == "prompt_first":
+        c["labelled_fraction"] = sp.get("labelled_fraction", 1.0)
+    if extra:
+        c.update(extra)
+    return c
+
+
+def flops_per_step(sp, n_lab):
+    return (6 if sp["want_dW"] else 4) * n_lab * sp["H"] * sp["V"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.proc = None
+        self.dev = dev
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_sample_rate(sp, inp, seconds, rows_per_call=32, rng_seed=99):
+    """Time the float64 oracle (as it stands) on seeded samples of labelled rows of this
+    workload until about `seconds` of CPU work; returns (BT-tokens per second, rows,
+    seconds). Ignored rows cost the oracle nothing, so labelled rows per second are scaled
+    by BT / n_labelled to the metric's BT-token convention."""
+    from oracle import flce_oracle as orc
+    t = inp["targets"].numpy()
+    lab = np.nonzero(t != I.IGNORE_INDEX)[0]
+    W = I.to_numpy_exact(inp["W"])
+    b = I.to_numpy_exact(inp["bias"])
+    X = inp["X"]
+    go = inp["grad_out"].numpy() if inp["grad_out"] is not None else None
+    rng = np.random.default_rng(rng_seed)
+    done, spent = 0, 0.0
+    while spent < seconds and done < lab.size:
+        rows = np.sort(rng.choice(lab, size=min(rows_per_call, lab.size), replace=False))
+        Xs = I.to_numpy_exact(X[torch.from_numpy(rows)])
+        gs = go[rows] if (go is not None and sp["reduction"] == "none") else None
+        t0 = time.perf_counter()
+        orc.flce_oracle(Xs, W, t[rows], bias=b, reduction=sp["reduction"],
+                        z_loss_scale=sp.get("z", 0.0), grad_out=gs, want_dX=True,
+                        want_dW=sp["want_dW"])
+        spent += time.perf_counter() - t0
+        done += rows.size
+    rate_lab = done / spent
+    return rate_lab * sp["BT"] / max(lab.size, 1), done, spent
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("internal_api") in ("openblas", "mkl", "blis")]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def traffic_record():
+    """ncu DRAM bytes of the dominant kernel, if taken with the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return rec
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_cross_entropy_logits_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    sp = workload_spec(args)
+    inp = I.generate(sp, seed=0)
+    n_lab = int((inp["targets"] != I.IGNORE_INDEX).sum())
+    per_step_seconds = max(2.0, 100.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        oracle_sample_rate(sp, inp, per_step_seconds / 4, rng_seed=1)
+    rates, rows_total, secs_total = [], 0, 0.0
+    for k in range(args.steps):
+        r, rows, secs = oracle_sample_rate(sp, inp, per_step_seconds, rng_seed=100 + k)
+        rates.append(r)
+        rows_total += rows
+        secs_total += secs
+    value = rows_total * sp["BT"] / max(n_lab, 1) / secs_total
+    ms_per_step = sp["BT"] / value * 1000.0
+    cores = cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.Generator)",
+        "config": config_of(sp, n_lab, {"sample": "seeded samples of labelled rows"}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_total} labelled rows in {args.steps} steps of "
+                                   f"~{per_step_seconds:.0f} s (float64 oracle: logits, lse, "
+                                   f"loss, dX and dW per row), scaled by BT/n_labelled"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    from linear_cross_entropy_logits_gb300 import build as B
+    B.build()
+    from linear_cross_entropy_logits_gb300 import flce
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    sp = workload_spec(args)
+    inp = I.generate(sp, seed=rank)
+    n_lab = int((inp["targets"] != I.IGNORE_INDEX).sum())
+    BT, H, V = sp["BT"], sp["H"], sp["V"]
+    dt = I.TORCH_DTYPES[sp["dtype"]]
+    X = inp["X"].to(dev)
+    W = inp["W"].to(dev)
+    tg = inp["targets"].to(dev)
+    bias = inp["bias"].to(dev) if inp["bias"] is not None else None
+    go = inp["grad_out"].to(dev) if inp["grad_out"] is not None else None
+    ws_bytes = flce.workspace_size(BT, H, V, dt, sp.get("workspace_cap", 0))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    R = flce.chunk_rows(BT, H, V, dt, ws_bytes)
+    nl = BT if sp["reduction"] == "none" else 1
+    outs = {"loss": torch.empty(nl, dtype=torch.float32, device=dev),
+            "z_loss": torch.empty(nl, dtype=torch.float32, device=dev),
+            "acc": torch.empty(nl, dtype=torch.float32, device=dev),
+            "lse": torch.empty(BT, dtype=torch.float32, device=dev),
+            "pred": torch.empty(BT, dtype=torch.int64, device=dev),
+            "n_labelled": torch.empty(1, dtype=torch.int32, device=dev),
+            "status": torch.zeros(1, dtype=torch.int32, device=dev),
+            "dX": torch.empty(BT, H, dtype=dt, device=dev)}
+    dW = torch.zeros(V, H, dtype=torch.float32, device=dev) if sp["want_dW"] else None
+    dbias = torch.zeros(V, dtype=torch.float32, device=dev) if (sp["want_dW"] and bias is not None) else None
+    prof = flce.Profiler()
+
+    def step(Xd=X, tgd=tg, profiler=None):
+        flce.fwd_bwd(Xd, W, tgd, bias, reduction=sp["reduction"], z_loss_scale=sp.get("z", 0.0),
+                     grad_out=go, want_dX=True, want_dW=sp["want_dW"], dW=dW, dbias=dbias,
+                     workspace=ws, outputs=outs, check=False, profiler=profiler)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = flce.load().flce_get_status(outs["status"].data_ptr(), None, stream.cuda_stream)
+    if st != flce.FLCE_OK:
+        raise RuntimeError(f"warm-up status {flce.status_string(st)}")
+
+    # ---- device-timed region
+    clk = ClockSampler(dev)
+    clk.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    prof.reset()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(profiler=prof)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clocks = clk.stop()
+    ms_total = e0.elapsed_time(e1)
+    stages = prof.read()
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = BT * world / (ms_step / 1000.0)
+
+    # ---- end to end through the public API with pinned host inputs / outputs
+    e2e = None
+    if not args.no_e2e:
+        Xh = inp["X"].pin_memory()
+        th = inp["targets"].pin_memory()
+        gh = inp["grad_out"].pin_memory() if inp["grad_out"] is not None else None
+        lh = torch.empty(nl, dtype=torch.float32).pin_memory()
+        Xd = torch.empty_like(X)
+        tgd = torch.empty_like(tg)
+
+        def e2e_step():
+            Xd.copy_(Xh, non_blocking=True)
+            tgd.copy_(th, non_blocking=True)
+            if gh is not None:
+                go.copy_(gh, non_blocking=True)
+            step(Xd, tgd)
+            lh.copy_(outs["loss"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = f0.elapsed_time(f1) / args.steps
+        if dist:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        h2d = Xh.numel() * Xh.element_size() + th.numel() * th.element_size() + \
+            (gh.numel() * gh.element_size() if gh is not None else 0)
+        e2e = {"value": BT * world / (ms_e2e / 1000.0), "unit": UNIT, "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(lh.numel() * 4)}
+
+    # ---- roofline of the dominant kernel (per-stage CUDA events on the launching stream)
+    peaks, peak_src = load_peaks()
+    flops = flops_per_step(sp, n_lab)
+    gemm_flops = 2.0 * n_lab * H * V
+    dom = max(stages, key=lambda k: stages[k][0])
+    dom_ms, dom_launches = stages[dom]
+    per_step_dom_ms = dom_ms / args.steps
+    stage_summary = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+                     for k, v in stages.items() if v[1] > 0}
+    rec = traffic_record()
+    if dom in ("fwd", "dx", "dw"):
+        achieved = gemm_flops / (per_step_dom_ms / 1000.0) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_kind": f"bf16 sustained ({peak_src})",
+                "per_launch": f"2*H*V FLOPs per labelled row x {n_lab * args.steps / max(dom_launches, 1):.0f} rows per launch",
+                "traffic": (rec["traffic_bytes_per_launch"] if rec and rec.get("kernel") == dom else None)}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks.get("hbm_gbs"),
+                "unit": "GB/s", "frac": None, "traffic": None}
+    tflops = flops / (ms_step / 1000.0) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if sp["dtype"] == "bf16" else sp["dtype"],
+        "data": "synthetic (seeded torch.Generator; random-init head weights)",
+        "config": config_of(sp, n_lab, {
+            "parallelism": f"replicas x{world} (no exchange step)",
+            "l2": f"no flush: W ({V * H * I.TORCH_DTYPES[sp['dtype']].itemsize / 1e9:.2f} GB) and the "
+                  f"per-chunk slab exceed the 129 MB L2",
+            "workspace_bytes": ws_bytes, "chunk_rows": R}),
+        "tokens_per_s_labelled": n_lab * world / (ms_step / 1000.0),
+        "tflops": tflops, "flops_per_step": flops,
+        "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
+                              "sustained": tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
+                              "source": peak_src},
+        "roofline": roof,
+        "stages": stage_summary,
+        "gpu_launches": int(sum(v[1] for v in stages.values())),
+        "clocks": clocks,
+        "e2e": e2e,
+        "context_vs_h200_public_default_ms": 53.039 if sp["name"] == "llama8b" else None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows, secs = oracle_sample_rate(sp, inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                                "sample": f"{rows} seeded labelled rows, {secs:.1f} s of float64 oracle "
+                                          f"work (logits, lse, loss, dX, dW), scaled by BT/n_labelled"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

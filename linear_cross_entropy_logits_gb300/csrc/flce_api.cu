@@ -1,0 +1,323 @@
+// C ABI of libflce.so: argument validation, workspace planning and the per-call launch
+// sequence. Declarations and their contracts are in include/flce.h.
+//
+// Launch sequence of one call (all on the caller's stream, no host synchronisation):
+//   compact + ignored rows  ->  for each row chunk: gather, forward GEMM (statistics and
+//   exp slab), finalize (lse, loss, prediction), gradient formation, dX GEMM, dW GEMM
+//   ->  reductions.
+// The number of chunks the host enqueues is cdiv(BT, R); chunks past the labelled count
+// (known only on the device) exit at once, so the transient memory is the workspace the
+// caller sized, whatever the labelled share.
+#include <mutex>
+#include <string.h>
+#include <vector>
+
+#include "flce_internal.cuh"
+
+namespace flce {
+
+namespace {
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+inline size_t rup_sz(size_t a, size_t b) { return (a + b - 1) / b * b; }
+inline bool aligned(const void* p, size_t n) { return ((uintptr_t)p % n) == 0; }
+}  // namespace
+
+bool plan_layout(int64_t BT, int64_t H, int64_t V, int dt, int64_t R, Plan* p) {
+  if (BT <= 0 || H <= 0 || V <= 0 || R <= 0) return false;
+  Plan q;
+  q.BT = BT;
+  q.H = H;
+  q.V = V;
+  q.esz = dtype_size(dt);
+  q.Hp = rup(H, 64);
+  q.nvt = cdiv(V, VT);
+  q.Vp = q.nvt * VT;
+  q.R = R;
+  q.kmax = cdiv(BT, R);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = rup_sz(off + bytes, 256);
+    return o;
+  };
+  q.off_ctrl = take(sizeof(Ctrl));
+  q.off_idx = take(4 * (size_t)BT);
+  q.off_rloss = take(4 * (size_t)BT);
+  q.off_rz = take(4 * (size_t)BT);
+  q.off_racc = take(4 * (size_t)BT);
+  q.off_xc = take((size_t)R * q.Hp * q.esz);
+  q.off_stm = take(4 * (size_t)q.nvt * R);
+  q.off_sts = take(4 * (size_t)q.nvt * R);
+  q.off_sti = take(4 * (size_t)q.nvt * R);
+  q.off_tgt = take(4 * (size_t)R);
+  q.off_lse = take(4 * (size_t)R);
+  q.off_arow = take(4 * (size_t)R);
+  q.off_slab = take((size_t)R * q.Vp * q.esz);
+  q.total = off;
+  *p = q;
+  return true;
+}
+
+int64_t plan_rows_for_bytes(int64_t BT, int64_t H, int64_t V, int dt, size_t bytes) {
+  Plan p;
+  const int64_t cap = rup(BT, CHUNK_ALIGN);
+  if (!plan_layout(BT, H, V, dt, CHUNK_ALIGN, &p) || p.total > bytes) return 0;
+  // per-row cost from two layouts, then step down until it fits
+  Plan p2;
+  plan_layout(BT, H, V, dt, 2 * CHUNK_ALIGN, &p2);
+  const size_t per128 = p2.total - p.total;
+  int64_t R = CHUNK_ALIGN + (int64_t)((bytes - p.total) / (per128 ? per128 : 1)) * CHUNK_ALIGN;
+  if (R > cap) R = cap;
+  while (R > CHUNK_ALIGN) {
+    if (plan_layout(BT, H, V, dt, R, &p) && p.total <= bytes) break;
+    R -= CHUNK_ALIGN;
+  }
+  return R;
+}
+
+Work make_work(const Plan& p, void* ws, int32_t* user_status) {
+  char* b = (char*)ws;
+  Work w;
+  w.ctrl = (Ctrl*)(b + p.off_ctrl);
+  w.idx = (int*)(b + p.off_idx);
+  w.rloss = (float*)(b + p.off_rloss);
+  w.rz = (float*)(b + p.off_rz);
+  w.racc = (float*)(b + p.off_racc);
+  w.xc = b + p.off_xc;
+  w.stm = (float*)(b + p.off_stm);
+  w.sts = (float*)(b + p.off_sts);
+  w.sti = (int*)(b + p.off_sti);
+  w.tgt = (float*)(b + p.off_tgt);
+  w.lse = (float*)(b + p.off_lse);
+  w.arow = (float*)(b + p.off_arow);
+  w.slab = b + p.off_slab;
+  w.status = user_status ? (int*)user_status : &w.ctrl->status;
+  return w;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 132;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 132;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+static int32_t validate(const flce_args* x) {
+  if (!x) return FLCE_ERR_INVALID_ARG;
+  if (x->BT <= 0 || x->H <= 0 || x->V <= 0) return FLCE_ERR_INVALID_ARG;
+  if (x->BT > 0x7fffffffLL || x->H > 0x7fffffffLL || x->V > 0x7fffffffLL) return FLCE_ERR_INVALID_ARG;
+  if (x->in_dtype != FLCE_F32 && x->in_dtype != FLCE_BF16 && x->in_dtype != FLCE_F16)
+    return FLCE_ERR_INVALID_ARG;
+  if (x->reduction != FLCE_MEAN && x->reduction != FLCE_SUM && x->reduction != FLCE_NONE)
+    return FLCE_ERR_INVALID_ARG;
+  if (!x->X || !x->W || !x->targets || !x->loss || !x->workspace) return FLCE_ERR_INVALID_ARG;
+  if (!(x->z_loss_scale >= 0.0f) || x->z_loss_scale > 1e30f) return FLCE_ERR_INVALID_ARG;
+  if (x->want_dX && !x->dX) return FLCE_ERR_INVALID_ARG;
+  if (x->want_dW && !x->dW) return FLCE_ERR_INVALID_ARG;
+  if (x->want_dW && x->dW_dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED;
+  const int esz = dtype_size(x->in_dtype);
+  if (!aligned(x->X, 16) || !aligned(x->W, 16) || !aligned(x->workspace, 256)) return FLCE_ERR_INVALID_ARG;
+  if (x->want_dX && !aligned(x->dX, 16)) return FLCE_ERR_INVALID_ARG;
+  if (x->want_dW && !aligned(x->dW, 16)) return FLCE_ERR_INVALID_ARG;
+  if (x->bias && !aligned(x->bias, esz)) return FLCE_ERR_INVALID_ARG;
+  if (x->dbias && !aligned(x->dbias, 4)) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(x->targets, 8) || (x->pred && !aligned(x->pred, 8))) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(x->loss, 4) || (x->status && !aligned(x->status, 4))) return FLCE_ERR_INVALID_ARG;
+  return FLCE_OK;
+}
+
+}  // namespace flce
+
+using namespace flce;
+
+struct flce_profile {
+  std::vector<cudaEvent_t> ev;  // pairs: ev[2i] before, ev[2i+1] after launch i
+  std::vector<int> stage;       // stage of pair i
+  std::vector<int> nkern;       // kernels launched by pair i
+  size_t used = 0;              // pairs recorded since the last reset
+};
+
+namespace {
+// Record `launch` on `s`, bracketed by an event pair when profiling.
+template <typename F>
+cudaError_t staged(flce_profile* prof, int stage, int nkern, cudaStream_t s, F&& launch) {
+  if (!prof) return launch();
+  if (prof->used * 2 + 2 > prof->ev.size()) {
+    for (int i = 0; i < 2; ++i) {
+      cudaEvent_t e;
+      cudaError_t r = cudaEventCreate(&e);
+      if (r != cudaSuccess) return r;
+      prof->ev.push_back(e);
+    }
+    prof->stage.push_back(0);
+    prof->nkern.push_back(0);
+  }
+  const size_t i = prof->used++;
+  prof->stage[i] = stage;
+  prof->nkern[i] = nkern;
+  cudaError_t r = cudaEventRecord(prof->ev[2 * i], s);
+  if (r != cudaSuccess) return r;
+  r = launch();
+  if (r != cudaSuccess) return r;
+  return cudaEventRecord(prof->ev[2 * i + 1], s);
+}
+}  // namespace
+
+extern "C" flce_profile* flce_profile_create(void) { return new (std::nothrow) flce_profile(); }
+
+extern "C" void flce_profile_reset(flce_profile* prof) {
+  if (prof) prof->used = 0;
+}
+
+extern "C" void flce_profile_destroy(flce_profile* prof) {
+  if (!prof) return;
+  for (cudaEvent_t e : prof->ev) cudaEventDestroy(e);
+  delete prof;
+}
+
+extern "C" int32_t flce_profile_read(flce_profile* prof, float* ms, int32_t* launches, int32_t n) {
+  if (!prof || n < 0) return FLCE_ERR_INVALID_ARG;
+  const int m = n < FLCE_STAGE_COUNT ? n : FLCE_STAGE_COUNT;
+  for (int k = 0; k < m; ++k) {
+    if (ms) ms[k] = 0.0f;
+    if (launches) launches[k] = 0;
+  }
+  if (prof->used == 0) return FLCE_OK;
+  if (cudaEventSynchronize(prof->ev[2 * prof->used - 1]) != cudaSuccess) return FLCE_ERR_CUDA;
+  for (size_t i = 0; i < prof->used; ++i) {
+    float t = 0.0f;
+    if (cudaEventElapsedTime(&t, prof->ev[2 * i], prof->ev[2 * i + 1]) != cudaSuccess) return FLCE_ERR_CUDA;
+    const int k = prof->stage[i];
+    if (k < m) {
+      if (ms) ms[k] += t;
+      if (launches) launches[k] += prof->nkern[i];
+    }
+  }
+  return FLCE_OK;
+}
+
+extern "C" size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V, int32_t in_dtype,
+                                      size_t budget_bytes) {
+  if (BT <= 0 || H <= 0 || V <= 0) return 0;
+  if (in_dtype != FLCE_F32 && in_dtype != FLCE_BF16 && in_dtype != FLCE_F16) return 0;
+  const size_t budget = budget_bytes ? budget_bytes : DEFAULT_BUDGET;
+  const int64_t R = plan_rows_for_bytes(BT, H, V, in_dtype, budget);
+  if (R <= 0) return 0;
+  Plan p;
+  if (!plan_layout(BT, H, V, in_dtype, R, &p)) return 0;
+  return p.total;
+}
+
+extern "C" int64_t flce_chunk_rows(int64_t BT, int64_t H, int64_t V, int32_t in_dtype,
+                                   size_t workspace_bytes) {
+  if (BT <= 0 || H <= 0 || V <= 0) return 0;
+  if (in_dtype != FLCE_F32 && in_dtype != FLCE_BF16 && in_dtype != FLCE_F16) return 0;
+  return plan_rows_for_bytes(BT, H, V, in_dtype, workspace_bytes);
+}
+
+extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
+  const int32_t v = validate(x);
+  if (v != FLCE_OK) return v;
+  const int64_t R = plan_rows_for_bytes(x->BT, x->H, x->V, x->in_dtype, x->workspace_bytes);
+  if (R <= 0) return FLCE_ERR_WORKSPACE;
+  Plan p;
+  if (!plan_layout(x->BT, x->H, x->V, x->in_dtype, R, &p)) return FLCE_ERR_INVALID_ARG;
+
+  CallArgs a;
+  memset(&a, 0, sizeof(a));
+  a.BT = x->BT;
+  a.H = x->H;
+  a.V = x->V;
+  a.Hp = p.Hp;
+  a.Vp = p.Vp;
+  a.nvt = p.nvt;
+  a.R = p.R;
+  a.dt = x->in_dtype;
+  a.reduction = x->reduction;
+  a.z = x->z_loss_scale;
+  a.ignore_index = x->ignore_index;
+  a.X = x->X;
+  a.W = x->W;
+  a.bias = x->bias;
+  a.targets = x->targets;
+  a.grad_out = x->grad_out;
+  a.loss = x->loss;
+  a.z_loss = x->z_loss;
+  a.acc = x->acc;
+  a.lse_out = x->lse;
+  a.pred = x->pred;
+  a.n_labelled = x->n_labelled;
+  a.want_dX = x->want_dX ? 1 : 0;
+  a.want_dW = x->want_dW ? 1 : 0;
+  a.dX = a.want_dX ? x->dX : nullptr;
+  a.dW = a.want_dW ? (float*)x->dW : nullptr;
+  a.dbias = (a.want_dW && x->bias) ? (float*)x->dbias : nullptr;
+  a.w = make_work(p, x->workspace, x->status);
+  const uint32_t tmo_ms = x->wait_timeout_ms ? x->wait_timeout_ms : DEFAULT_TIMEOUT_MS;
+  a.timeout_ns = (uint64_t)tmo_ms * 1000000ull;
+  a.flags = x->flags;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool tc = !(x->flags & FLCE_FLAG_FORCE_SIMT) && tc_supported(a);
+  const bool grads = a.want_dX || a.want_dW;
+
+#define FLCE_TRY(expr)                          \
+  do {                                          \
+    if ((expr) != cudaSuccess) return FLCE_ERR_CUDA; \
+  } while (0)
+
+  flce_profile* prof = x->profile;
+  FLCE_TRY(cudaMemsetAsync(a.w.status, 0, sizeof(int), s));
+  FLCE_TRY(staged(prof, FLCE_STAGE_PROLOGUE, 2, s, [&] { return launch_prologue(a, s); }));
+  for (int k = 0; k < (int)p.kmax; ++k) {
+    FLCE_TRY(staged(prof, FLCE_STAGE_GATHER, 1, s, [&] { return launch_gather(a, k, s); }));
+    FLCE_TRY(staged(prof, FLCE_STAGE_FWD, 1, s,
+                    [&] { return tc ? launch_fwd_tc(a, k, s) : launch_fwd_simt(a, k, s); }));
+    FLCE_TRY(staged(prof, FLCE_STAGE_FINALIZE, 1, s, [&] { return launch_finalize(a, k, s); }));
+    if (grads) FLCE_TRY(staged(prof, FLCE_STAGE_GPASS, 1, s, [&] { return launch_gpass(a, k, s); }));
+    if (a.want_dX)
+      FLCE_TRY(staged(prof, FLCE_STAGE_DX, 1, s,
+                      [&] { return tc ? launch_dx_tc(a, k, s) : launch_dx_simt(a, k, s); }));
+    if (a.want_dW)
+      FLCE_TRY(staged(prof, FLCE_STAGE_DW, 1, s,
+                      [&] { return tc ? launch_dw_tc(a, k, s) : launch_dw_simt(a, k, s); }));
+  }
+  if (a.reduction != FLCE_NONE)
+    FLCE_TRY(staged(prof, FLCE_STAGE_REDUCE, 1, s, [&] { return launch_epilogue(a, s); }));
+#undef FLCE_TRY
+  return FLCE_OK;
+}
+
+extern "C" int32_t flce_get_status(const int32_t* status, const void* workspace, void* stream) {
+  const int32_t* word = status;
+  if (!word) {
+    if (!workspace) return FLCE_ERR_INVALID_ARG;
+    word = (const int32_t*)&((const Ctrl*)workspace)->status;  // Ctrl sits at offset 0
+  }
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FLCE_ERR_CUDA;
+  int32_t h = 0;
+  if (cudaMemcpy(&h, word, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (h & ST_TIMEOUT) return FLCE_ERR_TIMEOUT;
+  if (h & ST_TARGET_RANGE) return FLCE_ERR_TARGET_RANGE;
+  return FLCE_OK;
+}
+
+extern "C" const char* flce_status_string(int32_t code) {
+  switch (code) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_INVALID_ARG: return "FLCE_ERR_INVALID_ARG";
+    case FLCE_ERR_UNSUPPORTED: return "FLCE_ERR_UNSUPPORTED";
+    case FLCE_ERR_TARGET_RANGE: return "FLCE_ERR_TARGET_RANGE";
+    case FLCE_ERR_WORKSPACE: return "FLCE_ERR_WORKSPACE";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA";
+    case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT";
+    default: return "FLCE_ERR_UNKNOWN";
+  }
+}
+
+extern "C" int32_t flce_abi_version(void) { return FLCE_ABI_VERSION; }

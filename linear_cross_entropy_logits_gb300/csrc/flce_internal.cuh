@@ -1,0 +1,141 @@
+// Internal declarations shared by the translation units of libflce.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/flce.h"
+
+namespace flce {
+
+// Vocabulary tile of the forward statistics: every forward GEMM (tensor-core or SIMT)
+// produces one (max, sum-exp, argmax) triple per row and per VT columns.
+constexpr int VT = 256;
+constexpr int CHUNK_ALIGN = 128;   // row-chunk granularity (one tensor-core M tile)
+constexpr uint32_t DEFAULT_TIMEOUT_MS = 4000;
+constexpr size_t DEFAULT_BUDGET = (size_t)3 << 29;  // 1.5 GiB
+
+// Device status bits (1 << flce_status).
+constexpr int ST_TARGET_RANGE = 1 << FLCE_ERR_TARGET_RANGE;
+constexpr int ST_TIMEOUT = 1 << FLCE_ERR_TIMEOUT;
+
+// Per-call values produced on the device by the compaction kernel and read by every
+// later kernel of the call (no host synchronisation anywhere).
+struct Ctrl {
+  int n_lab;      // rows that enter the loss
+  int n_chunks;   // cdiv(n_lab, R)
+  int r_eff;      // rows per chunk, a multiple of 128, <= R, balanced over the chunks
+  int status;     // status word used when the caller passes none
+  float cbar;     // uniform gradient factor: g/n_lab (mean), g (sum), 1 (none)
+  float inv_n;    // 1/n_lab for mean (0 when n_lab == 0), 1 for sum
+  int pad[2];
+};
+
+// Workspace layout for one call; every region is 256-byte aligned.
+struct Plan {
+  int64_t BT, H, V;
+  int esz;       // bytes per input element
+  int64_t Hp;    // X-chunk row pitch (elements), multiple of 64
+  int64_t nvt;   // vocabulary tiles of VT columns
+  int64_t Vp;    // slab row pitch (elements) = nvt * VT
+  int64_t R;     // max rows per chunk (multiple of 128)
+  int64_t kmax;  // chunks the host enqueues = cdiv(BT, R)
+  size_t off_ctrl, off_idx, off_rloss, off_rz, off_racc;
+  size_t off_xc, off_stm, off_sts, off_sti, off_tgt, off_lse, off_arow, off_slab;
+  size_t total;
+};
+
+inline int dtype_size(int dt) { return dt == FLCE_F32 ? 4 : 2; }
+bool plan_layout(int64_t BT, int64_t H, int64_t V, int dt, int64_t R, Plan* p);
+int64_t plan_rows_for_bytes(int64_t BT, int64_t H, int64_t V, int dt, size_t bytes);
+
+// Views of the workspace regions handed to kernels.
+struct Work {
+  Ctrl* ctrl;
+  int* idx;        // [BT] labelled rows, ascending
+  float* rloss;    // [BT] per labelled row (compacted order) loss
+  float* rz;       // [BT] z-loss
+  float* racc;     // [BT] accuracy
+  void* xc;        // [R, Hp] gathered rows of the current chunk (zero past its end)
+  float* stm;      // [nvt, R] tile max; rewritten by finalize as the G multiplier
+  float* sts;      // [nvt, R] tile sum of exp(s - tile max)
+  int* sti;        // [nvt, R] tile argmax (lowest index)
+  float* tgt;      // [R] target logit
+  float* lse;      // [R] row logsumexp
+  float* arow;     // [R] per-row factor a_i (g_i for none, 1 otherwise)
+  void* slab;      // [R, Vp] exp(s - tile max), then G, in the input dtype
+  int* status;     // device status word
+};
+Work make_work(const Plan& p, void* ws, int32_t* user_status);
+
+// Everything a kernel of one call needs (passed by value).
+struct CallArgs {
+  int64_t BT, H, V, Hp, Vp, nvt, R;
+  int dt;
+  int reduction;
+  float z;
+  int64_t ignore_index;
+  const void* X;
+  const void* W;
+  const void* bias;
+  const int64_t* targets;
+  const float* grad_out;
+  float* loss;
+  float* z_loss;
+  float* acc;
+  float* lse_out;
+  int64_t* pred;
+  int32_t* n_labelled;
+  void* dX;
+  float* dW;
+  float* dbias;
+  int want_dX, want_dW;
+  Work w;
+  uint64_t timeout_ns;
+  uint32_t flags;
+};
+
+// ---- launchers (flce_kernels.cu) ----
+cudaError_t launch_prologue(const CallArgs& a, cudaStream_t s);          // compact + ignored rows
+cudaError_t launch_gather(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_fwd_simt(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_finalize(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_gpass(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_dx_simt(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_dw_simt(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_epilogue(const CallArgs& a, cudaStream_t s);          // reductions
+
+// ---- launchers (flce_tc.cu): tcgen05 tensor-core GEMMs, bf16/f16 only ----
+bool tc_supported(const CallArgs& a);
+cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s);
+
+int num_sms();
+
+// ---- device helpers ----
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <> __device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+template <> __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+
+// Chunk k covers compacted rows [row0, row0 + rows); false when chunk k is empty.
+__device__ __forceinline__ bool chunk_bounds(const Ctrl* c, int k, int& row0, int& rows) {
+  const int n = c->n_lab;
+  if (k >= c->n_chunks) return false;
+  row0 = k * c->r_eff;
+  rows = n - row0 < c->r_eff ? n - row0 : c->r_eff;
+  return rows > 0;
+}
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+}  // namespace flce

@@ -1,0 +1,617 @@
+// Row compaction, per-chunk gather, forward-statistics merge, gradient formation,
+// reductions, and the SIMT (fp32 FMA) GEMMs used for fp32 inputs.
+//
+// The row-skipping idea follows "Liger-Kernel PR #1554: skip ignore_index rows"
+// (Summary): rows whose target is ignore_index take no part in any product. Here the
+// compaction is exact (every ignored row is removed, not only whole chunks) and happens
+// on the device, so no host synchronisation is needed.
+#include "flce_internal.cuh"
+
+#include <math.h>
+
+namespace flce {
+
+namespace {
+
+__host__ __device__ inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t rup64(int64_t a, int64_t b) { return cdiv64(a, b) * b; }
+
+__device__ __forceinline__ bool is_labelled(int64_t t, int64_t ignore_index, int64_t V) {
+  return t != ignore_index && t >= 0 && t < V;
+}
+
+// ---------------------------------------------------------------------------------------
+// Compaction: a stable list of labelled rows (ascending), the labelled count, the chunk
+// geometry and the uniform gradient factor. One block; BT is scanned 1024 rows at a time.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_compact(const __grid_constant__ CallArgs a) {
+  __shared__ int warp_incl[32];
+  __shared__ int s_base;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == 0) s_base = 0;
+  int bad = 0;
+  __syncthreads();
+  for (int64_t b0 = 0; b0 < a.BT; b0 += 1024) {
+    const int64_t i = b0 + tid;
+    int lab = 0;
+    if (i < a.BT) {
+      const int64_t t = a.targets[i];
+      if (t != a.ignore_index) {
+        if (t >= 0 && t < a.V) lab = 1;
+        else bad = 1;
+      }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, lab);
+    const int wpre = __popc(m & ((1u << lane) - 1u));
+    if (lane == 0) warp_incl[wid] = __popc(m);
+    __syncthreads();
+    if (wid == 0) {
+      int v = warp_incl[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      warp_incl[lane] = v;
+    }
+    __syncthreads();
+    const int base = s_base;
+    const int wbase = wid ? warp_incl[wid - 1] : 0;
+    if (lab) a.w.idx[base + wbase + wpre] = (int)i;
+    __syncthreads();
+    if (tid == 0) s_base = base + warp_incl[31];
+    __syncthreads();
+  }
+  if (bad) atomicOr(a.w.status, ST_TARGET_RANGE);
+  if (tid == 0) {
+    // Fields are written one by one: the status word may live inside Ctrl and other
+    // threads may be OR-ing into it.
+    const int n = s_base;
+    Ctrl* c = a.w.ctrl;
+    const int nch = n > 0 ? (int)cdiv64(n, a.R) : 0;
+    c->n_lab = n;
+    c->n_chunks = nch;
+    c->r_eff = n > 0 ? (int)rup64(cdiv64(n, nch), CHUNK_ALIGN) : 0;
+    float g = 1.0f;
+    if (a.reduction != FLCE_NONE && a.grad_out != nullptr) g = a.grad_out[0];
+    if (a.reduction == FLCE_MEAN) {
+      c->cbar = n > 0 ? g / (float)n : 0.0f;
+      c->inv_n = n > 0 ? 1.0f / (float)n : 0.0f;
+    } else if (a.reduction == FLCE_SUM) {
+      c->cbar = g;
+      c->inv_n = 1.0f;
+    } else {
+      c->cbar = 1.0f;
+      c->inv_n = 1.0f;
+    }
+    if (a.n_labelled) *a.n_labelled = n;
+  }
+}
+
+// Ignored rows: per-token outputs (PR #1554, Details item 1) and a zero dX row.
+__global__ void __launch_bounds__(256) k_ignored(const __grid_constant__ CallArgs a) {
+  for (int64_t i = blockIdx.x; i < a.BT; i += gridDim.x) {
+    const int64_t t = a.targets[i];
+    if (is_labelled(t, a.ignore_index, a.V)) continue;
+    if (threadIdx.x == 0) {
+      if (a.reduction == FLCE_NONE) {
+        a.loss[i] = 0.0f;
+        if (a.z_loss) a.z_loss[i] = 0.0f;
+        if (a.acc) a.acc[i] = 0.0f;
+      }
+      if (a.lse_out) a.lse_out[i] = 0.0f;
+      if (a.pred) a.pred[i] = -1;
+    }
+    if (a.want_dX) {
+      const int esz = a.dt == FLCE_F32 ? 4 : 2;
+      const int64_t bytes = a.H * esz;
+      char* row = (char*)a.dX + i * bytes;
+      if ((bytes & 15) == 0) {
+        uint4* r4 = (uint4*)row;
+        for (int64_t j = threadIdx.x; j < bytes / 16; j += blockDim.x) r4[j] = make_uint4(0, 0, 0, 0);
+      } else {
+        for (int64_t j = threadIdx.x; j < bytes; j += blockDim.x) row[j] = 0;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Gather the chunk's labelled rows of X into the dense chunk buffer; rows past the chunk
+// end (up to the next multiple of 128) and columns past H are zero, so that no stale or
+// uninitialised value ever enters a GEMM.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_gather(const __grid_constant__ CallArgs a, int chunk) {
+  int row0, rows;
+  if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  const int lim = (int)rup64(rows, CHUNK_ALIGN);
+  const int esz = a.dt == FLCE_F32 ? 4 : 2;
+  const int64_t src_bytes = a.H * esz, dst_bytes = a.Hp * esz;
+  for (int r = blockIdx.x; r < lim; r += gridDim.x) {
+    char* dst = (char*)a.w.xc + (int64_t)r * dst_bytes;
+    if (r < rows) {
+      const char* src = (const char*)a.X + (int64_t)a.w.idx[row0 + r] * src_bytes;
+      if ((src_bytes & 15) == 0) {
+        const uint4* s4 = (const uint4*)src;
+        uint4* d4 = (uint4*)dst;
+        for (int64_t j = threadIdx.x; j < src_bytes / 16; j += blockDim.x) d4[j] = s4[j];
+      } else {
+        for (int64_t j = threadIdx.x; j < src_bytes; j += blockDim.x) dst[j] = src[j];
+      }
+      for (int64_t j = src_bytes + threadIdx.x; j < dst_bytes; j += blockDim.x) dst[j] = 0;
+    } else {
+      uint4* d4 = (uint4*)dst;
+      for (int64_t j = threadIdx.x; j < dst_bytes / 16; j += blockDim.x) d4[j] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Finalize: merge the per-tile (max, sum-exp, argmax) triples of each row in ascending
+// tile order, giving lse, loss, z-loss, prediction and accuracy; then turn each tile max
+// into the multiplier that maps the stored exp(s - tile max) to the row's gradient
+// a_i (1 + 2 z lse) exp(s - lse).
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) k_finalize(const __grid_constant__ CallArgs a, int chunk) {
+  int row0, rows;
+  if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  const int64_t R = a.R;
+  const int nvt = (int)a.nvt;
+  float* stm = a.w.stm;
+  const float* sts = a.w.sts;
+  const int* sti = a.w.sti;
+
+  float M = -INFINITY;
+  int am = 0;
+  for (int t = 0; t < nvt; ++t) {
+    const float m = stm[t * R + r];
+    if (m > M) {
+      M = m;
+      am = sti[t * R + r];
+    }
+  }
+  float S = 0.0f;
+  for (int t = 0; t < nvt; ++t) S += sts[t * R + r] * expf(stm[t * R + r] - M);
+  const float lse = M + logf(S);
+
+  const int row = a.w.idx[row0 + r];
+  const int64_t tg = a.targets[row];
+  const float zl = a.z * lse * lse;
+  const float loss = (lse - a.w.tgt[r]) + zl;
+  const float accv = ((int64_t)am == tg) ? 1.0f : 0.0f;
+  float ar = 1.0f;
+  if (a.reduction == FLCE_NONE && a.grad_out != nullptr) ar = a.grad_out[row];
+  const float f = ar * (1.0f + 2.0f * a.z * lse);
+  for (int t = 0; t < nvt; ++t) stm[t * R + r] = f * expf(stm[t * R + r] - lse);
+  a.w.lse[r] = lse;
+  a.w.arow[r] = ar;
+
+  if (a.lse_out) a.lse_out[row] = lse;
+  if (a.pred) a.pred[row] = am;
+  if (a.reduction == FLCE_NONE) {
+    a.loss[row] = loss;
+    if (a.z_loss) a.z_loss[row] = zl;
+    if (a.acc) a.acc[row] = accv;
+  }
+  a.w.rloss[row0 + r] = loss;
+  a.w.rz[row0 + r] = zl;
+  a.w.racc[row0 + r] = accv;
+}
+
+// ---------------------------------------------------------------------------------------
+// Gradient formation: G[r, v] = mult[r, tile(v)] * e[r, v] - a_r [v == t_r], in place in
+// the slab; rows past the chunk end up to the next multiple of 64 are zeroed (the dW GEMM
+// reduces over them). With dbias wanted, one block owns a whole column strip and adds its
+// column sums to dbias in a fixed order.
+// ---------------------------------------------------------------------------------------
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+  __device__ static void load(const __nv_bfloat16* p, float (&f)[8]) {
+    const uint4 u = *(const uint4*)p;
+    const __nv_bfloat162* h = (const __nv_bfloat162*)&u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = __bfloat1622float2(h[j]);
+      f[2 * j] = x.x;
+      f[2 * j + 1] = x.y;
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&f)[8]) {
+    uint4 u;
+    __nv_bfloat162* h = (__nv_bfloat162*)&u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+    *(uint4*)p = u;
+  }
+};
+template <> struct Vec8<__half> {
+  __device__ static void load(const __half* p, float (&f)[8]) {
+    const uint4 u = *(const uint4*)p;
+    const __half2* h = (const __half2*)&u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = __half22float2(h[j]);
+      f[2 * j] = x.x;
+      f[2 * j + 1] = x.y;
+    }
+  }
+  __device__ static void store(__half* p, const float (&f)[8]) {
+    uint4 u;
+    __half2* h = (__half2*)&u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+    *(uint4*)p = u;
+  }
+};
+template <> struct Vec8<float> {
+  __device__ static void load(const float* p, float (&f)[8]) {
+    const float4 x = *(const float4*)p, y = *(const float4*)(p + 4);
+    f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+    f[4] = y.x; f[5] = y.y; f[6] = y.z; f[7] = y.w;
+  }
+  __device__ static void store(float* p, const float (&f)[8]) {
+    *(float4*)p = make_float4(f[0], f[1], f[2], f[3]);
+    *(float4*)(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_gpass(const __grid_constant__ CallArgs a, int chunk,
+                                               int rows_per_block, int do_dbias) {
+  int row0, rows;
+  if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  const int t = blockIdx.x;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int rlim = (int)rup64(rows, 64);
+  const int rb0 = blockIdx.y * rows_per_block;
+  const int rb1 = min(rb0 + rows_per_block, rlim);
+  const int64_t c0 = (int64_t)t * VT + tx * 8;
+  const int64_t R = a.R;
+  T* slab = (T*)a.w.slab;
+  float cs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int r = rb0 + ty; r < rb1; r += 8) {
+    T* p = slab + (int64_t)r * a.Vp + c0;
+    float f[8];
+    if (r < rows) {
+      const float m = a.w.stm[t * R + r];
+      const float ar = a.w.arow[r];
+      const int64_t tg = a.targets[a.w.idx[row0 + r]];
+      Vec8<T>::load(p, f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float g = m * f[j];
+        if (c0 + j == tg) g -= ar;
+        f[j] = g;
+        cs[j] += g;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = 0.0f;
+    }
+    Vec8<T>::store(p, f);
+  }
+  if (do_dbias) {
+    __shared__ float red[8][VT];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) red[ty][tx * 8 + j] = cs[j];
+    __syncthreads();
+    const float cb = a.w.ctrl->cbar;
+    for (int c = threadIdx.x; c < VT; c += blockDim.x) {
+      float s = 0.0f;
+#pragma unroll
+      for (int y = 0; y < 8; ++y) s += red[y][c];
+      const int64_t v = (int64_t)t * VT + c;
+      if (v < a.V) a.dbias[v] += cb * s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Final reductions (mean/sum) of loss, z-loss and accuracy over the labelled rows, in a
+// fixed order (deterministic).
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_reduce(const __grid_constant__ CallArgs a) {
+  __shared__ double red[3][32];
+  const int n = a.w.ctrl->n_lab;
+  double s0 = 0.0, s1 = 0.0, s2 = 0.0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    s0 += a.w.rloss[i];
+    s1 += a.w.rz[i];
+    s2 += a.w.racc[i];
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s0 += __shfl_down_sync(0xffffffffu, s0, o);
+    s1 += __shfl_down_sync(0xffffffffu, s1, o);
+    s2 += __shfl_down_sync(0xffffffffu, s2, o);
+  }
+  if (lane == 0) {
+    red[0][wid] = s0;
+    red[1][wid] = s1;
+    red[2][wid] = s2;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    s0 = red[0][lane];
+    s1 = red[1][lane];
+    s2 = red[2][lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s0 += __shfl_down_sync(0xffffffffu, s0, o);
+      s1 += __shfl_down_sync(0xffffffffu, s1, o);
+      s2 += __shfl_down_sync(0xffffffffu, s2, o);
+    }
+    if (lane == 0) {
+      double d = 1.0;
+      if (a.reduction == FLCE_MEAN) d = n > 0 ? (double)n : 0.0;
+      const double q0 = d > 0.0 ? s0 / d : 0.0, q1 = d > 0.0 ? s1 / d : 0.0, q2 = d > 0.0 ? s2 / d : 0.0;
+      a.loss[0] = (float)q0;
+      if (a.z_loss) a.z_loss[0] = (float)q1;
+      if (a.acc) a.acc[0] = (float)q2;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// SIMT forward: a 16-row x 256-column logit tile per block, fp32 FMA over H, then the
+// same per-tile statistics and stored exp(s - tile max) as the tensor-core forward.
+// ---------------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) k_fwd_simt(const __grid_constant__ CallArgs a, int chunk) {
+  int row0, rows;
+  if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  const int mb = blockIdx.x;
+  if (mb * 16 >= rows) return;
+  const int t = blockIdx.y;
+  __shared__ float As[16][33];
+  __shared__ float Bs[VT * 33];
+  const int tid = threadIdx.x;
+  const T* xc = (const T*)a.w.xc;
+  const T* W = (const T*)a.W;
+  const int64_t H = a.H, V = a.V;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+  for (int64_t k0 = 0; k0 < H; k0 += 32) {
+    for (int e = tid; e < 16 * 32; e += 256) {
+      const int rr = e >> 5, kk = e & 31;
+      const int64_t gk = k0 + kk;
+      As[rr][kk] = gk < H ? to_f<T>(xc[(int64_t)(mb * 16 + rr) * a.Hp + gk]) : 0.0f;
+    }
+    for (int e = tid; e < VT * 32; e += 256) {
+      const int nn = e >> 5, kk = e & 31;
+      const int64_t v = (int64_t)t * VT + nn, gk = k0 + kk;
+      Bs[nn * 33 + kk] = (v < V && gk < H) ? to_f<T>(W[v * H + gk]) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      const float b = Bs[tid * 33 + kk];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] = fmaf(As[i][kk], b, acc[i]);
+    }
+    __syncthreads();
+  }
+  // stage the tile (with bias) in shared memory: Ss[i][j] at Bs[i * 257 + j]
+  float* Ss = Bs;
+  {
+    const int64_t v = (int64_t)t * VT + tid;
+    float b = 0.0f;
+    if (a.bias != nullptr && v < V) b = to_f<T>(((const T*)a.bias)[v]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Ss[i * 257 + tid] = acc[i] + b;
+  }
+  __syncthreads();
+  const int lane = tid & 31, warp = tid >> 5;
+  T* slab = (T*)a.w.slab;
+  for (int i = warp; i < 16; i += 8) {
+    const int rr = mb * 16 + i;
+    if (rr >= rows) continue;
+    const int64_t tg = a.targets[a.w.idx[row0 + rr]];
+    float mx = -INFINITY;
+    int ai = t * VT;
+    float tl = 0.0f;
+    bool ht = false;
+    for (int j = lane; j < VT; j += 32) {
+      const int64_t v = (int64_t)t * VT + j;
+      if (v < V) {
+        const float s = Ss[i * 257 + j];
+        if (s > mx) {
+          mx = s;
+          ai = (int)v;
+        }
+        if (v == tg) {
+          tl = s;
+          ht = true;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, ai, o);
+      if (om > mx || (om == mx && oi < ai)) {
+        mx = om;
+        ai = oi;
+      }
+    }
+    float sum = 0.0f;
+    for (int j = lane; j < VT; j += 32) {
+      const int64_t v = (int64_t)t * VT + j;
+      const float e = v < V ? expf(Ss[i * 257 + j] - mx) : 0.0f;
+      sum += e;
+      slab[(int64_t)rr * a.Vp + v] = from_f<T>(e);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const unsigned hb = __ballot_sync(0xffffffffu, ht);
+    if (hb) tl = __shfl_sync(0xffffffffu, tl, __ffs(hb) - 1);
+    if (lane == 0) {
+      a.w.stm[t * a.R + rr] = mx;
+      a.w.sts[t * a.R + rr] = sum;
+      a.w.sti[t * a.R + rr] = ai;
+      if (hb) a.w.tgt[rr] = tl;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// SIMT GEMMs of the backward, 64x64 output tiles, fp32 FMA.
+//   MODE 0 (dX): dX[idx[r]] = cbar * sum_v G[r, v] W[v, :]        (M = rows, K = V)
+//   MODE 1 (dW): dW[v]     += cbar * sum_r G[r, v] Xc[r, :]       (M = V, K = rows)
+// ---------------------------------------------------------------------------------------
+template <typename T, int MODE>
+__global__ void __launch_bounds__(256) k_gemm_simt(const __grid_constant__ CallArgs a, int chunk) {
+  int row0, rows;
+  if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  const int64_t M = MODE == 0 ? rows : a.V;
+  const int64_t N = a.H;
+  const int64_t K = MODE == 0 ? a.V : rows;
+  const int64_t m0 = (int64_t)blockIdx.y * 64, n0 = (int64_t)blockIdx.x * 64;
+  if (m0 >= M) return;
+  __shared__ float As[16][68];
+  __shared__ float Bs[16][68];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const T* G = (const T*)a.w.slab;
+  const T* Bsrc = MODE == 0 ? (const T*)a.W : (const T*)a.w.xc;
+  const int64_t ldb = MODE == 0 ? a.H : a.Hp;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  for (int64_t k0 = 0; k0 < K; k0 += 16) {
+    for (int e = tid; e < 1024; e += 256) {
+      int mm, kk;
+      if (MODE == 0) {
+        mm = e >> 4;
+        kk = e & 15;
+      } else {
+        kk = e >> 6;
+        mm = e & 63;
+      }
+      const int64_t gm = m0 + mm, gk = k0 + kk;
+      float v = 0.0f;
+      if (gm < M && gk < K) v = MODE == 0 ? to_f<T>(G[gm * a.Vp + gk]) : to_f<T>(G[gk * a.Vp + gm]);
+      As[kk][mm] = v;
+    }
+    for (int e = tid; e < 1024; e += 256) {
+      const int kk = e >> 6, nn = e & 63;
+      const int64_t gk = k0 + kk, gn = n0 + nn;
+      Bs[kk][nn] = (gk < K && gn < N) ? to_f<T>(Bsrc[gk * ldb + gn]) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  const float cb = a.w.ctrl->cbar;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t n = n0 + tx * 4 + j;
+      if (n >= N) continue;
+      if (MODE == 0) {
+        const int64_t orow = a.w.idx[row0 + m];
+        ((T*)a.dX)[orow * a.H + n] = from_f<T>(cb * acc[i][j]);
+      } else {
+        a.dW[m * a.H + n] += cb * acc[i][j];
+      }
+    }
+  }
+}
+
+template <typename T>
+cudaError_t gpass_t(const CallArgs& a, int chunk, cudaStream_t s) {
+  const bool dbias = a.want_dW && a.bias != nullptr && a.dbias != nullptr;
+  const int rlim = (int)rup64(a.R, 64);
+  int rpb = dbias ? rlim : 256;
+  const int ry = (int)cdiv64(rlim, rpb);
+  dim3 grid((unsigned)a.nvt, (unsigned)ry);
+  k_gpass<T><<<grid, 256, 0, s>>>(a, chunk, rpb, dbias ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prologue(const CallArgs& a, cudaStream_t s) {
+  k_compact<<<1, 1024, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = a.BT < 8LL * num_sms() ? a.BT : 8LL * num_sms();
+  k_ignored<<<(unsigned)blocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const CallArgs& a, int chunk, cudaStream_t s) {
+  const int64_t blocks = a.R < 4LL * num_sms() ? a.R : 4LL * num_sms();
+  k_gather<<<(unsigned)blocks, 256, 0, s>>>(a, chunk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const CallArgs& a, int chunk, cudaStream_t s) {
+  k_finalize<<<(unsigned)cdiv64(a.R, 128), 128, 0, s>>>(a, chunk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gpass(const CallArgs& a, int chunk, cudaStream_t s) {
+  switch (a.dt) {
+    case FLCE_BF16: return gpass_t<__nv_bfloat16>(a, chunk, s);
+    case FLCE_F16: return gpass_t<__half>(a, chunk, s);
+    default: return gpass_t<float>(a, chunk, s);
+  }
+}
+
+cudaError_t launch_fwd_simt(const CallArgs& a, int chunk, cudaStream_t s) {
+  dim3 grid((unsigned)cdiv64(a.R, 16), (unsigned)a.nvt);
+  switch (a.dt) {
+    case FLCE_BF16: k_fwd_simt<__nv_bfloat16><<<grid, 256, 0, s>>>(a, chunk); break;
+    case FLCE_F16: k_fwd_simt<__half><<<grid, 256, 0, s>>>(a, chunk); break;
+    default: k_fwd_simt<float><<<grid, 256, 0, s>>>(a, chunk); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dx_simt(const CallArgs& a, int chunk, cudaStream_t s) {
+  dim3 grid((unsigned)cdiv64(a.H, 64), (unsigned)cdiv64(a.R, 64));
+  switch (a.dt) {
+    case FLCE_BF16: k_gemm_simt<__nv_bfloat16, 0><<<grid, 256, 0, s>>>(a, chunk); break;
+    case FLCE_F16: k_gemm_simt<__half, 0><<<grid, 256, 0, s>>>(a, chunk); break;
+    default: k_gemm_simt<float, 0><<<grid, 256, 0, s>>>(a, chunk); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_simt(const CallArgs& a, int chunk, cudaStream_t s) {
+  dim3 grid((unsigned)cdiv64(a.H, 64), (unsigned)cdiv64(a.V, 64));
+  switch (a.dt) {
+    case FLCE_BF16: k_gemm_simt<__nv_bfloat16, 1><<<grid, 256, 0, s>>>(a, chunk); break;
+    case FLCE_F16: k_gemm_simt<__half, 1><<<grid, 256, 0, s>>>(a, chunk); break;
+    default: k_gemm_simt<float, 1><<<grid, 256, 0, s>>>(a, chunk); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_epilogue(const CallArgs& a, cudaStream_t s) {
+  if (a.reduction == FLCE_NONE) return cudaSuccess;
+  k_reduce<<<1, 1024, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

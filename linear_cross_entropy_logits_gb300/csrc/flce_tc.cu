@@ -1,0 +1,620 @@
+// Tensor-core GEMMs of the fused linear cross entropy for sm_103a: tcgen05.mma with
+// fp32 accumulators in tensor memory (TMEM), operands staged in shared memory by TMA
+// (cp.async.bulk.tensor, 128-byte swizzle), warp-specialised and persistent.
+//
+// One kernel template serves the three products of the method:
+//   FWD: S = Xc W^T (K = H). The epilogue never writes S: per row and per 256-column
+//        vocabulary tile it keeps the max, the sum of exp(s - max), the lowest-index
+//        argmax and the target logit, and stores exp(s - max) (in the input dtype) into
+//        the chunk slab, from which the gradient is formed once the row's lse is known.
+//   DX:  dX[idx] = cbar * G W (K = V), written through the compaction index.
+//   DW:  dW += cbar * G^T Xc (K = chunk rows), read-modify-write of the fp32 destination
+//        by the single CTA that owns each tile (deterministic, no atomics).
+// The three products are the logits, grad_input and grad_weight GEMMs that the pages'
+// op runs in its forward ("Liger-Kernel PR #1554: skip ignore_index rows", Summary); dW is
+// accumulated straight into the caller's buffer with no [V,H] temporary ("Reduce FLCE
+// weight-gradient allocation overhead across FP16, BF16, and FP32", Proposed direction).
+//
+// Block layout (192 threads, one CTA per SM):
+//   warp 0        TMA producer (one thread)
+//   warp 1        TMEM allocator + MMA issuer (one thread)
+//   warps 2..5    epilogue; warp w reads TMEM lanes 32*(w%4) .. +31
+// Tiles: 128 (M) x 256 (N) x 64 (K) per stage, 4 stages (192 KB), two 256-column TMEM
+// accumulators so the epilogue of one tile overlaps the mainloop of the next.
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records FLCE_ERR_TIMEOUT,
+// waits for its own copies and MMAs in flight, frees TMEM and returns.
+#include <cuda.h>
+#include <mutex>
+
+#include "flce_internal.cuh"
+
+namespace flce {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;               // 16 KB
+constexpr int B_BYTES = BN * BK * 2;               // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 48 KB
+constexpr int BOX_BYTES = 64 * 64 * 2;             // one 64x64 MN-major TMA box (8 KB)
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int NUM_BARS = 2 * STAGES + 5;           // full, empty, tfull[2], tempty[2], drain
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+enum Mode { FWD = 0, DX = 1, DW = 2 };
+
+__host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase of `bar` with parity `parity`. Gives up (returning false)
+// when another role of the CTA has aborted (if honor_abort) or after timeout_ns, in which
+// case it raises the CTA abort flag and the device status bit.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, uint64_t timeout_ns, bool honor_abort) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try(bar, parity)) return true;
+    if (honor_abort && *abort_flag) return false;
+    if (gtimer() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(status, ST_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), sm100 version bit.
+//   K-major operand:  rows of 128 B (64 elements along K), 8-row atoms of 1024 B;
+//                     SBO = 1024 (next 8 rows), LBO unused; K steps of 16 = +32 B.
+//   MN-major operand: 64 MN-elements per 128-B row, one row per K index, 8-row atoms of
+//                     1024 B; SBO = 1024 (next 8 K indices), LBO = 8192 (next 64-wide
+//                     MN block = next 64x64 TMA box); K steps of 16 = +2048 B.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A/B format, majors,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+template <int MODE, typename T>
+__device__ __forceinline__ constexpr uint32_t make_idesc() {
+  constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  constexpr uint32_t a_mn = MODE == DW ? 1u : 0u;
+  constexpr uint32_t b_mn = MODE == FWD ? 0u : 1u;
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | (b_mn << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane; waits for completion so the
+// registers are valid on return.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+template <typename T> __device__ __forceinline__ uint32_t pack2(float x, float y);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float x, float y) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  return *(uint32_t*)&h;
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float x, float y) {
+  __half2 h = __floats2half2_rn(x, y);
+  return *(uint32_t*)&h;
+}
+
+// ------------------------------------------------------------------ tile space
+struct TileSpace {
+  int mt, nt, nkb;
+};
+template <int MODE>
+__device__ __forceinline__ TileSpace tile_space(const CallArgs& a, int rows) {
+  TileSpace t;
+  if (MODE == FWD) {
+    t.mt = cdiv(rows, BM);
+    t.nt = (int)a.nvt;
+    t.nkb = cdiv((int)a.H, BK);
+  } else if (MODE == DX) {
+    t.mt = cdiv(rows, BM);
+    t.nt = cdiv((int)a.H, BN);
+    t.nkb = cdiv((int)a.V, BK);
+  } else {
+    t.mt = cdiv((int)a.V, BM);
+    t.nt = cdiv((int)a.H, BN);
+    t.nkb = cdiv(rows, BK);
+  }
+  return t;
+}
+// FWD walks m fastest (the CTAs in flight share W tiles); DX and DW walk n fastest (the
+// CTAs in flight share the slab rows / columns).
+template <int MODE>
+__device__ __forceinline__ void tile_coords(const TileSpace& ts, int tile, int& m, int& n) {
+  if (MODE == FWD) {
+    m = tile % ts.mt;
+    n = tile / ts.mt;
+  } else {
+    n = tile % ts.nt;
+    m = tile / ts.nt;
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+template <typename T>
+__device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int rows, int m, int n,
+                                             uint32_t taddr, int q, int lane) {
+  const int rr = m * BM + q * 32 + lane;  // row within the chunk
+  const bool valid = rr < rows;
+  const int V = (int)a.V;
+  int64_t tg = -1;
+  if (valid) tg = a.targets[a.w.idx[row0 + rr]];
+  const int v0 = n * VT;
+  const T* bias = (const T*)a.bias;
+  float mx = -INFINITY, tl = 0.0f;
+  int ai = v0;
+  bool ht = false;
+#pragma unroll 1
+  for (int cc = 0; cc < BN / 32; ++cc) {
+    uint32_t r[32];
+    tmem_ld32(taddr + cc * 32, r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int v = v0 + cc * 32 + j;
+      float s = __uint_as_float(r[j]);
+      if (v < V) {
+        if (bias != nullptr) s += to_f<T>(bias[v]);
+        if (s > mx) {
+          mx = s;
+          ai = v;
+        }
+        if (v == tg) {
+          tl = s;
+          ht = true;
+        }
+      }
+    }
+  }
+  float sum = 0.0f;
+  T* srow = (T*)a.w.slab + (int64_t)(valid ? rr : 0) * a.Vp + v0;
+  const float mxl = mx * LOG2E;
+#pragma unroll 1
+  for (int cc = 0; cc < BN / 32; ++cc) {
+    uint32_t r[32];
+    tmem_ld32(taddr + cc * 32, r);
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const int v = v0 + cc * 32 + j;
+      float s0 = __uint_as_float(r[j]), s1 = __uint_as_float(r[j + 1]);
+      float e0 = 0.0f, e1 = 0.0f;
+      if (v < V) {
+        if (bias != nullptr) s0 += to_f<T>(bias[v]);
+        e0 = exp2f(fmaf(s0, LOG2E, -mxl));
+      }
+      if (v + 1 < V) {
+        if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
+        e1 = exp2f(fmaf(s1, LOG2E, -mxl));
+      }
+      sum += e0 + e1;
+      pk[j / 2] = pack2<T>(e0, e1);
+    }
+    if (valid) {
+      uint4* dst = (uint4*)(srow + cc * 32);
+      dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+      dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+    }
+  }
+  if (valid) {
+    const int64_t o = (int64_t)n * a.R + rr;
+    a.w.stm[o] = mx;
+    a.w.sts[o] = sum;
+    a.w.sti[o] = ai;
+    if (ht) a.w.tgt[rr] = tl;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void epilogue_dx(const CallArgs& a, int row0, int rows, int m, int n,
+                                            uint32_t taddr, int q, int lane, float cb) {
+  const int rr = m * BM + q * 32 + lane;
+  const bool valid = rr < rows;
+  const int H = (int)a.H;
+  const int64_t orow = valid ? (int64_t)a.w.idx[row0 + rr] : 0;
+  T* drow = (T*)a.dX + orow * a.H;
+#pragma unroll 1
+  for (int cc = 0; cc < BN / 32; ++cc) {
+    uint32_t r[32];
+    tmem_ld32(taddr + cc * 32, r);
+    const int h0 = n * BN + cc * 32;
+    if (valid && h0 < H) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        if (h0 + g * 8 < H) {
+          uint4 u;
+          u.x = pack2<T>(cb * __uint_as_float(r[g * 8 + 0]), cb * __uint_as_float(r[g * 8 + 1]));
+          u.y = pack2<T>(cb * __uint_as_float(r[g * 8 + 2]), cb * __uint_as_float(r[g * 8 + 3]));
+          u.z = pack2<T>(cb * __uint_as_float(r[g * 8 + 4]), cb * __uint_as_float(r[g * 8 + 5]));
+          u.w = pack2<T>(cb * __uint_as_float(r[g * 8 + 6]), cb * __uint_as_float(r[g * 8 + 7]));
+          *(uint4*)(drow + h0 + g * 8) = u;
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void epilogue_dw(const CallArgs& a, int m, int n, uint32_t taddr, int q,
+                                            int lane, float cb) {
+  const int v = m * BM + q * 32 + lane;
+  const bool valid = v < (int)a.V;
+  const int H = (int)a.H;
+  float* wrow = a.dW + (int64_t)(valid ? v : 0) * a.H;
+#pragma unroll 1
+  for (int cc = 0; cc < BN / 32; ++cc) {
+    uint32_t r[32];
+    tmem_ld32(taddr + cc * 32, r);
+    const int h0 = n * BN + cc * 32;
+    if (valid && h0 < H) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        if (h0 + g * 8 < H) {
+          float4* p = (float4*)(wrow + h0 + g * 8);
+          float4 x0 = p[0], x1 = p[1];
+          x0.x = fmaf(cb, __uint_as_float(r[g * 8 + 0]), x0.x);
+          x0.y = fmaf(cb, __uint_as_float(r[g * 8 + 1]), x0.y);
+          x0.z = fmaf(cb, __uint_as_float(r[g * 8 + 2]), x0.z);
+          x0.w = fmaf(cb, __uint_as_float(r[g * 8 + 3]), x0.w);
+          x1.x = fmaf(cb, __uint_as_float(r[g * 8 + 4]), x1.x);
+          x1.y = fmaf(cb, __uint_as_float(r[g * 8 + 5]), x1.y);
+          x1.z = fmaf(cb, __uint_as_float(r[g * 8 + 6]), x1.z);
+          x1.w = fmaf(cb, __uint_as_float(r[g * 8 + 7]), x1.w);
+          p[0] = x0;
+          p[1] = x1;
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int MODE, typename T>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CallArgs a, const int chunk) {
+  int row0 = 0, rows = 0;
+  if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  const TileSpace ts = tile_space<MODE>(a, rows);
+  const int ntiles = ts.mt * ts.nt;
+  if ((int)blockIdx.x >= ntiles || ts.nkb <= 0) return;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = (uint32_t*)(bars + NUM_BARS);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  auto tempty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 + s); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* status = a.w.status;
+  const uint64_t tmo = a.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(tfull_bar(s), 1);
+      mbar_init(tempty_bar(s), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t armed = 0, last_par = 0;
+      bool ok = true;
+      const bool stall = (a.flags & FLCE_FLAG_DEBUG_STALL) && MODE == FWD;
+      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+        int m, n;
+        tile_coords<MODE>(ts, tile, m, n);
+        for (int kb = 0; kb < ts.nkb; ++kb) {
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, status, tmo, true)) {
+            ok = false;
+            break;
+          }
+          if (!(stall && tile == (int)blockIdx.x && kb == ts.nkb - 1)) {
+            const uint32_t fb = full_bar(s);
+            const uint32_t adst = smem_u32(smem + s * STAGE_BYTES);
+            const uint32_t bdst = adst + A_BYTES;
+            mbar_expect_tx(fb, STAGE_BYTES);
+            if (MODE == FWD) {
+              tma_load_2d(adst, &tmA, fb, kb * BK, m * BM);
+              tma_load_2d(bdst, &tmB, fb, kb * BK, n * BN);
+            } else if (MODE == DX) {
+              tma_load_2d(adst, &tmA, fb, kb * BK, m * BM);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tma_load_2d(bdst + j * BOX_BYTES, &tmB, fb, n * BN + j * 64, kb * BK);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 2; ++j) tma_load_2d(adst + j * BOX_BYTES, &tmA, fb, m * BM + j * 64, kb * BK);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tma_load_2d(bdst + j * BOX_BYTES, &tmB, fb, n * BN + j * 64, kb * BK);
+            }
+            armed |= 1u << s;
+            last_par = (last_par & ~(1u << s)) | (ph << s);
+          }
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // Every copy this thread issued lands before the CTA may exit.
+      for (int i = 0; i < STAGES; ++i)
+        if (armed & (1u << i)) wait_bounded(full_bar(i), (last_par >> i) & 1u, abort_flag, status, tmo, false);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = make_idesc<MODE, T>();
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+        const int as = it & 1;
+        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+        if (!wait_bounded(tempty_bar(as), aph ^ 1u, abort_flag, status, tmo, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(as * BN);
+        for (int kb = 0; kb < ts.nkb; ++kb) {
+          if (!wait_bounded(full_bar(s), ph, abort_flag, status, tmo, true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t abase = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t bbase = abase + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = MODE == DW ? sdesc(abase + k * 2048, 8192, 1024) : sdesc(abase + k * 32, 16, 1024);
+            const uint64_t bd = MODE == FWD ? sdesc(bbase + k * 32, 16, 1024) : sdesc(bbase + k * 2048, 8192, 1024);
+            mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(empty_bar(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(as));
+      }
+      // Every MMA this thread issued completes before TMEM is freed.
+      mma_commit(drain_bar);
+      wait_bounded(drain_bar, 0u, abort_flag, status, tmo, false);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5
+    const int q = warp & 3;
+    const float cb = MODE == FWD ? 0.0f : a.w.ctrl->cbar;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      const int as = it & 1;
+      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      bool ok = wait_bounded(tfull_bar(as), aph, abort_flag, status, tmo, true);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      int m, n;
+      tile_coords<MODE>(ts, tile, m, n);
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * BN);
+      if (MODE == FWD) epilogue_fwd<T>(a, row0, rows, m, n, taddr, q, lane);
+      else if (MODE == DX) epilogue_dx<T>(a, row0, rows, m, n, taddr, q, lane, cb);
+      else epilogue_dw(a, m, n, taddr, q, lane, cb);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(as));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  });
+  return fn;
+}
+
+// 2-D tiled map over a row-major matrix [outer, inner] with row pitch `pitch_bytes`;
+// 128-byte swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap* m, const void* ptr, int dt, uint64_t inner, uint64_t outer,
+              uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const CUtensorMapDataType ty =
+      dt == FLCE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, ty, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, typename T>
+cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
+                     const CUtensorMap& B, int64_t tiles_max) {
+  auto kern = k_gemm_tc<MODE, T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int64_t sms = num_sms();
+  const int grid = (int)(tiles_max < sms ? tiles_max : sms);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(A, B, a, chunk);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
+                        const CUtensorMap& B, int64_t tiles_max) {
+  if (a.dt == FLCE_BF16) return launch_t<MODE, __nv_bfloat16>(a, chunk, s, A, B, tiles_max);
+  return launch_t<MODE, __half>(a, chunk, s, A, B, tiles_max);
+}
+
+}  // namespace tc
+
+bool tc_supported(const CallArgs& a) {
+  if (a.dt != FLCE_BF16 && a.dt != FLCE_F16) return false;
+  if (a.H % 8 != 0) return false;  // TMA: the W row pitch must be a multiple of 16 bytes
+  if (a.H > (1LL << 30) || a.V > (1LL << 30)) return false;
+  return tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s) {
+  CUtensorMap A, B;
+  const uint64_t esz = 2;
+  if (!tc::make_map(&A, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 128)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 256)) return cudaErrorInvalidValue;
+  const int64_t tiles = ((a.R + 127) / 128) * a.nvt;
+  return tc::launch_mode<tc::FWD>(a, chunk, s, A, B, tiles);
+}
+
+cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
+  CUtensorMap A, B;
+  const uint64_t esz = 2;
+  if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 128)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 64)) return cudaErrorInvalidValue;
+  const int64_t tiles = ((a.R + 127) / 128) * ((a.H + 255) / 256);
+  return tc::launch_mode<tc::DX>(a, chunk, s, A, B, tiles);
+}
+
+cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
+  CUtensorMap A, B;
+  const uint64_t esz = 2;
+  if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 64)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&B, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 64)) return cudaErrorInvalidValue;
+  const int64_t tiles = ((a.V + 127) / 128) * ((a.H + 255) / 256);
+  return tc::launch_mode<tc::DW>(a, chunk, s, A, B, tiles);
+}
+
+}  // namespace flce

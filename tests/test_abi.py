@@ -1,0 +1,130 @@
+"""Host-side checks of the C-ABI library: it builds, loads without a GPU, exports every
+symbol include/flce.h declares, its struct layout matches the binding, the workspace
+planner keeps the transient flat in BT, and invalid arguments are rejected on the host
+before any CUDA call."""
+
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+import torch
+
+from linear_cross_entropy_logits_gb300 import build as B
+from linear_cross_entropy_logits_gb300 import flce
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return flce.load()
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return re.findall(r"FLCE_API\s+[\w\s\*]+?\b(flce_\w+)\s*\(", txt)
+
+
+def test_header_declares_the_binding_symbols():
+    assert sorted(_declared()) == sorted(flce.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", flce.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (flce_\w+)", out))
+    for name in _declared():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    assert lib.flce_abi_version() == 1
+
+
+def test_struct_layout_matches_c(lib):
+    fields = [f for f, _ in flce.FlceArgs._fields_]
+    src = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){",
+           'printf("%zu\\n", sizeof(flce_args));']
+    src += [f'printf("%zu\\n", offsetof(flce_args, {f}));' for f in fields]
+    src.append("return 0;}")
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "layout.c")
+        exe = os.path.join(d, "layout")
+        open(c, "w").write("\n".join(src))
+        subprocess.run(["gcc", "-std=c99", "-o", exe, c], check=True)
+        vals = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
+                                               check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(flce.FlceArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(flce.FlceArgs, f).offset == off, f
+
+
+@pytest.mark.parametrize("H,V,dt", [(4096, 128256, torch.bfloat16), (5376, 262144, torch.bfloat16),
+                                    (2048, 128256, torch.bfloat16), (64, 1000, torch.float32)])
+def test_workspace_flat_in_BT(lib, H, V, dt):
+    """With a fixed budget the workspace differs between BT values only by the 16 bytes
+    per row of the compaction index and per-row loss terms."""
+    budget = int(1.5 * 2 ** 30)
+    sizes = {BT: flce.workspace_size(BT, H, V, dt, budget) for BT in (8192, 16384, 32768)}
+    rows = {BT: flce.chunk_rows(BT, H, V, dt, sizes[BT]) for BT in sizes}
+    for BT, s in sizes.items():
+        assert 0 < s <= budget
+        assert rows[BT] % 128 == 0 and rows[BT] >= 128
+    if len(set(rows.values())) == 1:
+        d = sizes[32768] - sizes[16384]
+        assert abs(d - 16 * 16384) <= 4 * 256
+
+
+def test_large_vocab_workspace_fits_the_cap(lib):
+    cap = int(1.5 * 2 ** 30)
+    s = flce.workspace_size(32768, 5376, 262144, torch.bfloat16, cap)
+    assert 0 < s <= cap
+    assert flce.chunk_rows(32768, 5376, 262144, torch.bfloat16, s) >= 2048
+
+
+def test_workspace_too_small(lib):
+    assert flce.workspace_size(1024, 4096, 128256, torch.bfloat16, 1 << 20) == 0
+    assert flce.chunk_rows(1024, 4096, 128256, torch.bfloat16, 1 << 20) == 0
+
+
+def _args(**kw):
+    a = flce.FlceArgs()
+    a.BT, a.H, a.V = 16, 64, 100
+    a.in_dtype, a.reduction = 1, 0
+    a.X, a.W, a.targets, a.loss = 0x1000, 0x2000, 0x3000, 0x4000
+    a.workspace, a.workspace_bytes = 0x100000, 1 << 30
+    a.want_dX, a.dX = 0, None
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(X=None), flce.FLCE_ERR_INVALID_ARG),
+    (dict(W=None), flce.FLCE_ERR_INVALID_ARG),
+    (dict(targets=None), flce.FLCE_ERR_INVALID_ARG),
+    (dict(loss=None), flce.FLCE_ERR_INVALID_ARG),
+    (dict(workspace=None), flce.FLCE_ERR_INVALID_ARG),
+    (dict(BT=0), flce.FLCE_ERR_INVALID_ARG),
+    (dict(H=-1), flce.FLCE_ERR_INVALID_ARG),
+    (dict(in_dtype=7), flce.FLCE_ERR_INVALID_ARG),
+    (dict(reduction=3), flce.FLCE_ERR_INVALID_ARG),
+    (dict(z_loss_scale=-1.0), flce.FLCE_ERR_INVALID_ARG),
+    (dict(z_loss_scale=float("nan")), flce.FLCE_ERR_INVALID_ARG),
+    (dict(want_dX=1, dX=None), flce.FLCE_ERR_INVALID_ARG),
+    (dict(want_dW=1, dW=None), flce.FLCE_ERR_INVALID_ARG),
+    (dict(want_dW=1, dW=0x5000, dW_dtype=1), flce.FLCE_ERR_UNSUPPORTED),
+    (dict(X=0x1008), flce.FLCE_ERR_INVALID_ARG),
+    (dict(workspace=0x100010), flce.FLCE_ERR_INVALID_ARG),
+    (dict(workspace_bytes=1024), flce.FLCE_ERR_WORKSPACE),
+])
+def test_host_validation_rejects_before_any_cuda_call(lib, kw, code):
+    a = _args(**kw)
+    assert flce.raw_call(a, 0) == code
+
+
+def test_null_args_pointer(lib):
+    assert lib.flce_fwd_bwd(None, None) == flce.FLCE_ERR_INVALID_ARG

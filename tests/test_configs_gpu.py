@@ -1,0 +1,123 @@
+"""Parity at the workloads' full sizes, in the launch configuration the benchmark times
+(default 1.5 GiB workspace budget).
+
+The oracle cannot evaluate every row of these problems in seconds, so each check is
+either on sampled outputs the oracle computes one by one, or on a property that holds at
+any size:
+  * per-token lse / prediction / loss and dX rows on 48 seeded rows (labelled and
+    ignored) of the full run;
+  * the reduced loss equals the mean/sum of the per-token losses of a reduction="none"
+    run (and those per-token losses match the oracle on the sampled rows);
+  * with z = 0, every column of dW sums to zero over the vocabulary (sum_v dS_iv = 0);
+  * dW exactly, on 256 sampled vocabulary rows, from a run at the same full shapes in
+    which only 64 seeded rows keep their label (so the oracle needs only those rows).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from linear_cross_entropy_logits_gb300 import build as B
+from linear_cross_entropy_logits_gb300 import flce
+from linear_cross_entropy_logits_gb300 import inputs as I
+from oracle import flce_oracle as orc
+from parity_util import TOL, pred_ok, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = [
+    ("llama1b", {}),
+    ("llama8b", dict(labelled_fraction=1.0)),
+    ("llama8b", dict(labelled_fraction=0.75)),
+    ("llama8b", dict(labelled_fraction=0.5)),
+    ("llama8b", dict(labelled_fraction=0.25)),
+    ("llama8b", dict(labelled_fraction=0.1)),
+    ("large_vocab", {}),
+    ("frozen_head", {}),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.build()
+    flce.load()
+
+
+def _gpu(d, sp, reduction=None, targets=None, want_dW=None):
+    red = reduction or sp["reduction"]
+    wdw = sp["want_dW"] if want_dW is None else want_dW
+    dW = torch.zeros(sp["V"], sp["H"], dtype=torch.float32, device="cuda") if wdw else None
+    go = d["grad_out"] if red == "none" else None
+    out = flce.fwd_bwd(d["X"], d["W"], d["targets"] if targets is None else targets, d["bias"],
+                       reduction=red, z_loss_scale=sp.get("z", 0.0), grad_out=go,
+                       want_dX=True, want_dW=wdw, dW=dW,
+                       budget_bytes=sp.get("workspace_cap", 0))
+    torch.cuda.synchronize()
+    assert out["status_code"] == flce.FLCE_OK
+    return out
+
+
+@pytest.mark.parametrize("base,ov", CONFIGS,
+                         ids=[b + "".join(f"-{k}{v}" for k, v in o.items()) for b, o in CONFIGS])
+def test_config_sampled(base, ov):
+    sp = I.spec(base, **ov)
+    inp = I.generate(sp, seed=0)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    BT, H, V = sp["BT"], sp["H"], sp["V"]
+    dt = sp["dtype"]
+    tol = TOL[dt]
+    X = I.to_numpy_exact(inp["X"])
+    W = I.to_numpy_exact(inp["W"])
+    b = I.to_numpy_exact(inp["bias"])
+    t = inp["targets"].numpy()
+    g_np = inp["grad_out"].numpy() if inp["grad_out"] is not None else None
+    mask = t != I.IGNORE_INDEX
+
+    full = _gpu(d, sp)
+    rng = np.random.default_rng(1234)
+    rows = np.sort(rng.choice(BT, size=48, replace=False))
+    o = orc.flce_oracle_rows(X, W, t, rows, bias=b, reduction=sp["reduction"],
+                             z_loss_scale=sp.get("z", 0.0), grad_out=g_np)
+    lse = full["lse"].cpu().numpy()[rows]
+    pred = full["pred"].cpu().numpy()[rows]
+    dX = full["dX"][torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    assert int(full["n_labelled"][0]) == int(mask.sum())
+    m = mask[rows]
+    assert np.all(pred[~m] == -1) and np.all(lse[~m] == 0) and np.all(dX[~m] == 0)
+    assert np.max(np.abs(lse[m] - o["lse_tok"][m]) / np.abs(o["lse_tok"][m])) <= tol["loss"]
+    ok, _ = pred_ok(pred, o["pred_tok"], X, W, b, rows, m)
+    assert ok
+    assert rel_fro(dX, o["dX"]) <= tol["grad"]
+
+    # per-token losses of a reduction="none" run, and the reduced loss as their mean/sum
+    if sp["reduction"] == "none":
+        per = full["loss"].cpu().numpy()
+    else:
+        per = _gpu(d, sp, reduction="none", want_dW=False)["loss"].cpu().numpy()
+        tot = float(np.sum(per.astype(np.float64)))
+        ref = tot / max(int(mask.sum()), 1) if sp["reduction"] == "mean" else tot
+        assert abs(float(full["loss"][0]) - ref) <= 1e-5 * abs(ref)
+    assert np.max(np.abs(per[rows][m] - o["loss_tok"][m]) / np.abs(o["loss_tok"][m])) <= tol["loss"]
+    assert np.all(per[rows][~m] == 0)
+
+    if sp["want_dW"]:
+        dW = full["dW"]
+        if sp.get("z", 0.0) == 0.0:
+            colsum = dW.double().sum(dim=0).abs().max().item()
+            scale = dW.double().abs().sum(dim=0).max().item()
+            assert colsum <= 1e-3 * scale
+        # exact dW on sampled vocabulary rows from a run where 64 rows keep their label
+        keep = np.sort(rng.choice(np.nonzero(mask)[0], size=min(64, int(mask.sum())), replace=False))
+        t2 = np.full(BT, I.IGNORE_INDEX, dtype=np.int64)
+        t2[keep] = t[keep]
+        g2 = _gpu(d, sp, targets=torch.from_numpy(t2).cuda())
+        vs = np.unique(np.concatenate([t2[keep], rng.choice(V, size=256 - len(keep), replace=False)]))
+        c = orc.grad_scales(t2 != I.IGNORE_INDEX, sp["reduction"], None)[keep]
+        s = orc.logits_rows(X[keep], W, b)
+        lse2, _, _, _, _, p = orc.rows_forward(s, t2[keep], sp.get("z", 0.0))
+        dS = orc.rows_grad_logits(p, t2[keep], lse2, c, sp.get("z", 0.0))
+        ref = dS[:, vs].T @ np.asarray(X[keep], np.float64)
+        got = g2["dW"][torch.from_numpy(vs).cuda()].cpu().numpy()
+        assert rel_fro(got, ref) <= tol["grad"]

@@ -1,0 +1,217 @@
+"""GPU parity of the CUDA path (through the C ABI) against the float64 oracle, element by
+element, at sizes the oracle finishes in seconds that span several tiles and ragged tails,
+plus the method's edge cases. Both GEMM back-ends are covered: the tcgen05 tensor-core
+kernels (bf16/fp16) and the SIMT fp32-FMA kernels (fp32, and bf16 when forced)."""
+
+import numpy as np
+import pytest
+import torch
+
+from linear_cross_entropy_logits_gb300 import build as B
+from linear_cross_entropy_logits_gb300 import flce
+from linear_cross_entropy_logits_gb300 import inputs as I
+from parity_util import compare_full, rel_fro, run_gpu, run_oracle, TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.build()
+    flce.load()
+
+
+# Small problems: (name, base workload, overrides)
+SMALL = [
+    ("bf16_mean_ragged", "llama1b", dict(BT=300, H=192, V=3000, w_std=0.2, ignore="random",
+                                          n_ignored=40)),
+    ("bf16_sum_bias_z", "large_vocab", dict(BT=260, H=520, V=1300, w_std=0.1, bias_std=0.5,
+                                             z=0.01, targets="uniform", ignore="random",
+                                             n_ignored=31)),
+    ("bf16_prompt_first", "llama8b", dict(BT=1024, H=256, V=2304, w_std=0.1,
+                                          labelled_fraction=0.5)),
+    ("bf16_none_frozen_bias", "frozen_head", dict(BT=400, H=128, V=5000, w_std=0.15,
+                                                   bias_std=0.3, n_ignored=200)),
+    ("f16_mean", "llama1b", dict(BT=256, H=320, V=2000, dtype="f16", w_std=0.1,
+                                 ignore="random", n_ignored=5)),
+    ("bf16_tiny_H64", "llama1b", dict(BT=130, H=64, V=1000, w_std=0.3, ignore="random",
+                                      n_ignored=3)),
+]
+
+
+def _spec(base, ov):
+    sp = I.spec(base, **ov)
+    return sp
+
+
+@pytest.mark.parametrize("name,base,ov", SMALL, ids=[s[0] for s in SMALL])
+@pytest.mark.parametrize("path", ["tc", "simt"])
+def test_small_parity(name, base, ov, path):
+    sp = _spec(base, ov)
+    inp = I.generate(sp, seed=0)
+    o = run_oracle(inp, sp)
+    g = run_gpu(inp, sp, flags=flce.FLAG_FORCE_SIMT if path == "simt" else 0)
+    assert g["status_code"] == flce.FLCE_OK
+    compare_full(g, o, inp, sp)
+
+
+def test_config1_tiny_fp32_full():
+    """BT=128, H=64, V=1000 fp32, 13 rows ignored, mean: every output element against the
+    oracle at 1e-5."""
+    sp = I.spec("tiny_fp32")
+    inp = I.generate(sp, seed=0)
+    o = run_oracle(inp, sp)
+    g = run_gpu(inp, sp)
+    assert g["status_code"] == flce.FLCE_OK
+    assert int(g["n_labelled"][0]) == 115
+    compare_full(g, o, inp, sp)
+
+
+def test_fp32_none_with_bias_and_z():
+    sp = I.spec("tiny_fp32", BT=200, H=96, V=700, bias_std=0.2, reduction="none",
+                grad_out="uniform", z=0.05, n_ignored=20)
+    inp = I.generate(sp, seed=3)
+    compare_full(run_gpu(inp, sp), run_oracle(inp, sp), inp, sp)
+
+
+def _ws_for_rows(BT, H, V, dt, R):
+    return flce.workspace_size(R, H, V, dt, 0) + 16 * BT + 4096
+
+
+@pytest.mark.parametrize("path", ["tc", "simt"])
+def test_multichunk(path):
+    """A workspace that holds 128 rows forces several chunks (uneven last chunk); the
+    result must match the oracle and the single-chunk result."""
+    sp = I.spec("llama8b", BT=1024, H=128, V=1500, w_std=0.2, labelled_fraction=0.75,
+                z=1e-3)
+    inp = I.generate(sp, seed=1)
+    flags = flce.FLAG_FORCE_SIMT if path == "simt" else 0
+    wb = _ws_for_rows(sp["BT"], sp["H"], sp["V"], torch.bfloat16, 128)
+    assert flce.chunk_rows(sp["BT"], sp["H"], sp["V"], torch.bfloat16, wb) == 128
+    g1 = run_gpu(inp, sp, flags=flags, workspace_bytes=wb)
+    g2 = run_gpu(inp, sp, flags=flags)
+    o = run_oracle(inp, sp)
+    compare_full(g1, o, inp, sp)
+    compare_full(g2, o, inp, sp)
+    assert rel_fro(g1["dW"], g2["dW"]) < 1e-5
+    assert rel_fro(g1["dX"], g2["dX"]) < 1e-5
+
+
+def test_deterministic():
+    sp = I.spec("llama1b", BT=512, H=256, V=3000, w_std=0.2, ignore="random", n_ignored=50)
+    inp = I.generate(sp, seed=2)
+    a = run_gpu(inp, sp)
+    b = run_gpu(inp, sp)
+    for k in ("loss", "lse", "pred", "dX", "dW"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("path", ["tc", "simt"])
+def test_nan_in_ignored_rows_does_not_leak(path):
+    """A NaN stored in an ignored row reaches no output; results equal the clean run bit
+    for bit (Liger-Kernel PR #1554, Tests: test_ignored_rows_do_not_enter_projection)."""
+    sp = I.spec("frozen_head", BT=256, H=128, V=1200, w_std=0.2, n_ignored=100,
+                reduction="sum", want_dW=True, grad_out=None)
+    inp = I.generate(sp, seed=4)
+    flags = flce.FLAG_FORCE_SIMT if path == "simt" else 0
+    clean = run_gpu(inp, sp, flags=flags)
+    ign = inp["targets"] == I.IGNORE_INDEX
+    Xn = inp["X"].clone()
+    Xn[ign] = float("nan")
+    dirty = run_gpu(dict(inp, X=Xn), sp, flags=flags)
+    for k in ("loss", "lse", "pred", "dX", "dW", "dbias", "z_loss", "acc"):
+        assert np.array_equal(clean[k], dirty[k], equal_nan=False), k
+    assert np.all(np.isfinite(dirty["dW"])) and np.all(np.isfinite(dirty["dX"]))
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_all_rows_ignored(reduction):
+    sp = I.spec("llama1b", BT=200, H=64, V=500, ignore="all", reduction=reduction,
+                bias_std=0.1)
+    inp = I.generate(sp, seed=5)
+    g = run_gpu(inp, sp)
+    assert g["status_code"] == flce.FLCE_OK
+    assert int(g["n_labelled"][0]) == 0
+    assert np.all(g["loss"] == 0) and np.all(g["pred"] == -1) and np.all(g["lse"] == 0)
+    assert np.all(g["dX"] == 0) and np.all(g["dW"] == 0) and np.all(g["dbias"] == 0)
+
+
+def test_single_labelled_row_and_target_edges():
+    sp = I.spec("llama1b", BT=150, H=72, V=777, w_std=0.3, ignore="none")
+    inp = I.generate(sp, seed=6)
+    t = inp["targets"]
+    t[:] = I.IGNORE_INDEX
+    t[77] = sp["V"] - 1
+    o = run_oracle(inp, sp)
+    compare_full(run_gpu(inp, sp), o, inp, sp)
+    t[:] = 0
+    t[1::2] = sp["V"] - 1
+    compare_full(run_gpu(inp, sp), run_oracle(inp, sp), inp, sp)
+
+
+def test_out_of_range_target_sets_status_and_is_ignored():
+    sp = I.spec("llama1b", BT=128, H=64, V=300, w_std=0.3, ignore="random", n_ignored=4)
+    inp = I.generate(sp, seed=7)
+    inp["targets"][10] = sp["V"]
+    inp["targets"][11] = -5
+    g = run_gpu(inp, sp)
+    assert g["status_code"] == flce.FLCE_ERR_TARGET_RANGE
+    o = run_oracle(inp, sp)
+    assert o["out_of_range"]
+    compare_full(g, o, inp, sp)
+
+
+def test_dW_accumulates_into_destination():
+    sp = I.spec("llama1b", BT=300, H=128, V=900, w_std=0.2, ignore="random", n_ignored=30)
+    inp = I.generate(sp, seed=8)
+    init = torch.randn(sp["V"], sp["H"], generator=torch.Generator().manual_seed(9))
+    g = run_gpu(inp, sp, dW_init=init)
+    o = run_oracle(inp, sp)
+    assert rel_fro(g["dW"] - init.numpy(), o["dW"]) <= TOL["bf16"]["grad"]
+
+
+def test_grad_scalar_scales_gradients():
+    sp = I.spec("llama1b", BT=128, H=64, V=640, w_std=0.2, ignore="random", n_ignored=8,
+                grad_scalar=0.37, z=0.02)
+    inp = I.generate(sp, seed=10)
+    compare_full(run_gpu(inp, sp), run_oracle(inp, sp), inp, sp)
+
+
+def test_guard_bands_untouched():
+    """Canary bands around every output and around the workspace stay intact (the
+    stand-in for an out-of-bounds checker)."""
+    sp = I.spec("frozen_head", BT=300, H=192, V=1700, w_std=0.2, n_ignored=90,
+                reduction="none", want_dW=True)
+    inp = I.generate(sp, seed=11)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    BT, H, V = sp["BT"], sp["H"], sp["V"]
+    G = 4096
+    sentinel = 0x5A
+
+    def guarded(n, dtype):
+        esz = torch.empty(0, dtype=dtype).element_size()
+        raw = torch.full((n * esz + 2 * G,), sentinel, dtype=torch.uint8, device="cuda")
+        return raw, raw[G:G + n * esz].view(dtype)
+
+    bufs = {
+        "loss": guarded(BT, torch.float32), "z_loss": guarded(BT, torch.float32),
+        "acc": guarded(BT, torch.float32), "lse": guarded(BT, torch.float32),
+        "pred": guarded(BT, torch.int64), "dX": guarded(BT * H, torch.bfloat16),
+    }
+    dW_raw, dW = guarded(V * H, torch.float32)
+    dW.zero_()
+    db_raw, db = guarded(V, torch.float32)
+    db.zero_()
+    wsb = flce.workspace_size(BT, H, V, torch.bfloat16, 0)
+    ws_raw = torch.full((wsb + 2 * G,), sentinel, dtype=torch.uint8, device="cuda")
+    ws = ws_raw[G:G + wsb]
+    outs = {k: (v[1].view(BT, H) if k == "dX" else v[1]) for k, v in bufs.items()}
+    o = flce.fwd_bwd(d["X"], d["W"], d["targets"], d["bias"], reduction="none",
+                     grad_out=d["grad_out"], dW=dW.view(V, H), dbias=db, workspace=ws,
+                     outputs=outs)
+    torch.cuda.synchronize()
+    assert o["status_code"] == flce.FLCE_OK
+    for raw in [b[0] for b in bufs.values()] + [dW_raw, db_raw, ws_raw]:
+        assert torch.all(raw[:G] == sentinel) and torch.all(raw[-G:] == sentinel)
