@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--bt", type=int, default=None,
+                   help="override BT (smaller cases for profiler captures)")
     return p.parse_args()
 
 
@@ -63,6 +65,8 @@ def workload_spec(args):
     ov = {}
     if args.labelled_fraction is not None:
         ov["labelled_fraction"] = args.labelled_fraction
+    if args.bt is not None:
+        ov["BT"] = args.bt
     return I.spec(args.workload, **ov)
 
 
