@@ -70,8 +70,10 @@ typedef enum flce_status {
   FLCE_ERR_TARGET_RANGE = 3, /* device: a labelled target outside [0,V); row ignored    */
   FLCE_ERR_WORKSPACE = 4,    /* workspace too small for one 128-row chunk               */
   FLCE_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed                    */
-  FLCE_ERR_TIMEOUT = 6       /* device: a pipeline wait exceeded its limit; outputs are
+  FLCE_ERR_TIMEOUT = 6,      /* device: a pipeline wait exceeded its limit; outputs are
                                 not valid                                               */
+  FLCE_ERR_SCRATCH_LIMIT = 7 /* flce_fwd_bwd_noalloc: the problem does not fit the fixed
+                                scratch of FLCE_NOALLOC_SCRATCH_BYTES                   */
 } flce_status;
 
 typedef enum flce_reduction { FLCE_MEAN = 0, FLCE_SUM = 1, FLCE_NONE = 2 } flce_reduction;
@@ -159,6 +161,29 @@ FLCE_API int64_t flce_chunk_rows(int64_t BT, int64_t H, int64_t V, int32_t in_dt
  * stream). Returns FLCE_OK once every kernel is enqueued, or an error code with nothing
  * enqueued (FLCE_ERR_CUDA may follow a partial enqueue if a launch fails). */
 FLCE_API int32_t flce_fwd_bwd(const flce_args* args, void* stream);
+
+/* Size of the fixed device scratch used by flce_fwd_bwd_noalloc (128 MiB). */
+#define FLCE_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20)
+
+/* Same operation and arguments as flce_fwd_bwd, for callers that cannot allocate device
+ * memory (a framework that owns all device memory through its own pool, code that must
+ * not allocate after start-up, a foreign-function layer that forwards only the op's
+ * inputs and outputs). The pages have no counterpart of this entry point.
+ *
+ * Instead of a caller workspace it uses a scratch array of FLCE_NOALLOC_SCRATCH_BYTES
+ * compiled into the library: every GPU that loads the library holds that memory until the
+ * process exits. args->workspace must be NULL, args->workspace_bytes 0 and args->profile
+ * NULL (FLCE_ERR_INVALID_ARG otherwise). Problems whose 128-row chunk does not fit the
+ * scratch (roughly 2 * V * 128 + 16 * BT bytes and more) are rejected with
+ * FLCE_ERR_SCRATCH_LIMIT before anything is enqueued; fitting problems run in chunks of
+ * as many rows as the scratch holds. The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * The first call on each device, with that device current, looks up the scratch's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ * capture. All calls share the one scratch array and it keeps the last call's contents:
+ * calls that overlap on the GPU (on streams with no ordering between them) race on it. */
+FLCE_API int32_t flce_fwd_bwd_noalloc(const flce_args* args, void* stream);
 
 /* Synchronise `stream`, read the device status word and return the most severe code it
  * holds (FLCE_ERR_TIMEOUT, then FLCE_ERR_TARGET_RANGE, else FLCE_OK); FLCE_ERR_CUDA if the

@@ -316,6 +316,7 @@ extern "C" const char* flce_status_string(int32_t code) {
     case FLCE_ERR_WORKSPACE: return "FLCE_ERR_WORKSPACE";
     case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA";
     case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT";
+    case FLCE_ERR_SCRATCH_LIMIT: return "FLCE_ERR_SCRATCH_LIMIT";
     default: return "FLCE_ERR_UNKNOWN";
   }
 }

@@ -16,12 +16,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libflce.so")
 
 FLCE_OK, FLCE_ERR_INVALID_ARG, FLCE_ERR_UNSUPPORTED, FLCE_ERR_TARGET_RANGE = 0, 1, 2, 3
-FLCE_ERR_WORKSPACE, FLCE_ERR_CUDA, FLCE_ERR_TIMEOUT = 4, 5, 6
+FLCE_ERR_WORKSPACE, FLCE_ERR_CUDA, FLCE_ERR_TIMEOUT, FLCE_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
+NOALLOC_SCRATCH_BYTES = 128 << 20
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 FLAG_FORCE_SIMT = 0x1
 FLAG_DEBUG_STALL = 0x100
-EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_get_status",
+EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_fwd_bwd_noalloc",
+            "flce_get_status",
             "flce_profile_create", "flce_profile_reset", "flce_profile_destroy",
             "flce_profile_read", "flce_status_string", "flce_abi_version")
 STAGES = ("prologue", "gather", "fwd", "finalize", "gpass", "dx", "dw", "reduce")
@@ -64,6 +66,8 @@ def load(path: str | None = None):
     lib.flce_chunk_rows.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int32, ctypes.c_size_t]
     lib.flce_fwd_bwd.restype = ctypes.c_int32
     lib.flce_fwd_bwd.argtypes = [ctypes.POINTER(FlceArgs), ctypes.c_void_p]
+    lib.flce_fwd_bwd_noalloc.restype = ctypes.c_int32
+    lib.flce_fwd_bwd_noalloc.argtypes = [ctypes.POINTER(FlceArgs), ctypes.c_void_p]
     lib.flce_get_status.restype = ctypes.c_int32
     lib.flce_get_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.flce_status_string.restype = ctypes.c_char_p
