@@ -60,9 +60,9 @@ struct Work {
   float* rz;       // [BT] z-loss
   float* racc;     // [BT] accuracy
   void* xc;        // [R, Hp] gathered rows of the current chunk (zero past its end)
-  float* stm;      // [nvt, R] tile max; rewritten by finalize as the G multiplier
-  float* sts;      // [nvt, R] tile sum of exp(s - tile max)
-  int* sti;        // [nvt, R] tile argmax (lowest index)
+  float* stm;      // [R, nvt] tile max; rewritten by finalize as the G multiplier
+  float* sts;      // [R, nvt] tile sum of exp(s - tile max)
+  int* sti;        // [R, nvt] tile argmax (lowest index)
   float* tgt;      // [R] target logit
   float* lse;      // [R] row logsumexp
   float* arow;     // [R] per-row factor a_i (g_i for none, 1 otherwise)

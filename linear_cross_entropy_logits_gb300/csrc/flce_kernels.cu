@@ -147,47 +147,55 @@ __global__ void __launch_bounds__(256) k_gather(const __grid_constant__ CallArgs
 }
 
 // ---------------------------------------------------------------------------------------
-// Finalize: merge the per-tile (max, sum-exp, argmax) triples of each row in ascending
-// tile order, giving lse, loss, z-loss, prediction and accuracy; then turn each tile max
-// into the multiplier that maps the stored exp(s - tile max) to the row's gradient
-// a_i (1 + 2 z lse) exp(s - lse).
+// Finalize: one warp per row merges the row's per-tile (max, sum-exp, argmax) triples,
+// giving lse, loss, z-loss, prediction and accuracy; then turns each tile max into the
+// multiplier that maps the stored exp(s - tile max) to the row's gradient
+// a_i (1 + 2 z lse) exp(s - lse). The merge order is fixed (lane-strided tiles, then an
+// xor butterfly whose combine is commutative), so every lane and every run agree bitwise.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) k_finalize(const __grid_constant__ CallArgs a, int chunk) {
+__device__ __forceinline__ void lse_combine(float& M, float& S, int& am, float M2, float S2, int a2) {
+  const float Mn = fmaxf(M, M2);
+  const float Sn = Mn == -INFINITY ? 0.0f : S * expf(M - Mn) + S2 * expf(M2 - Mn);
+  am = M > M2 ? am : (M2 > M ? a2 : min(am, a2));
+  M = Mn;
+  S = Sn;
+}
+
+__global__ void __launch_bounds__(256) k_finalize(const __grid_constant__ CallArgs a, int chunk) {
   int row0, rows;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= rows) return;
-  const int64_t R = a.R;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;  // warp-uniform
   const int nvt = (int)a.nvt;
-  float* stm = a.w.stm;
-  const float* sts = a.w.sts;
-  const int* sti = a.w.sti;
+  float* stm = a.w.stm + (int64_t)r * nvt;
+  const float* sts = a.w.sts + (int64_t)r * nvt;
+  const int* sti = a.w.sti + (int64_t)r * nvt;
 
-  float M = -INFINITY;
-  int am = 0;
-  for (int t = 0; t < nvt; ++t) {
-    const float m = stm[t * R + r];
-    if (m > M) {
-      M = m;
-      am = sti[t * R + r];
-    }
+  float M = -INFINITY, S = 0.0f;
+  int am = 0x7fffffff;
+  for (int t = lane; t < nvt; t += 32) lse_combine(M, S, am, stm[t], sts[t], sti[t]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
+    const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const int a2 = __shfl_xor_sync(0xffffffffu, am, o);
+    lse_combine(M, S, am, M2, S2, a2);
   }
-  float S = 0.0f;
-  for (int t = 0; t < nvt; ++t) S += sts[t * R + r] * expf(stm[t * R + r] - M);
   const float lse = M + logf(S);
 
   const int row = a.w.idx[row0 + r];
   const int64_t tg = a.targets[row];
-  const float zl = a.z * lse * lse;
-  const float loss = (lse - a.w.tgt[r]) + zl;
-  const float accv = ((int64_t)am == tg) ? 1.0f : 0.0f;
   float ar = 1.0f;
   if (a.reduction == FLCE_NONE && a.grad_out != nullptr) ar = a.grad_out[row];
   const float f = ar * (1.0f + 2.0f * a.z * lse);
-  for (int t = 0; t < nvt; ++t) stm[t * R + r] = f * expf(stm[t * R + r] - lse);
+  for (int t = lane; t < nvt; t += 32) stm[t] = f * expf(stm[t] - lse);
+  if (lane != 0) return;
+  const float zl = a.z * lse * lse;
+  const float loss = (lse - a.w.tgt[r]) + zl;
+  const float accv = ((int64_t)am == tg) ? 1.0f : 0.0f;
   a.w.lse[r] = lse;
   a.w.arow[r] = ar;
-
   if (a.lse_out) a.lse_out[row] = lse;
   if (a.pred) a.pred[row] = am;
   if (a.reduction == FLCE_NONE) {
@@ -275,7 +283,7 @@ __global__ void __launch_bounds__(256) k_gpass(const __grid_constant__ CallArgs 
     T* p = slab + (int64_t)r * a.Vp + c0;
     float f[8];
     if (r < rows) {
-      const float m = a.w.stm[t * R + r];
+      const float m = a.w.stm[(int64_t)r * a.nvt + t];
       const float ar = a.w.arow[r];
       const int64_t tg = a.targets[a.w.idx[row0 + r]];
       Vec8<T>::load(p, f);
@@ -450,9 +458,10 @@ __global__ void __launch_bounds__(256) k_fwd_simt(const __grid_constant__ CallAr
     const unsigned hb = __ballot_sync(0xffffffffu, ht);
     if (hb) tl = __shfl_sync(0xffffffffu, tl, __ffs(hb) - 1);
     if (lane == 0) {
-      a.w.stm[t * a.R + rr] = mx;
-      a.w.sts[t * a.R + rr] = sum;
-      a.w.sti[t * a.R + rr] = ai;
+      const int64_t o = (int64_t)rr * a.nvt + t;
+      a.w.stm[o] = mx;
+      a.w.sts[o] = sum;
+      a.w.sti[o] = ai;
       if (hb) a.w.tgt[rr] = tl;
     }
   }
@@ -566,7 +575,7 @@ cudaError_t launch_gather(const CallArgs& a, int chunk, cudaStream_t s) {
 }
 
 cudaError_t launch_finalize(const CallArgs& a, int chunk, cudaStream_t s) {
-  k_finalize<<<(unsigned)cdiv64(a.R, 128), 128, 0, s>>>(a, chunk);
+  k_finalize<<<(unsigned)cdiv64(a.R, 8), 256, 0, s>>>(a, chunk);
   return cudaGetLastError();
 }
 

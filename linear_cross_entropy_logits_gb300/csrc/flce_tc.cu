@@ -8,8 +8,9 @@
 //        argmax and the target logit, and stores exp(s - max) (in the input dtype) into
 //        the chunk slab, from which the gradient is formed once the row's lse is known.
 //   DX:  dX[idx] = cbar * G W (K = V), written through the compaction index.
-//   DW:  dW += cbar * G^T Xc (K = chunk rows), read-modify-write of the fp32 destination
-//        by the single CTA that owns each tile (deterministic, no atomics).
+//   DW:  dW += cbar * G^T Xc (K = chunk rows), added into the fp32 destination by TMA
+//        reduce-add from the single CTA that owns each tile (one add per element per
+//        launch: deterministic).
 // The three products are the logits, grad_input and grad_weight GEMMs that the pages'
 // op runs in its forward ("Liger-Kernel PR #1554: skip ignore_index rows", Summary); dW is
 // accumulated straight into the caller's buffer with no [V,H] temporary ("Reduce FLCE
@@ -25,6 +26,7 @@
 // waits for its own copies and MMAs in flight, frees TMEM and returns.
 #include <cuda.h>
 #include <mutex>
+#include <type_traits>
 
 #include "flce_internal.cuh"
 
@@ -39,7 +41,14 @@ constexpr int BOX_BYTES = 64 * 64 * 2;             // one 64x64 MN-major TMA box
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_BARS = 2 * STAGES + 5;           // full, empty, tfull[2], tempty[2], drain
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+// DW epilogue staging: per epilogue warp, two 32-row x 128-byte buffers that feed TMA
+// reduce-add (the L2 performs dW += tile; no register read-modify-write).
+constexpr int EPI_BUF_BYTES = 32 * 128;
+constexpr int EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;   // 32 KB
+template <int MODE>
+constexpr int smem_bytes() {
+  return STAGES * STAGE_BYTES + (MODE == 2 ? EPI_BYTES : 0) + 1024 + 256;
+}
 
 enum Mode { FWD = 0, DX = 1, DW = 2 };
 
@@ -103,6 +112,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
       : "memory");
+}
+
+// dst[box at (x, y)] += smem tile, performed by the TMA unit / L2 (fp32 add).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          (uint64_t)map),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_le1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -276,7 +302,7 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
     }
   }
   if (valid) {
-    const int64_t o = (int64_t)n * a.R + rr;
+    const int64_t o = (int64_t)rr * a.nvt + n;
     a.w.stm[o] = mx;
     a.w.sts[o] = sum;
     a.w.sti[o] = ai;
@@ -313,36 +339,40 @@ __device__ __forceinline__ void epilogue_dx(const CallArgs& a, int row0, int row
   }
 }
 
-__device__ __forceinline__ void epilogue_dw(const CallArgs& a, int m, int n, uint32_t taddr, int q,
-                                            int lane, float cb) {
-  const int v = m * BM + q * 32 + lane;
-  const bool valid = v < (int)a.V;
+// dW tile += cbar * acc through TMA reduce-add. Each epilogue warp owns 32 rows (its TMEM
+// lane quadrant) and stages 32 columns at a time (32 x 128 B, 128-byte swizzle: 16-byte
+// chunk j of row r sits at chunk j ^ (r % 8)), alternating two buffers; the TMA unit adds
+// the box into dW in L2. Each dW element gets exactly one add per launch (one owning CTA),
+// so the result does not depend on timing. Boxes past V or H are clipped by the TMA unit.
+__device__ __forceinline__ void epilogue_dw(const CallArgs& a, const CUtensorMap* tmC, uint8_t* stg,
+                                            int m, int n, uint32_t taddr, int q, int lane, float cb,
+                                            uint32_t& epi_it) {
   const int H = (int)a.H;
-  float* wrow = a.dW + (int64_t)(valid ? v : 0) * a.H;
+  const int y = m * BM + q * 32;
+  if (y >= (int)a.V) return;  // this warp's 32 rows lie past V (warp-uniform)
 #pragma unroll 1
   for (int cc = 0; cc < BN / 32; ++cc) {
+    const int x = n * BN + cc * 32;
+    if (x >= H) break;  // warp-uniform
     uint32_t r[32];
     tmem_ld32(taddr + cc * 32, r);
-    const int h0 = n * BN + cc * 32;
-    if (valid && h0 < H) {
+    uint8_t* buf = stg + (epi_it & 1u) * EPI_BUF_BYTES;
+    if (lane == 0) bulk_wait_read_le1();  // the reduce that last read this buffer is done
+    __syncwarp();
+    uint8_t* row = buf + lane * 128;
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        if (h0 + g * 8 < H) {
-          float4* p = (float4*)(wrow + h0 + g * 8);
-          float4 x0 = p[0], x1 = p[1];
-          x0.x = fmaf(cb, __uint_as_float(r[g * 8 + 0]), x0.x);
-          x0.y = fmaf(cb, __uint_as_float(r[g * 8 + 1]), x0.y);
-          x0.z = fmaf(cb, __uint_as_float(r[g * 8 + 2]), x0.z);
-          x0.w = fmaf(cb, __uint_as_float(r[g * 8 + 3]), x0.w);
-          x1.x = fmaf(cb, __uint_as_float(r[g * 8 + 4]), x1.x);
-          x1.y = fmaf(cb, __uint_as_float(r[g * 8 + 5]), x1.y);
-          x1.z = fmaf(cb, __uint_as_float(r[g * 8 + 6]), x1.z);
-          x1.w = fmaf(cb, __uint_as_float(r[g * 8 + 7]), x1.w);
-          p[0] = x0;
-          p[1] = x1;
-        }
-      }
+    for (int j = 0; j < 8; ++j) {
+      float4 v = make_float4(cb * __uint_as_float(r[4 * j + 0]), cb * __uint_as_float(r[4 * j + 1]),
+                             cb * __uint_as_float(r[4 * j + 2]), cb * __uint_as_float(r[4 * j + 3]));
+      *(float4*)(row + ((j ^ (lane & 7)) << 4)) = v;
     }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_reduce_add_2d(tmC, smem_u32(buf), x, y);
+      bulk_commit();
+    }
+    ++epi_it;
   }
 }
 
@@ -350,7 +380,8 @@ __device__ __forceinline__ void epilogue_dw(const CallArgs& a, int m, int n, uin
 template <int MODE, typename T>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CallArgs a, const int chunk) {
+              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CallArgs a,
+              const int chunk) {
   int row0 = 0, rows = 0;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
   const TileSpace ts = tile_space<MODE>(a, rows);
@@ -359,7 +390,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES);
+  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;  // DW only
+  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES + (MODE == DW ? EPI_BYTES : 0));
   uint32_t* tmem_slot = (uint32_t*)(bars + NUM_BARS);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -495,6 +527,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------- epilogue warps 2..5
     const int q = warp & 3;
     const float cb = MODE == FWD ? 0.0f : a.w.ctrl->cbar;
+    uint8_t* stg = epi_stage + (warp - 2) * 2 * EPI_BUF_BYTES;
+    uint32_t epi_it = 0;
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
       const int as = it & 1;
@@ -508,11 +542,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * BN);
       if (MODE == FWD) epilogue_fwd<T>(a, row0, rows, m, n, taddr, q, lane);
       else if (MODE == DX) epilogue_dx<T>(a, row0, rows, m, n, taddr, q, lane, cb);
-      else epilogue_dw(a, m, n, taddr, q, lane, cb);
+      else epilogue_dw(a, &tmC, stg, m, n, taddr, q, lane, cb, epi_it);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(as));
     }
+    // every reduce this warp issued has finished reading its staging buffer and written dW
+    if (MODE == DW && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -550,8 +587,9 @@ bool make_map(CUtensorMap* m, const void* ptr, int dt, uint64_t inner, uint64_t 
               uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const CUtensorMapDataType ty =
-      dt == FLCE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType ty = dt == FLCE_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dt == FLCE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {pitch_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
@@ -563,22 +601,23 @@ bool make_map(CUtensorMap* m, const void* ptr, int dt, uint64_t inner, uint64_t 
 
 template <int MODE, typename T>
 cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
-                     const CUtensorMap& B, int64_t tiles_max) {
+                     const CUtensorMap& B, const CUtensorMap& C, int64_t tiles_max) {
   auto kern = k_gemm_tc<MODE, T>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  constexpr int smem = smem_bytes<MODE>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t sms = num_sms();
   const int grid = (int)(tiles_max < sms ? tiles_max : sms);
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(A, B, a, chunk);
+  kern<<<grid, NUM_THREADS, smem, s>>>(A, B, C, a, chunk);
   return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t launch_mode(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
-                        const CUtensorMap& B, int64_t tiles_max) {
-  if (a.dt == FLCE_BF16) return launch_t<MODE, __nv_bfloat16>(a, chunk, s, A, B, tiles_max);
-  return launch_t<MODE, __half>(a, chunk, s, A, B, tiles_max);
+                        const CUtensorMap& B, const CUtensorMap& C, int64_t tiles_max) {
+  if (a.dt == FLCE_BF16) return launch_t<MODE, __nv_bfloat16>(a, chunk, s, A, B, C, tiles_max);
+  return launch_t<MODE, __half>(a, chunk, s, A, B, C, tiles_max);
 }
 
 }  // namespace tc
@@ -596,7 +635,7 @@ cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&A, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 256)) return cudaErrorInvalidValue;
   const int64_t tiles = ((a.R + 127) / 128) * a.nvt;
-  return tc::launch_mode<tc::FWD>(a, chunk, s, A, B, tiles);
+  return tc::launch_mode<tc::FWD>(a, chunk, s, A, B, A, tiles);
 }
 
 cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
@@ -605,7 +644,7 @@ cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 64)) return cudaErrorInvalidValue;
   const int64_t tiles = ((a.R + 127) / 128) * ((a.H + 255) / 256);
-  return tc::launch_mode<tc::DX>(a, chunk, s, A, B, tiles);
+  return tc::launch_mode<tc::DX>(a, chunk, s, A, B, A, tiles);
 }
 
 cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
@@ -613,8 +652,10 @@ cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 64)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 64)) return cudaErrorInvalidValue;
+  CUtensorMap C;
+  if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, 32, 32)) return cudaErrorInvalidValue;
   const int64_t tiles = ((a.V + 127) / 128) * ((a.H + 255) / 256);
-  return tc::launch_mode<tc::DW>(a, chunk, s, A, B, tiles);
+  return tc::launch_mode<tc::DW>(a, chunk, s, A, B, C, tiles);
 }
 
 }  // namespace flce

@@ -1,0 +1,40 @@
+"""Bounded pipeline waits (GPU). With FLCE_FLAG_DEBUG_STALL the tensor-core forward GEMM
+leaves one pipeline stage of each CTA unfilled — a barrier that nothing completes — so its
+waits run out after wait_timeout_ms. The call must report FLCE_ERR_TIMEOUT (no trap, no
+hang), and the context must stay usable: the next normal call gives the same result as a
+normal call before it."""
+
+import pytest
+import torch
+
+from linear_cross_entropy_logits_gb300 import build as B
+from linear_cross_entropy_logits_gb300 import flce
+from linear_cross_entropy_logits_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.build()
+    flce.load()
+
+
+def test_stalled_pipeline_reports_timeout_and_context_survives():
+    sp = I.spec("llama1b", BT=512, H=256, V=4000, w_std=0.2, ignore="random", n_ignored=64)
+    inp = I.generate(sp, seed=30)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+
+    def call(**kw):
+        return flce.fwd_bwd(d["X"], d["W"], d["targets"], None, reduction="mean", **kw)
+
+    before = call()
+    assert before["status_code"] == flce.FLCE_OK
+    stalled = call(flags=flce.FLAG_DEBUG_STALL, wait_timeout_ms=200)
+    assert stalled["status_code"] == flce.FLCE_ERR_TIMEOUT
+    after = call()
+    assert after["status_code"] == flce.FLCE_OK
+    for k in ("loss", "lse", "pred", "dX", "dW"):
+        assert torch.equal(before[k], after[k]), k
