@@ -16,14 +16,25 @@
 // accumulated straight into the caller's buffer with no [V,H] temporary ("Reduce FLCE
 // weight-gradient allocation overhead across FP16, BF16, and FP32", Proposed direction).
 //
-// Block layout (192 threads, one CTA per SM):
-//   warp 0        TMA producer (one thread)
-//   warp 1        TMEM allocator + MMA issuer (one thread)
-//   warps 2..5    epilogue; warp w reads TMEM lanes 32*(w%4) .. +31
-// Tiles: 128 (M) x 256 (N) x 64 (K) per stage, 4 stages (192 KB), two 256-column TMEM
-// accumulators so the epilogue of one tile overlaps the mainloop of the next.
-// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records FLCE_ERR_TIMEOUT,
-// waits for its own copies and MMAs in flight, frees TMEM and returns.
+// Launch shape: clusters of 2 CTAs (one CTA pair = two SMs of a TPC), one CTA per SM,
+// persistent over pair tiles of 256 (M) x 256 (N). The pair runs
+// tcgen05.mma.cta_group::2 with M = 256: each CTA stages its own 128 rows of A and one
+// half (128 rows) of B, and holds its 128 x 256 fp32 accumulator in its own TMEM. Per CTA
+// and k-block of 64 this is 32 KB of shared memory for 512 tensor cycles, two thirds of
+// the traffic of a 128 x 256 single-CTA tile, which leaves room for 6 stages (192 KB).
+//
+// Warp roles (192 threads per CTA):
+//   warp 0        TMA producer (one thread) in both CTAs; the peer's copies complete on
+//                 the leader's "full" barrier, which the leader arms for both halves
+//   warp 1        TMEM allocator (both CTAs) and, in the leader CTA, the MMA issuer (one
+//                 thread); its commits arrive on both CTAs' "empty" / "tmem full" barriers
+//   warps 2..5    epilogue in both CTAs; warp w reads TMEM lanes 32*(w%4) .. +31 and both
+//                 CTAs' epilogues arrive on the leader's "tmem empty" barrier
+// Two 256-column TMEM accumulators let the epilogue of one tile overlap the mainloop of
+// the next. Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+// FLCE_ERR_TIMEOUT, tells its peer, and both leave their loops; before TMEM is freed the
+// pair reconciles the copies each CTA issued against the leader's barriers and waits
+// (bounded) for them and for the MMAs in flight.
 #include <cuda.h>
 #include <mutex>
 #include <type_traits>
@@ -33,10 +44,13 @@
 namespace flce {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128;                            // rows of A per CTA (pair tile M = 256)
+constexpr int BN = 256;                            // pair tile N (each CTA holds BN/2 of B)
+constexpr int BK = 64;
+constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;               // 16 KB
-constexpr int B_BYTES = BN * BK * 2;               // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 48 KB
+constexpr int B_BYTES = (BN / 2) * BK * 2;         // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB per CTA
 constexpr int BOX_BYTES = 64 * 64 * 2;             // one 64x64 MN-major TMA box (8 KB)
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
@@ -47,7 +61,7 @@ constexpr int EPI_BUF_BYTES = 32 * 128;
 constexpr int EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;   // 32 KB
 template <int MODE>
 constexpr int smem_bytes() {
-  return STAGES * STAGE_BYTES + (MODE == 2 ? EPI_BYTES : 0) + 1024 + 256;
+  return STAGES * STAGE_BYTES + (MODE == 2 ? EPI_BYTES : 0) + 1024 + 512;
 }
 
 enum Mode { FWD = 0, DX = 1, DW = 2 };
@@ -58,6 +72,38 @@ __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -65,8 +111,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -85,30 +137,40 @@ __device__ __forceinline__ uint64_t gtimer() {
   return t;
 }
 
+// Where a CTA gives up: its own abort flag, the peer's (cluster address), the status word.
+struct Abort {
+  volatile int* flag;
+  uint32_t peer_flag;
+  int* status;
+  uint64_t timeout_ns;
+};
+
 // Bounded wait for the phase of `bar` with parity `parity`. Gives up (returning false)
-// when another role of the CTA has aborted (if honor_abort) or after timeout_ns, in which
-// case it raises the CTA abort flag and the device status bit.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, uint64_t timeout_ns, bool honor_abort) {
+// when this CTA has been told to abort (if honor_abort) or after timeout_ns, in which case
+// it raises both CTAs' abort flags and the device status bit.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Abort& ab, bool honor_abort) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = gtimer();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
       if (mbar_try(bar, parity)) return true;
-    if (honor_abort && *abort_flag) return false;
-    if (gtimer() - t0 > timeout_ns) {
-      *abort_flag = 1;
-      atomicOr(status, ST_TIMEOUT);
+    if (honor_abort && *ab.flag) return false;
+    if (gtimer() - t0 > ab.timeout_ns) {
+      *ab.flag = 1;
+      st_cluster_u32(ab.peer_flag, 1u);
+      atomicOr(ab.status, ST_TIMEOUT);
       return false;
     }
   }
 }
 
+// TMA tile load into this CTA's shared memory; completion is counted on `bar`, which may
+// be in either CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
       : "memory");
@@ -150,26 +212,36 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A/B format, majors,
-// N >> 3 at bit 17, M >> 4 at bit 24.
+// N >> 3 at bit 17, M >> 4 at bit 24 (M = 256: the pair's two 128-row halves).
 template <int MODE, typename T>
 __device__ __forceinline__ constexpr uint32_t make_idesc() {
   constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
   constexpr uint32_t a_mn = MODE == DW ? 1u : 0u;
   constexpr uint32_t b_mn = MODE == FWD ? 0u : 1u;
   return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | (b_mn << 16) |
-         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+// Arrive on `bar` (same offset) in both CTAs of the pair once all MMAs issued so far are
+// complete.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+// Arrive on this CTA's `bar` once all MMAs issued so far are complete.
+__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
 
@@ -207,22 +279,23 @@ template <int MODE>
 __device__ __forceinline__ TileSpace tile_space(const CallArgs& a, int rows) {
   TileSpace t;
   if (MODE == FWD) {
-    t.mt = cdiv(rows, BM);
+    t.mt = cdiv(rows, 2 * BM);
     t.nt = (int)a.nvt;
     t.nkb = cdiv((int)a.H, BK);
   } else if (MODE == DX) {
-    t.mt = cdiv(rows, BM);
+    t.mt = cdiv(rows, 2 * BM);
     t.nt = cdiv((int)a.H, BN);
     t.nkb = cdiv((int)a.V, BK);
   } else {
-    t.mt = cdiv((int)a.V, BM);
+    t.mt = cdiv((int)a.V, 2 * BM);
     t.nt = cdiv((int)a.H, BN);
     t.nkb = cdiv(rows, BK);
   }
   return t;
 }
-// FWD walks m fastest (the CTAs in flight share W tiles); DX and DW walk n fastest (the
-// CTAs in flight share the slab rows / columns).
+// Pair tiles: m indexes 256-row blocks of the output, n 256-column blocks. FWD walks m
+// fastest (the pairs in flight share W tiles); DX and DW walk n fastest (the pairs in
+// flight share the slab rows / columns).
 template <int MODE>
 __device__ __forceinline__ void tile_coords(const TileSpace& ts, int tile, int& m, int& n) {
   if (MODE == FWD) {
@@ -236,9 +309,9 @@ __device__ __forceinline__ void tile_coords(const TileSpace& ts, int tile, int& 
 
 // ------------------------------------------------------------------ epilogues
 template <typename T>
-__device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int rows, int m, int n,
+__device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int rows, int mrow, int n,
                                              uint32_t taddr, int q, int lane) {
-  const int rr = m * BM + q * 32 + lane;  // row within the chunk
+  const int rr = mrow + q * 32 + lane;  // row within the chunk
   const bool valid = rr < rows;
   const int V = (int)a.V;
   int64_t tg = -1;
@@ -311,9 +384,9 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
 }
 
 template <typename T>
-__device__ __forceinline__ void epilogue_dx(const CallArgs& a, int row0, int rows, int m, int n,
+__device__ __forceinline__ void epilogue_dx(const CallArgs& a, int row0, int rows, int mrow, int n,
                                             uint32_t taddr, int q, int lane, float cb) {
-  const int rr = m * BM + q * 32 + lane;
+  const int rr = mrow + q * 32 + lane;
   const bool valid = rr < rows;
   const int H = (int)a.H;
   const int64_t orow = valid ? (int64_t)a.w.idx[row0 + rr] : 0;
@@ -345,10 +418,10 @@ __device__ __forceinline__ void epilogue_dx(const CallArgs& a, int row0, int row
 // the box into dW in L2. Each dW element gets exactly one add per launch (one owning CTA),
 // so the result does not depend on timing. Boxes past V or H are clipped by the TMA unit.
 __device__ __forceinline__ void epilogue_dw(const CallArgs& a, const CUtensorMap* tmC, uint8_t* stg,
-                                            int m, int n, uint32_t taddr, int q, int lane, float cb,
+                                            int mrow, int n, uint32_t taddr, int q, int lane, float cb,
                                             uint32_t& epi_it) {
   const int H = (int)a.H;
-  const int y = m * BM + q * 32;
+  const int y = mrow + q * 32;
   if (y >= (int)a.V) return;  // this warp's 32 rows lie past V (warp-uniform)
 #pragma unroll 1
   for (int cc = 0; cc < BN / 32; ++cc) {
@@ -386,7 +459,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
   const TileSpace ts = tile_space<MODE>(a, rows);
   const int ntiles = ts.mt * ts.nt;
-  if ((int)blockIdx.x >= ntiles || ts.nkb <= 0) return;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = (int)cluster_id_x(), npairs = (int)nclusters_x();
+  // both CTAs of a pair take the same decision
+  if (pair >= ntiles || ts.nkb <= 0) return;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -394,6 +471,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES + (MODE == DW ? EPI_BYTES : 0));
   uint32_t* tmem_slot = (uint32_t*)(bars + NUM_BARS);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  int* copies = (int*)(tmem_slot + 2);  // per stage: phases this CTA's producer filled / armed
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -402,17 +480,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* status = a.w.status;
-  const uint64_t tmo = a.timeout_ns;
+  const Abort ab{abort_flag, mapa(smem_u32((const void*)abort_flag), rank ^ 1u), a.w.status, a.timeout_ns};
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(full_bar(s), 1);   // leader: one arrive (its expect_tx for both halves)
+      mbar_init(empty_bar(s), 1);  // one MMA commit per phase (multicast to both CTAs)
+      copies[s] = 0;
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(tfull_bar(s), 1);
-      mbar_init(tempty_bar(s), 4);
+      mbar_init(tfull_bar(s), 1);   // one MMA commit per tile (multicast)
+      mbar_init(tempty_bar(s), 8);  // leader: 4 local + 4 peer epilogue warps
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -421,83 +499,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(TMEM_COLS)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (both CTAs)
       int s = 0;
       uint32_t ph = 0;
-      uint32_t armed = 0, last_par = 0;
-      bool ok = true;
-      const bool stall = (a.flags & FLCE_FLAG_DEBUG_STALL) && MODE == FWD;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+      const bool stall = (a.flags & FLCE_FLAG_DEBUG_STALL) && MODE == FWD && leader;
+      const int half = (int)rank * BM;  // this CTA's 128-row half of A and of B
+      for (int tile = pair; tile < ntiles; tile += npairs) {
         int m, n;
         tile_coords<MODE>(ts, tile, m, n);
-        for (int kb = 0; kb < ts.nkb; ++kb) {
-          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, status, tmo, true)) {
-            ok = false;
-            break;
-          }
-          if (!(stall && tile == (int)blockIdx.x && kb == ts.nkb - 1)) {
-            const uint32_t fb = full_bar(s);
+        int kb = 0;
+        for (; kb < ts.nkb; ++kb) {
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, ab, true)) break;
+          const uint32_t fb = leader ? full_bar(s) : mapa(full_bar(s), 0);
+          if (leader) mbar_expect_tx(full_bar(s), 2 * STAGE_BYTES);
+          if (!(stall && tile == pair && kb == ts.nkb - 1)) {
             const uint32_t adst = smem_u32(smem + s * STAGE_BYTES);
             const uint32_t bdst = adst + A_BYTES;
-            mbar_expect_tx(fb, STAGE_BYTES);
             if (MODE == FWD) {
-              tma_load_2d(adst, &tmA, fb, kb * BK, m * BM);
-              tma_load_2d(bdst, &tmB, fb, kb * BK, n * BN);
+              tma_load_2d(adst, &tmA, fb, kb * BK, m * 2 * BM + half);
+              tma_load_2d(bdst, &tmB, fb, kb * BK, n * BN + half);
             } else if (MODE == DX) {
-              tma_load_2d(adst, &tmA, fb, kb * BK, m * BM);
+              tma_load_2d(adst, &tmA, fb, kb * BK, m * 2 * BM + half);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) tma_load_2d(bdst + j * BOX_BYTES, &tmB, fb, n * BN + j * 64, kb * BK);
+              for (int j = 0; j < 2; ++j) tma_load_2d(bdst + j * BOX_BYTES, &tmB, fb, n * BN + half + j * 64, kb * BK);
             } else {
 #pragma unroll
-              for (int j = 0; j < 2; ++j) tma_load_2d(adst + j * BOX_BYTES, &tmA, fb, m * BM + j * 64, kb * BK);
+              for (int j = 0; j < 2; ++j) tma_load_2d(adst + j * BOX_BYTES, &tmA, fb, m * 2 * BM + half + j * 64, kb * BK);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) tma_load_2d(bdst + j * BOX_BYTES, &tmB, fb, n * BN + j * 64, kb * BK);
+              for (int j = 0; j < 2; ++j) tma_load_2d(bdst + j * BOX_BYTES, &tmB, fb, n * BN + half + j * 64, kb * BK);
             }
-            armed |= 1u << s;
-            last_par = (last_par & ~(1u << s)) | (ph << s);
           }
+          copies[s] += 1;  // leader: phases armed; peer: phases filled
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
+        if (kb < ts.nkb) break;
       }
-      // Every copy this thread issued lands before the CTA may exit.
-      for (int i = 0; i < STAGES; ++i)
-        if (armed & (1u << i)) wait_bounded(full_bar(i), (last_par >> i) & 1u, abort_flag, status, tmo, false);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (leader CTA)
       constexpr uint32_t idesc = make_idesc<MODE, T>();
       int s = 0;
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++it) {
+      for (int tile = pair; ok && tile < ntiles; tile += npairs, ++it) {
         const int as = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-        if (!wait_bounded(tempty_bar(as), aph ^ 1u, abort_flag, status, tmo, true)) {
+        if (!wait_bounded(tempty_bar(as), aph ^ 1u, ab, true)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(as * BN);
         for (int kb = 0; kb < ts.nkb; ++kb) {
-          if (!wait_bounded(full_bar(s), ph, abort_flag, status, tmo, true)) {
+          if (!wait_bounded(full_bar(s), ph, ab, true)) {
             ok = false;
             break;
           }
@@ -510,53 +582,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t bd = MODE == FWD ? sdesc(bbase + k * 32, 16, 1024) : sdesc(bbase + k * 2048, 8192, 1024);
             mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          mma_commit(empty_bar(s));
+          mma_commit_pair(empty_bar(s));
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(as));
+        mma_commit_pair(tfull_bar(as));
       }
-      // Every MMA this thread issued completes before TMEM is freed.
-      mma_commit(drain_bar);
-      wait_bounded(drain_bar, 0u, abort_flag, status, tmo, false);
+      // every MMA issued completes before TMEM is freed or shared memory released
+      mma_commit_local(drain_bar);
+      wait_bounded(drain_bar, 0u, ab, false);
     }
   } else {
-    // ---------------- epilogue warps 2..5
+    // ---------------- epilogue warps 2..5 (both CTAs)
     const int q = warp & 3;
     const float cb = MODE == FWD ? 0.0f : a.w.ctrl->cbar;
     uint8_t* stg = epi_stage + (warp - 2) * 2 * EPI_BUF_BYTES;
     uint32_t epi_it = 0;
     int it = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+    for (int tile = pair; tile < ntiles; tile += npairs, ++it) {
       const int as = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-      bool ok = wait_bounded(tfull_bar(as), aph, abort_flag, status, tmo, true);
+      bool ok = wait_bounded(tfull_bar(as), aph, ab, true);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       int m, n;
       tile_coords<MODE>(ts, tile, m, n);
+      const int mrow = m * 2 * BM + (int)rank * BM;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * BN);
-      if (MODE == FWD) epilogue_fwd<T>(a, row0, rows, m, n, taddr, q, lane);
-      else if (MODE == DX) epilogue_dx<T>(a, row0, rows, m, n, taddr, q, lane, cb);
-      else epilogue_dw(a, &tmC, stg, m, n, taddr, q, lane, cb, epi_it);
+      if (MODE == FWD) epilogue_fwd<T>(a, row0, rows, mrow, n, taddr, q, lane);
+      else if (MODE == DX) epilogue_dx<T>(a, row0, rows, mrow, n, taddr, q, lane, cb);
+      else epilogue_dw(a, &tmC, stg, mrow, n, taddr, q, lane, cb, epi_it);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(as));
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty_bar(as));
+        else mbar_arrive_cluster(mapa(tempty_bar(as), 0));
+      }
     }
     // every reduce this warp issued has finished reading its staging buffer and written dW
     if (MODE == DW && lane == 0) bulk_wait_all();
     __syncwarp();
   }
 
+  // ---------------- teardown
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // no role of either CTA issues anything after this point
+  if (warp == 0 && lane == 0 && leader) {
+    // Every copy either CTA issued must land before the pair frees its shared memory. The
+    // peer's copies complete on the leader's barriers; an aborted pipeline can leave the
+    // two producers one phase apart on a stage, which is reconciled here.
+    for (int s = 0; s < STAGES; ++s) {
+      const int mine = copies[s];
+      const int peer = (int)ld_cluster_u32(mapa(smem_u32(&copies[s]), 1));
+      int last = mine;
+      if (peer > mine) {
+        mbar_expect_tx(full_bar(s), STAGE_BYTES);  // arm the phase only the peer filled
+        last = peer;
+      } else if (peer < mine) {
+        mbar_complete_tx(full_bar(s), STAGE_BYTES);  // the peer's half never came
+      }
+      if (last > 0) wait_bounded(full_bar(s), (uint32_t)(last - 1) & 1u, ab, false);
+    }
+  }
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                  : "memory");
   }
 }
@@ -599,17 +694,47 @@ bool make_map(CUtensorMap* m, const void* ptr, int dt, uint64_t inner, uint64_t 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch as clusters of 2 CTAs, one pair per pair tile up to the number of pairs that fit
+// the GPU at once (persistent).
 template <int MODE, typename T>
 cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
-                     const CUtensorMap& B, const CUtensorMap& C, int64_t tiles_max) {
+                     const CUtensorMap& B, const CUtensorMap& C, int64_t pair_tiles_max) {
   auto kern = k_gemm_tc<MODE, T>;
   constexpr int smem = smem_bytes<MODE>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static int max_pairs[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int64_t sms = num_sms();
-  const int grid = (int)(tiles_max < sms ? tiles_max : sms);
-  if (grid <= 0) return cudaSuccess;
-  kern<<<grid, NUM_THREADS, smem, s>>>(A, B, C, a, chunk);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dev < 0 || dev >= 64 || max_pairs[dev] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (unsigned)(num_sms() / 2), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    if (dev >= 0 && dev < 64) max_pairs[dev] = n;
+    else return cudaErrorInvalidDevice;
+  } else {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t pairs = pair_tiles_max < max_pairs[dev] ? pair_tiles_max : max_pairs[dev];
+  if (pairs <= 0) return cudaSuccess;
+  cfg.gridDim = dim3(2 * (unsigned)pairs, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, A, B, C, a, chunk);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -633,8 +758,8 @@ cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   CUtensorMap A, B;
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 128)) return cudaErrorInvalidValue;
-  if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 256)) return cudaErrorInvalidValue;
-  const int64_t tiles = ((a.R + 127) / 128) * a.nvt;
+  if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 128)) return cudaErrorInvalidValue;
+  const int64_t tiles = ((a.R + 255) / 256) * a.nvt;
   return tc::launch_mode<tc::FWD>(a, chunk, s, A, B, A, tiles);
 }
 
@@ -643,7 +768,7 @@ cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 64)) return cudaErrorInvalidValue;
-  const int64_t tiles = ((a.R + 127) / 128) * ((a.H + 255) / 256);
+  const int64_t tiles = ((a.R + 255) / 256) * ((a.H + 255) / 256);
   return tc::launch_mode<tc::DX>(a, chunk, s, A, B, A, tiles);
 }
 
@@ -654,7 +779,7 @@ cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&B, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 64)) return cudaErrorInvalidValue;
   CUtensorMap C;
   if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, 32, 32)) return cudaErrorInvalidValue;
-  const int64_t tiles = ((a.V + 127) / 128) * ((a.H + 255) / 256);
+  const int64_t tiles = ((a.V + 255) / 256) * ((a.H + 255) / 256);
   return tc::launch_mode<tc::DW>(a, chunk, s, A, B, C, tiles);
 }
 
