@@ -54,6 +54,8 @@ bool plan_layout(int64_t BT, int64_t H, int64_t V, int dt, int64_t R, Plan* p) {
   q.off_lse = take(4 * (size_t)R);
   q.off_arow = take(4 * (size_t)R);
   q.off_slab = take((size_t)R * q.Vp * q.esz);
+  // fp32 dX accumulator of the tensor-core path (16-bit inputs only)
+  q.off_dxacc = take(q.esz == 2 ? (size_t)R * H * 4 : 0);
   q.total = off;
   *p = q;
   return true;
@@ -92,6 +94,7 @@ Work make_work(const Plan& p, void* ws, int32_t* user_status) {
   w.lse = (float*)(b + p.off_lse);
   w.arow = (float*)(b + p.off_arow);
   w.slab = b + p.off_slab;
+  w.dxacc = (float*)(b + p.off_dxacc);
   w.status = user_status ? (int*)user_status : &w.ctrl->status;
   return w;
 }
@@ -280,9 +283,19 @@ extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
                     [&] { return tc ? launch_fwd_tc(a, k, s) : launch_fwd_simt(a, k, s); }));
     FLCE_TRY(staged(prof, FLCE_STAGE_FINALIZE, 1, s, [&] { return launch_finalize(a, k, s); }));
     if (grads) FLCE_TRY(staged(prof, FLCE_STAGE_GPASS, 1, s, [&] { return launch_gpass(a, k, s); }));
-    if (a.want_dX)
-      FLCE_TRY(staged(prof, FLCE_STAGE_DX, 1, s,
-                      [&] { return tc ? launch_dx_tc(a, k, s) : launch_dx_simt(a, k, s); }));
+    if (a.want_dX) {
+      if (tc) {
+        FLCE_TRY(staged(prof, FLCE_STAGE_DX, 2, s, [&] {
+          cudaError_t e = cudaMemsetAsync(a.w.dxacc, 0, (size_t)a.R * a.H * 4, s);
+          if (e != cudaSuccess) return e;
+          e = launch_dx_tc(a, k, s);
+          if (e != cudaSuccess) return e;
+          return launch_dx_store(a, k, s);
+        }));
+      } else {
+        FLCE_TRY(staged(prof, FLCE_STAGE_DX, 1, s, [&] { return launch_dx_simt(a, k, s); }));
+      }
+    }
     if (a.want_dW)
       FLCE_TRY(staged(prof, FLCE_STAGE_DW, 1, s,
                       [&] { return tc ? launch_dw_tc(a, k, s) : launch_dw_simt(a, k, s); }));

@@ -44,7 +44,7 @@ struct Plan {
   int64_t R;     // max rows per chunk (multiple of 128)
   int64_t kmax;  // chunks the host enqueues = cdiv(BT, R)
   size_t off_ctrl, off_idx, off_rloss, off_rz, off_racc;
-  size_t off_xc, off_stm, off_sts, off_sti, off_tgt, off_lse, off_arow, off_slab;
+  size_t off_xc, off_stm, off_sts, off_sti, off_tgt, off_lse, off_arow, off_slab, off_dxacc;
   size_t total;
 };
 
@@ -67,6 +67,7 @@ struct Work {
   float* lse;      // [R] row logsumexp
   float* arow;     // [R] per-row factor a_i (g_i for none, 1 otherwise)
   void* slab;      // [R, Vp] exp(s - tile max), then G, in the input dtype
+  float* dxacc;    // [R, H] fp32 dX accumulator of the tensor-core path (stream-K halves)
   int* status;     // device status word
 };
 Work make_work(const Plan& p, void* ws, int32_t* user_status);
@@ -113,6 +114,7 @@ bool tc_supported(const CallArgs& a);
 cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_dx_store(const CallArgs& a, int chunk, cudaStream_t s);  // dxacc -> dX rows
 
 int num_sms();
 

@@ -276,7 +276,6 @@ __global__ void __launch_bounds__(256) k_gpass(const __grid_constant__ CallArgs 
   const int rb0 = blockIdx.y * rows_per_block;
   const int rb1 = min(rb0 + rows_per_block, rlim);
   const int64_t c0 = (int64_t)t * VT + tx * 8;
-  const int64_t R = a.R;
   T* slab = (T*)a.w.slab;
   float cs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int r = rb0 + ty; r < rb1; r += 8) {
@@ -546,6 +545,24 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const __grid_constant__ CallA
   }
 }
 
+// dX rows of the chunk: dX[idx[row0 + r]] = dxacc[r] in the input dtype (the tensor-core
+// dX GEMM accumulates cbar * G W into the fp32 buffer dxacc).
+template <typename T>
+__global__ void __launch_bounds__(256) k_dx_store(const __grid_constant__ CallArgs a, int chunk) {
+  int row0, rows;
+  if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  const int64_t H = a.H;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const float* src = a.w.dxacc + (int64_t)r * H;
+    T* dst = (T*)a.dX + (int64_t)a.w.idx[row0 + r] * H;
+    for (int64_t j = (int64_t)threadIdx.x * 8; j < H; j += (int64_t)blockDim.x * 8) {
+      float f[8];
+      Vec8<float>::load(src + j, f);
+      Vec8<T>::store(dst + j, f);
+    }
+  }
+}
+
 template <typename T>
 cudaError_t gpass_t(const CallArgs& a, int chunk, cudaStream_t s) {
   const bool dbias = a.want_dW && a.bias != nullptr && a.dbias != nullptr;
@@ -614,6 +631,13 @@ cudaError_t launch_dw_simt(const CallArgs& a, int chunk, cudaStream_t s) {
     case FLCE_F16: k_gemm_simt<__half, 1><<<grid, 256, 0, s>>>(a, chunk); break;
     default: k_gemm_simt<float, 1><<<grid, 256, 0, s>>>(a, chunk); break;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dx_store(const CallArgs& a, int chunk, cudaStream_t s) {
+  const int64_t blocks = a.R < 8LL * num_sms() ? a.R : 8LL * num_sms();
+  if (a.dt == FLCE_BF16) k_dx_store<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(a, chunk);
+  else k_dx_store<__half><<<(unsigned)blocks, 256, 0, s>>>(a, chunk);
   return cudaGetLastError();
 }
 

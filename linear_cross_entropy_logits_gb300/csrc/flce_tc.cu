@@ -7,7 +7,9 @@
 //        vocabulary tile it keeps the max, the sum of exp(s - max), the lowest-index
 //        argmax and the target logit, and stores exp(s - max) (in the input dtype) into
 //        the chunk slab, from which the gradient is formed once the row's lse is known.
-//   DX:  dX[idx] = cbar * G W (K = V), written through the compaction index.
+//   DX:  dX[idx] = cbar * G W (K = V): tiles (optionally split in two K halves) added by
+//        TMA reduce-add into a zeroed fp32 chunk buffer, then scattered to the dX rows
+//        through the compaction index by k_dx_store.
 //   DW:  dW += cbar * G^T Xc (K = chunk rows), added into the fp32 destination by TMA
 //        reduce-add from the single CTA that owns each tile (one add per element per
 //        launch: deterministic).
@@ -47,21 +49,26 @@ namespace tc {
 constexpr int BM = 128;                            // rows of A per CTA (pair tile M = 256)
 constexpr int BN = 256;                            // pair tile N (each CTA holds BN/2 of B)
 constexpr int BK = 64;
-constexpr int STAGES = 6;
+// Pipeline depth: 6 stages of 32 KB (192 KB); DX and DW add 32 KB of epilogue staging.
+template <int MODE>
+constexpr int stages_of() {
+  return 6;
+}
+constexpr int MAX_STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;               // 16 KB
 constexpr int B_BYTES = (BN / 2) * BK * 2;         // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB per CTA
 constexpr int BOX_BYTES = 64 * 64 * 2;             // one 64x64 MN-major TMA box (8 KB)
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_BARS = 2 * STAGES + 5;           // full, empty, tfull[2], tempty[2], drain
-// DW epilogue staging: per epilogue warp, two 32-row x 128-byte buffers that feed TMA
-// reduce-add (the L2 performs dW += tile; no register read-modify-write).
+constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tfull[2], tempty[2], drain
+// DX/DW epilogue staging: per epilogue warp, two 32-row x 128-byte buffers that feed TMA
+// reduce-add (the L2 performs dst += tile; no register read-modify-write).
 constexpr int EPI_BUF_BYTES = 32 * 128;
 constexpr int EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;   // 32 KB
 template <int MODE>
 constexpr int smem_bytes() {
-  return STAGES * STAGE_BYTES + (MODE == 2 ? EPI_BYTES : 0) + 1024 + 512;
+  return stages_of<MODE>() * STAGE_BYTES + (MODE != 0 ? EPI_BYTES : 0) + 1024 + 512;
 }
 
 enum Mode { FWD = 0, DX = 1, DW = 2 };
@@ -131,6 +138,20 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try, but the thread may sleep up to `hint_ns` waiting for the phase (it resumes
+// as soon as the phase completes), so waiting warps take no issue slots from the warps
+// that feed the tensor cores.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -152,9 +173,7 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const A
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = gtimer();
   for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try(bar, parity)) return true;
+    if (mbar_try_sleep(bar, parity, 50000u)) return true;
     if (honor_abort && *ab.flag) return false;
     if (gtimer() - t0 > ab.timeout_ns) {
       *ab.flag = 1;
@@ -307,6 +326,36 @@ __device__ __forceinline__ void tile_coords(const TileSpace& ts, int tile, int& 
   }
 }
 
+// Work items of one pair: (pair tile, k-block range), taken round-robin over the pairs so
+// that the pairs in flight walk the same k-blocks in step and share operand tiles in L2.
+// FWD and DW take whole tiles. DX (few, long tiles: K = V) may split each tile's K range
+// in two halves (items ordered split-major: all first halves, then all second halves)
+// when that fills the last wave better; the two partial sums are added into a zeroed
+// buffer, so the result does not depend on their order.
+__device__ __forceinline__ int dx_splits(int ntiles, int npairs) {
+  const int w1 = (ntiles + npairs - 1) / npairs, w2 = (2 * ntiles + npairs - 1) / npairs;
+  // wave efficiency ntiles*S / (waves*P): compare ntiles/w1 with 2*ntiles/w2
+  return (2 * ntiles) * w1 > ntiles * w2 + (ntiles * w2) / 50 ? 2 : 1;
+}
+template <int MODE>
+struct Items {
+  int i, nitems, npairs, ntiles, nkb, S;
+  __device__ __forceinline__ Items(int pair, int npairs_, int ntiles_, int nkb_)
+      : i(pair), npairs(npairs_), ntiles(ntiles_), nkb(nkb_) {
+    S = (MODE == DX && nkb_ >= 2) ? dx_splits(ntiles_, npairs_) : 1;
+    nitems = S * ntiles_;
+  }
+  __device__ __forceinline__ bool next(int& t, int& k0, int& k1) {
+    if (i >= nitems) return false;
+    const int s = i / ntiles;
+    t = i - s * ntiles;
+    k0 = (int)((int64_t)nkb * s / S);
+    k1 = (int)((int64_t)nkb * (s + 1) / S);
+    i += npairs;
+    return true;
+  }
+};
+
 // ------------------------------------------------------------------ epilogues
 template <typename T>
 __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int rows, int mrow, int n,
@@ -383,46 +432,19 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
   }
 }
 
-template <typename T>
-__device__ __forceinline__ void epilogue_dx(const CallArgs& a, int row0, int rows, int mrow, int n,
-                                            uint32_t taddr, int q, int lane, float cb) {
-  const int rr = mrow + q * 32 + lane;
-  const bool valid = rr < rows;
-  const int H = (int)a.H;
-  const int64_t orow = valid ? (int64_t)a.w.idx[row0 + rr] : 0;
-  T* drow = (T*)a.dX + orow * a.H;
-#pragma unroll 1
-  for (int cc = 0; cc < BN / 32; ++cc) {
-    uint32_t r[32];
-    tmem_ld32(taddr + cc * 32, r);
-    const int h0 = n * BN + cc * 32;
-    if (valid && h0 < H) {
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        if (h0 + g * 8 < H) {
-          uint4 u;
-          u.x = pack2<T>(cb * __uint_as_float(r[g * 8 + 0]), cb * __uint_as_float(r[g * 8 + 1]));
-          u.y = pack2<T>(cb * __uint_as_float(r[g * 8 + 2]), cb * __uint_as_float(r[g * 8 + 3]));
-          u.z = pack2<T>(cb * __uint_as_float(r[g * 8 + 4]), cb * __uint_as_float(r[g * 8 + 5]));
-          u.w = pack2<T>(cb * __uint_as_float(r[g * 8 + 6]), cb * __uint_as_float(r[g * 8 + 7]));
-          *(uint4*)(drow + h0 + g * 8) = u;
-        }
-      }
-    }
-  }
-}
-
-// dW tile += cbar * acc through TMA reduce-add. Each epilogue warp owns 32 rows (its TMEM
-// lane quadrant) and stages 32 columns at a time (32 x 128 B, 128-byte swizzle: 16-byte
-// chunk j of row r sits at chunk j ^ (r % 8)), alternating two buffers; the TMA unit adds
-// the box into dW in L2. Each dW element gets exactly one add per launch (one owning CTA),
-// so the result does not depend on timing. Boxes past V or H are clipped by the TMA unit.
-__device__ __forceinline__ void epilogue_dw(const CallArgs& a, const CUtensorMap* tmC, uint8_t* stg,
-                                            int mrow, int n, uint32_t taddr, int q, int lane, float cb,
-                                            uint32_t& epi_it) {
+// dst tile += cbar * acc through TMA reduce-add (dst = dW for DW, the fp32 dX accumulator
+// for DX). Each epilogue warp owns 32 rows (its TMEM lane quadrant) and stages 32 columns
+// at a time (32 x 128 B, 128-byte swizzle: 16-byte chunk j of row r sits at chunk
+// j ^ (r % 8)), alternating two buffers; the TMA unit adds the box into dst in L2. A dW
+// element gets exactly one add per launch (one owning pair); a dX accumulator element at
+// most two (stream-K), added to zero: either way the result does not depend on timing.
+// Boxes past the destination's extent are clipped by the TMA unit.
+__device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtensorMap* tmC, uint8_t* stg,
+                                                int mrow, int n, int ylimit, uint32_t taddr, int q,
+                                                int lane, float cb, uint32_t& epi_it) {
   const int H = (int)a.H;
   const int y = mrow + q * 32;
-  if (y >= (int)a.V) return;  // this warp's 32 rows lie past V (warp-uniform)
+  if (y >= ylimit) return;  // this warp's 32 rows lie past the destination (warp-uniform)
 #pragma unroll 1
   for (int cc = 0; cc < BN / 32; ++cc) {
     const int x = n * BN + cc * 32;
@@ -455,6 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CallArgs a,
               const int chunk) {
+  constexpr int STAGES = stages_of<MODE>();
   int row0 = 0, rows = 0;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
   const TileSpace ts = tile_space<MODE>(a, rows);
@@ -463,12 +486,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const bool leader = rank == 0;
   const int pair = (int)cluster_id_x(), npairs = (int)nclusters_x();
   // both CTAs of a pair take the same decision
-  if (pair >= ntiles || ts.nkb <= 0) return;
+  if (ts.nkb <= 0 || pair >= Items<MODE>(0, npairs, ntiles, ts.nkb).nitems) return;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;  // DW only
-  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES + (MODE == DW ? EPI_BYTES : 0));
+  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;  // DX and DW only
+  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES + (MODE != FWD ? EPI_BYTES : 0));
   uint32_t* tmem_slot = (uint32_t*)(bars + NUM_BARS);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   int* copies = (int*)(tmem_slot + 2);  // per stage: phases this CTA's producer filled / armed
@@ -517,15 +540,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t ph = 0;
       const bool stall = (a.flags & FLCE_FLAG_DEBUG_STALL) && MODE == FWD && leader;
       const int half = (int)rank * BM;  // this CTA's 128-row half of A and of B
-      for (int tile = pair; tile < ntiles; tile += npairs) {
+      Items<MODE> items(pair, npairs, ntiles, ts.nkb);
+      int tile, k0, k1;
+      bool first = true;
+      while (items.next(tile, k0, k1)) {
         int m, n;
         tile_coords<MODE>(ts, tile, m, n);
-        int kb = 0;
-        for (; kb < ts.nkb; ++kb) {
+        int kb = k0;
+        for (; kb < k1; ++kb) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, ab, true)) break;
           const uint32_t fb = leader ? full_bar(s) : mapa(full_bar(s), 0);
           if (leader) mbar_expect_tx(full_bar(s), 2 * STAGE_BYTES);
-          if (!(stall && tile == pair && kb == ts.nkb - 1)) {
+          if (!(stall && first && kb == k1 - 1)) {
             const uint32_t adst = smem_u32(smem + s * STAGE_BYTES);
             const uint32_t bdst = adst + A_BYTES;
             if (MODE == FWD) {
@@ -548,7 +574,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ph ^= 1u;
           }
         }
-        if (kb < ts.nkb) break;
+        if (kb < k1) break;
+        first = false;
       }
     }
   } else if (warp == 1) {
@@ -559,7 +586,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t ph = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < ntiles; tile += npairs, ++it) {
+      Items<MODE> items(pair, npairs, ntiles, ts.nkb);
+      int tile, k0, k1;
+      for (; ok && items.next(tile, k0, k1); ++it) {
         const int as = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
         if (!wait_bounded(tempty_bar(as), aph ^ 1u, ab, true)) {
@@ -568,7 +597,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(as * BN);
-        for (int kb = 0; kb < ts.nkb; ++kb) {
+        for (int kb = k0; kb < k1; ++kb) {
           if (!wait_bounded(full_bar(s), ph, ab, true)) {
             ok = false;
             break;
@@ -580,7 +609,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = MODE == DW ? sdesc(abase + k * 2048, 8192, 1024) : sdesc(abase + k * 32, 16, 1024);
             const uint64_t bd = MODE == FWD ? sdesc(bbase + k * 32, 16, 1024) : sdesc(bbase + k * 2048, 8192, 1024);
-            mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            mma_f16(d, ad, bd, idesc, (kb != k0 || k != 0) ? 1u : 0u);
           }
           mma_commit_pair(empty_bar(s));
           if (++s == STAGES) {
@@ -602,7 +631,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* stg = epi_stage + (warp - 2) * 2 * EPI_BUF_BYTES;
     uint32_t epi_it = 0;
     int it = 0;
-    for (int tile = pair; tile < ntiles; tile += npairs, ++it) {
+    Items<MODE> items(pair, npairs, ntiles, ts.nkb);
+    int tile, k0, k1;
+    for (; items.next(tile, k0, k1); ++it) {
       const int as = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
       bool ok = wait_bounded(tfull_bar(as), aph, ab, true);
@@ -614,8 +645,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int mrow = m * 2 * BM + (int)rank * BM;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * BN);
       if (MODE == FWD) epilogue_fwd<T>(a, row0, rows, mrow, n, taddr, q, lane);
-      else if (MODE == DX) epilogue_dx<T>(a, row0, rows, mrow, n, taddr, q, lane, cb);
-      else epilogue_dw(a, &tmC, stg, mrow, n, taddr, q, lane, cb, epi_it);
+      else epilogue_reduce(a, &tmC, stg, mrow, n, MODE == DX ? (int)a.R : (int)a.V, taddr, q, lane, cb, epi_it);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -623,8 +653,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         else mbar_arrive_cluster(mapa(tempty_bar(as), 0));
       }
     }
-    // every reduce this warp issued has finished reading its staging buffer and written dW
-    if (MODE == DW && lane == 0) bulk_wait_all();
+    // every reduce this warp issued has finished reading its staging buffer and written
+    if (MODE != FWD && lane == 0) bulk_wait_all();
     __syncwarp();
   }
 
@@ -768,8 +798,10 @@ cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 64)) return cudaErrorInvalidValue;
-  const int64_t tiles = ((a.R + 255) / 256) * ((a.H + 255) / 256);
-  return tc::launch_mode<tc::DX>(a, chunk, s, A, B, A, tiles);
+  CUtensorMap C;
+  if (!tc::make_map(&C, a.w.dxacc, FLCE_F32, a.H, a.R, a.H * 4, 32, 32)) return cudaErrorInvalidValue;
+  const int64_t tiles = 2 * ((a.R + 255) / 256) * ((a.H + 255) / 256);  // up to 2 K halves
+  return tc::launch_mode<tc::DX>(a, chunk, s, A, B, C, tiles);
 }
 
 cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
