@@ -201,6 +201,10 @@ FLCE_API void flce_profile_destroy(flce_profile* prof);
  * each array are written (up to FLCE_STAGE_COUNT). Returns FLCE_OK or FLCE_ERR_CUDA. */
 FLCE_API int32_t flce_profile_read(flce_profile* prof, float* ms, int32_t* launches, int32_t n);
 
+/* Name of the CUDA runtime error behind the last FLCE_ERR_CUDA returned on this host
+ * thread ("cudaSuccess" if none). The string is static; do not free it. */
+FLCE_API const char* flce_last_cuda_error(void);
+
 /* Human-readable name of an flce_status value. */
 FLCE_API const char* flce_status_string(int32_t code);
 

@@ -138,6 +138,10 @@ static int32_t validate(const flce_args* x) {
 
 using namespace flce;
 
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+extern "C" const char* flce_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
+
 struct flce_profile {
   std::vector<cudaEvent_t> ev;  // pairs: ev[2i] before, ev[2i+1] after launch i
   std::vector<int> stage;       // stage of pair i
@@ -269,9 +273,13 @@ extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
   const bool tc = !(x->flags & FLCE_FLAG_FORCE_SIMT) && tc_supported(a);
   const bool grads = a.want_dX || a.want_dW;
 
-#define FLCE_TRY(expr)                          \
-  do {                                          \
-    if ((expr) != cudaSuccess) return FLCE_ERR_CUDA; \
+#define FLCE_TRY(expr)                    \
+  do {                                    \
+    const cudaError_t e_ = (expr);        \
+    if (e_ != cudaSuccess) {              \
+      g_last_cuda_error = e_;             \
+      return FLCE_ERR_CUDA;               \
+    }                                     \
   } while (0)
 
   flce_profile* prof = x->profile;

@@ -25,7 +25,7 @@ FLAG_DEBUG_STALL = 0x100
 EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_fwd_bwd_noalloc",
             "flce_get_status",
             "flce_profile_create", "flce_profile_reset", "flce_profile_destroy",
-            "flce_profile_read", "flce_status_string", "flce_abi_version")
+            "flce_profile_read", "flce_last_cuda_error", "flce_status_string", "flce_abi_version")
 STAGES = ("prologue", "gather", "fwd", "finalize", "gpass", "dx", "dw", "reduce")
 
 
@@ -73,6 +73,8 @@ def load(path: str | None = None):
     lib.flce_status_string.restype = ctypes.c_char_p
     lib.flce_status_string.argtypes = [ctypes.c_int32]
     lib.flce_abi_version.restype = ctypes.c_int32
+    lib.flce_last_cuda_error.restype = ctypes.c_char_p
+    lib.flce_last_cuda_error.argtypes = []
     lib.flce_profile_create.restype = ctypes.c_void_p
     lib.flce_profile_create.argtypes = []
     lib.flce_profile_reset.restype = None
@@ -89,7 +91,10 @@ def load(path: str | None = None):
 class FlceError(RuntimeError):
     def __init__(self, code, where):
         self.code = code
-        super().__init__(f"{where}: {status_string(code)}")
+        msg = f"{where}: {status_string(code)}"
+        if code == FLCE_ERR_CUDA:
+            msg += f" ({load().flce_last_cuda_error().decode()})"
+        super().__init__(msg)
 
 
 def status_string(code: int) -> str:
