@@ -376,7 +376,8 @@ def run_ours(args):
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_kind": f"bf16 sustained ({peak_src})",
                 "per_launch": f"2*H*V FLOPs per labelled row x {n_lab * args.steps / max(dom_launches, 1):.0f} rows per launch",
-                "traffic": (rec["traffic_bytes_per_launch"] if rec and rec.get("kernel") == dom else None)}
+                "traffic": (rec["per_launch_bytes"].get(dom) if rec else None),
+                "traffic_source": "profiles/traffic.json (ncu, full size)" if rec else None}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks.get("hbm_gbs"),
                 "unit": "GB/s", "frac": None, "traffic": None}
