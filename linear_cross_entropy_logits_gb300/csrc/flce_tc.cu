@@ -62,13 +62,14 @@ constexpr int BOX_BYTES = 64 * 64 * 2;             // one 64x64 MN-major TMA box
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tfull[2], tempty[2], drain
-// DX/DW epilogue staging: per epilogue warp, two 32-row x 128-byte buffers that feed TMA
-// reduce-add (the L2 performs dst += tile; no register read-modify-write).
+// Epilogue staging: per epilogue warp, two 32-row x 128-byte buffers that feed TMA bulk
+// tensor stores (FWD: the exp slab) or reduce-adds (DX/DW: the L2 performs dst += tile;
+// no register read-modify-write).
 constexpr int EPI_BUF_BYTES = 32 * 128;
 constexpr int EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;   // 32 KB
 template <int MODE>
 constexpr int smem_bytes() {
-  return stages_of<MODE>() * STAGE_BYTES + (MODE != 0 ? EPI_BYTES : 0) + 1024 + 512;
+  return stages_of<MODE>() * STAGE_BYTES + EPI_BYTES + 1024 + 512;
 }
 
 enum Mode { FWD = 0, DX = 1, DW = 2 };
@@ -202,6 +203,13 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
           (uint64_t)map),
       "r"(src), "r"(x), "r"(y)
       : "memory");
+}
+// Box at (x, y) of the map's tensor = smem tile (clipped at the tensor's extent).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   (uint64_t)map),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_le1() {
@@ -358,8 +366,9 @@ struct Items {
 
 // ------------------------------------------------------------------ epilogues
 template <typename T>
-__device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int rows, int mrow, int n,
-                                             uint32_t taddr, int q, int lane) {
+__device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMap* tmS, uint8_t* stg,
+                                             int row0, int rows, int mrow, int n, uint32_t taddr, int q,
+                                             int lane, uint32_t& epi_it) {
   const int rr = mrow + q * 32 + lane;  // row within the chunk
   const bool valid = rr < rows;
   const int V = (int)a.V;
@@ -391,37 +400,52 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
       }
     }
   }
+  // exp(s - max) to the slab: 64 columns at a time, staged per warp in a 32-row x 128-byte
+  // buffer (128-byte swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8)) and written
+  // by one TMA bulk tensor store (whole lines; rows past the chunk hold values nothing
+  // reads, rows past R are clipped by the TMA unit)
   float sum = 0.0f;
-  T* srow = (T*)a.w.slab + (int64_t)(valid ? rr : 0) * a.Vp + v0;
   const float mxl = mx * LOG2E;
+  uint8_t* row = nullptr;
 #pragma unroll 1
-  for (int cc = 0; cc < BN / 32; ++cc) {
-    uint32_t r[32];
-    tmem_ld32(taddr + cc * 32, r);
-    uint32_t pk[16];
+  for (int c2 = 0; c2 < BN / 64; ++c2) {
+    uint8_t* buf = stg + (epi_it & 1u) * EPI_BUF_BYTES;
+    row = buf + lane * 128;
+    if (lane == 0) bulk_wait_read_le1();  // the store that last read this buffer is done
+    __syncwarp();
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c2 * 64 + hh * 32, r);
+      uint32_t pk[16];
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const int v = v0 + cc * 32 + j;
-      float s0 = __uint_as_float(r[j]), s1 = __uint_as_float(r[j + 1]);
-      float e0 = 0.0f, e1 = 0.0f;
-      if (v < V) {
-        if (bias != nullptr) s0 += to_f<T>(bias[v]);
-        e0 = exp2f(fmaf(s0, LOG2E, -mxl));
+      for (int j = 0; j < 32; j += 2) {
+        const int v = v0 + c2 * 64 + hh * 32 + j;
+        float s0 = __uint_as_float(r[j]), s1 = __uint_as_float(r[j + 1]);
+        float e0 = 0.0f, e1 = 0.0f;
+        if (v < V) {
+          if (bias != nullptr) s0 += to_f<T>(bias[v]);
+          e0 = exp2f(fmaf(s0, LOG2E, -mxl));
+        }
+        if (v + 1 < V) {
+          if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
+          e1 = exp2f(fmaf(s1, LOG2E, -mxl));
+        }
+        sum += e0 + e1;
+        pk[j / 2] = pack2<T>(e0, e1);
       }
-      if (v + 1 < V) {
-        if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
-        e1 = exp2f(fmaf(s1, LOG2E, -mxl));
-      }
-      sum += e0 + e1;
-      pk[j / 2] = pack2<T>(e0, e1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *(uint4*)(row + (((hh * 4 + j) ^ (lane & 7)) << 4)) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
     }
-    if (valid) {
-      uint4* dst = (uint4*)(srow + cc * 32);
-      dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-      dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmS, smem_u32(buf), v0 + c2 * 64, mrow + q * 32);
+      bulk_commit();
     }
+    ++epi_it;
   }
   if (valid) {
     const int64_t o = (int64_t)rr * a.nvt + n;
@@ -490,8 +514,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;  // DX and DW only
-  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES + (MODE != FWD ? EPI_BYTES : 0));
+  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES + EPI_BYTES);
   uint32_t* tmem_slot = (uint32_t*)(bars + NUM_BARS);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   int* copies = (int*)(tmem_slot + 2);  // per stage: phases this CTA's producer filled / armed
@@ -644,7 +668,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tile_coords<MODE>(ts, tile, m, n);
       const int mrow = m * 2 * BM + (int)rank * BM;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * BN);
-      if (MODE == FWD) epilogue_fwd<T>(a, row0, rows, mrow, n, taddr, q, lane);
+      if (MODE == FWD) epilogue_fwd<T>(a, &tmC, stg, row0, rows, mrow, n, taddr, q, lane, epi_it);
       else epilogue_reduce(a, &tmC, stg, mrow, n, MODE == DX ? (int)a.R : (int)a.V, taddr, q, lane, cb, epi_it);
       tc_fence_before();
       __syncwarp();
@@ -653,8 +677,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         else mbar_arrive_cluster(mapa(tempty_bar(as), 0));
       }
     }
-    // every reduce this warp issued has finished reading its staging buffer and written
-    if (MODE != FWD && lane == 0) bulk_wait_all();
+    // every store / reduce this warp issued has finished reading its staging buffer and
+    // written its destination
+    if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
 
@@ -789,8 +814,10 @@ cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 128)) return cudaErrorInvalidValue;
+  CUtensorMap C;  // the exp slab, written by the epilogue
+  if (!tc::make_map(&C, a.w.slab, a.dt, a.Vp, a.R, a.Vp * esz, 64, 32)) return cudaErrorInvalidValue;
   const int64_t tiles = ((a.R + 255) / 256) * a.nvt;
-  return tc::launch_mode<tc::FWD>(a, chunk, s, A, B, A, tiles);
+  return tc::launch_mode<tc::FWD>(a, chunk, s, A, B, C, tiles);
 }
 
 cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
