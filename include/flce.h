@@ -122,7 +122,9 @@ typedef struct flce_args {
   const float* grad_out;    /* NULL means 1.0; [1] for mean/sum, [BT] for none           */
   int32_t want_dX;          /* 1: write dX                                               */
   int32_t want_dW;          /* 1: accumulate dW (and dbias when bias != NULL)            */
-  int32_t dW_dtype;         /* flce_dtype of dW/dbias; FLCE_F32 is supported             */
+  int32_t dW_dtype;         /* flce_dtype of dW/dbias: FLCE_F32, or in_dtype itself
+                               (same-dtype accumulation: each call rounds dW + G^T X to
+                               in_dtype once); others give FLCE_ERR_UNSUPPORTED          */
   uint32_t flags;           /* FLCE_FLAG_*                                               */
   /* outputs (NULL = not wanted, except loss) */
   float* loss;              /* [1] for mean/sum (reduced), [BT] for none (per token)     */

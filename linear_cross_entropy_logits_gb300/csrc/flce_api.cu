@@ -122,13 +122,15 @@ static int32_t validate(const flce_args* x) {
   if (!(x->z_loss_scale >= 0.0f) || x->z_loss_scale > 1e30f) return FLCE_ERR_INVALID_ARG;
   if (x->want_dX && !x->dX) return FLCE_ERR_INVALID_ARG;
   if (x->want_dW && !x->dW) return FLCE_ERR_INVALID_ARG;
-  if (x->want_dW && x->dW_dtype != FLCE_F32) return FLCE_ERR_UNSUPPORTED;
+  // dW / dbias accumulate in fp32, or in the input dtype itself (same-dtype accumulation)
+  if (x->want_dW && x->dW_dtype != FLCE_F32 && x->dW_dtype != x->in_dtype) return FLCE_ERR_UNSUPPORTED;
   const int esz = dtype_size(x->in_dtype);
   if (!aligned(x->X, 16) || !aligned(x->W, 16) || !aligned(x->workspace, 256)) return FLCE_ERR_INVALID_ARG;
   if (x->want_dX && !aligned(x->dX, 16)) return FLCE_ERR_INVALID_ARG;
   if (x->want_dW && !aligned(x->dW, 16)) return FLCE_ERR_INVALID_ARG;
   if (x->bias && !aligned(x->bias, esz)) return FLCE_ERR_INVALID_ARG;
-  if (x->dbias && !aligned(x->dbias, 4)) return FLCE_ERR_INVALID_ARG;
+  if (x->dbias && !aligned(x->dbias, dtype_size(x->dW_dtype == FLCE_F32 ? FLCE_F32 : x->in_dtype)))
+    return FLCE_ERR_INVALID_ARG;
   if (!aligned(x->targets, 8) || (x->pred && !aligned(x->pred, 8))) return FLCE_ERR_INVALID_ARG;
   if (!aligned(x->loss, 4) || (x->status && !aligned(x->status, 4))) return FLCE_ERR_INVALID_ARG;
   return FLCE_OK;
@@ -262,8 +264,9 @@ extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
   a.want_dX = x->want_dX ? 1 : 0;
   a.want_dW = x->want_dW ? 1 : 0;
   a.dX = a.want_dX ? x->dX : nullptr;
-  a.dW = a.want_dW ? (float*)x->dW : nullptr;
-  a.dbias = (a.want_dW && x->bias) ? (float*)x->dbias : nullptr;
+  a.dW = a.want_dW ? x->dW : nullptr;
+  a.dbias = (a.want_dW && x->bias) ? x->dbias : nullptr;
+  a.dW_dt = x->dW_dtype;
   a.w = make_work(p, x->workspace, x->status);
   const uint32_t tmo_ms = x->wait_timeout_ms ? x->wait_timeout_ms : DEFAULT_TIMEOUT_MS;
   a.timeout_ns = (uint64_t)tmo_ms * 1000000ull;

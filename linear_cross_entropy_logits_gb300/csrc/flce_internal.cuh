@@ -91,8 +91,9 @@ struct CallArgs {
   int64_t* pred;
   int32_t* n_labelled;
   void* dX;
-  float* dW;
-  float* dbias;
+  void* dW;        // [V, H] in dW_dt (fp32, or the input dtype for same-dtype accumulation)
+  void* dbias;     // [V] in dW_dt
+  int dW_dt;
   int want_dX, want_dW;
   Work w;
   uint64_t timeout_ns;

@@ -310,7 +310,14 @@ __global__ void __launch_bounds__(256) k_gpass(const __grid_constant__ CallArgs 
 #pragma unroll
       for (int y = 0; y < 8; ++y) s += red[y][c];
       const int64_t v = (int64_t)t * VT + c;
-      if (v < a.V) a.dbias[v] += cb * s;
+      if (v < a.V) {
+        if (a.dW_dt == FLCE_F32) {
+          ((float*)a.dbias)[v] += cb * s;
+        } else {
+          T* db = (T*)a.dbias;  // same-dtype accumulation
+          db[v] = from_f<T>(to_f<T>(db[v]) + cb * s);
+        }
+      }
     }
   }
 }
@@ -538,8 +545,11 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const __grid_constant__ CallA
       if (MODE == 0) {
         const int64_t orow = a.w.idx[row0 + m];
         ((T*)a.dX)[orow * a.H + n] = from_f<T>(cb * acc[i][j]);
+      } else if (a.dW_dt == FLCE_F32) {
+        ((float*)a.dW)[m * a.H + n] += cb * acc[i][j];
       } else {
-        a.dW[m * a.H + n] += cb * acc[i][j];
+        T* w = (T*)a.dW + m * a.H + n;  // same-dtype accumulation
+        *w = from_f<T>(to_f<T>(*w) + cb * acc[i][j]);
       }
     }
   }

@@ -495,6 +495,40 @@ __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtenso
   }
 }
 
+// Same-dtype dW (bf16/fp16 destination): dW[v, h] = round(dW[v, h] + cbar * acc) by the
+// thread that owns row v of the tile (one read-modify-write per element per launch, by the
+// owning pair: deterministic). 8 columns per 16-byte access.
+template <typename T>
+__device__ __forceinline__ void epilogue_dw_same_dtype(const CallArgs& a, int mrow, int x0, uint32_t taddr,
+                                                       int q, int lane, float cb) {
+  const int H = (int)a.H;
+  const int v = mrow + q * 32 + lane;
+  const bool valid = v < (int)a.V;
+  T* wrow = (T*)a.dW + (int64_t)(valid ? v : 0) * a.H;
+#pragma unroll 1
+  for (int cc = 0; cc < BN / 32; ++cc) {
+    const int h0 = x0 + cc * 32;
+    if (h0 >= H) break;  // warp-uniform
+    uint32_t r[32];
+    tmem_ld32(taddr + cc * 32, r);
+    if (!valid) continue;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (h0 + g * 8 < H) {
+        uint4* p = (uint4*)(wrow + h0 + g * 8);
+        uint4 u = *p;
+        T* t = (T*)&u;
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = pack2<T>(to_f<T>(t[2 * j]) + cb * __uint_as_float(r[g * 8 + 2 * j]),
+                          to_f<T>(t[2 * j + 1]) + cb * __uint_as_float(r[g * 8 + 2 * j + 1]));
+        *p = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 template <int MODE, typename T>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -669,6 +703,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int mrow = m * 2 * BM + (int)rank * BM;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * BN);
       if (MODE == FWD) epilogue_fwd<T>(a, &tmC, stg, row0, rows, mrow, n, taddr, q, lane, epi_it);
+      else if (MODE == DW && a.dW_dt != FLCE_F32) epilogue_dw_same_dtype<T>(a, mrow, n * BN, taddr, q, lane, cb);
       else epilogue_reduce(a, &tmC, stg, mrow, n, MODE == DX ? (int)a.R : (int)a.V, taddr, q, lane, cb, epi_it);
       tc_fence_before();
       __syncwarp();
@@ -836,8 +871,12 @@ cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 64)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 64)) return cudaErrorInvalidValue;
-  CUtensorMap C;
-  if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, 32, 32)) return cudaErrorInvalidValue;
+  CUtensorMap C;  // fp32 dW for TMA reduce-add; unused (a copy of A) for same-dtype dW
+  if (a.dW_dt == FLCE_F32) {
+    if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, 32, 32)) return cudaErrorInvalidValue;
+  } else {
+    C = A;
+  }
   const int64_t tiles = ((a.V + 255) / 256) * ((a.H + 255) / 256);
   return tc::launch_mode<tc::DW>(a, chunk, s, A, B, C, tiles);
 }

@@ -154,7 +154,8 @@ def fwd_bwd(X, W, targets, bias=None, *, ignore_index=-100, reduction="mean",
     """Fused linear cross entropy forward + backward on X's device.
 
     X [BT,H] and W [V,H] share a dtype (fp32, bf16 or fp16); targets int64 [BT]. dW/dbias
-    (fp32) are accumulated into when given, else allocated as zeros. Returns a dict of
+    are accumulated into when given (fp32, or X's dtype for same-dtype accumulation), else
+    allocated as fp32 zeros. Returns a dict of
     tensors: loss, z_loss, acc (reduced per ``reduction``), lse, pred, n_labelled, dX, dW,
     dbias, and the status code when ``check`` is set (which synchronises the stream).
     ``outputs`` may carry preallocated output tensors under the same keys.
@@ -184,10 +185,11 @@ def fwd_bwd(X, W, targets, bias=None, *, ignore_index=-100, reduction="mean",
         o["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
     if want_dX and o.get("dX") is None:
         o["dX"] = torch.empty_like(X)
+    dW_dt = torch.float32 if dW is None else dW.dtype
     if want_dW and dW is None:
-        dW = torch.zeros(V, H, dtype=torch.float32, device=dev)
+        dW = torch.zeros(V, H, dtype=dW_dt, device=dev)
     if want_dW and bias is not None and dbias is None:
-        dbias = torch.zeros(V, dtype=torch.float32, device=dev)
+        dbias = torch.zeros(V, dtype=dW_dt, device=dev)
     if workspace is None:
         nbytes = workspace_bytes or workspace_size(BT, H, V, X.dtype, budget_bytes)
         if nbytes == 0:
@@ -206,7 +208,8 @@ def fwd_bwd(X, W, targets, bias=None, *, ignore_index=-100, reduction="mean",
     a.ignore_index = ignore_index
     a.z_loss_scale = z_loss_scale
     a.grad_out = _ptr(grad_out)
-    a.want_dX, a.want_dW, a.dW_dtype = int(bool(want_dX)), int(bool(want_dW)), 0
+    a.want_dX, a.want_dW = int(bool(want_dX)), int(bool(want_dW))
+    a.dW_dtype = DTYPES[dW_dt]
     a.flags = flags
     a.loss, a.z_loss, a.acc = _ptr(o["loss"]), _ptr(o["z_loss"]), _ptr(o["acc"])
     a.lse, a.pred, a.n_labelled = _ptr(o["lse"]), _ptr(o["pred"]), _ptr(o["n_labelled"])

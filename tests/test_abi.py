@@ -116,7 +116,8 @@ def _args(**kw):
     (dict(z_loss_scale=float("nan")), flce.FLCE_ERR_INVALID_ARG),
     (dict(want_dX=1, dX=None), flce.FLCE_ERR_INVALID_ARG),
     (dict(want_dW=1, dW=None), flce.FLCE_ERR_INVALID_ARG),
-    (dict(want_dW=1, dW=0x5000, dW_dtype=1), flce.FLCE_ERR_UNSUPPORTED),
+    (dict(want_dW=1, dW=0x5000, dW_dtype=2), flce.FLCE_ERR_UNSUPPORTED),
+    (dict(in_dtype=0, want_dW=1, dW=0x5000, dW_dtype=1), flce.FLCE_ERR_UNSUPPORTED),
     (dict(X=0x1008), flce.FLCE_ERR_INVALID_ARG),
     (dict(workspace=0x100010), flce.FLCE_ERR_INVALID_ARG),
     (dict(workspace_bytes=1024), flce.FLCE_ERR_WORKSPACE),
@@ -128,3 +129,10 @@ def test_host_validation_rejects_before_any_cuda_call(lib, kw, code):
 
 def test_null_args_pointer(lib):
     assert lib.flce_fwd_bwd(None, None) == flce.FLCE_ERR_INVALID_ARG
+
+
+def test_torch_custom_op_registers():
+    """The torch integration imports without a GPU and registers its custom op."""
+    from linear_cross_entropy_logits_gb300 import torch_ops
+    assert hasattr(torch.ops.flce_gb300, "fused_linear_cross_entropy")
+    assert callable(torch_ops.fused_linear_cross_entropy)

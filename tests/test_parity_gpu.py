@@ -172,6 +172,33 @@ def test_dW_accumulates_into_destination():
     assert rel_fro(g["dW"] - init.numpy(), o["dW"]) <= TOL["bf16"]["grad"]
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("path", ["tc", "simt"])
+def test_same_dtype_dW_accumulation(dt, path):
+    """dW and dbias accumulated in the input dtype ("Reduce FLCE weight-gradient allocation
+    overhead across FP16, BF16, and FP32", support matrix: same-dtype FP16/BF16 direct
+    accumulation). Each call rounds dW_init + G^T X to the input dtype once."""
+    sp = I.spec("frozen_head", BT=300, H=136, V=2100, dtype=dt, w_std=0.15, bias_std=0.3,
+                n_ignored=60, reduction="sum", grad_out=None, want_dW=True, z=1e-3)
+    inp = I.generate(sp, seed=12)
+    tdt = I.TORCH_DTYPES[dt]
+    init = (torch.randn(sp["V"], sp["H"], generator=torch.Generator().manual_seed(13)) * 0.01).to(tdt)
+    binit = (torch.randn(sp["V"], generator=torch.Generator().manual_seed(14)) * 0.01).to(tdt)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    dW = init.clone().cuda()
+    db = binit.clone().cuda()
+    out = flce.fwd_bwd(d["X"], d["W"], d["targets"], d["bias"], reduction="sum", z_loss_scale=sp["z"],
+                       dW=dW, dbias=db, flags=flce.FLAG_FORCE_SIMT if path == "simt" else 0)
+    assert out["status_code"] == flce.FLCE_OK
+    o = run_oracle(inp, sp)
+    got_dW = out["dW"].float().cpu().numpy() - init.float().numpy()
+    got_db = out["dbias"].float().cpu().numpy() - binit.float().numpy()
+    assert out["dW"].dtype == tdt and out["dbias"].dtype == tdt
+    assert rel_fro(got_dW, o["dW"]) <= TOL[dt]["grad"]
+    assert rel_fro(got_db, o["dbias"]) <= TOL[dt]["grad"]
+    assert rel_fro(out["dX"].float().cpu().numpy(), o["dX"]) <= TOL[dt]["grad"]
+
+
 def test_grad_scalar_scales_gradients():
     sp = I.spec("llama1b", BT=128, H=64, V=640, w_std=0.2, ignore="random", n_ignored=8,
                 grad_scalar=0.37, z=0.02)

@@ -1,0 +1,79 @@
+"""The torch integration (custom op + autograd Function) on the GPU: gradients through
+loss.backward() match the float64 oracle for every reduction with a trained and a frozen
+head, and torch.compile(fullgraph=True) gives the eager results (the pages check that
+compiled results equal eager: "Liger-Kernel PR #1554", Details item 6)."""
+
+import numpy as np
+import pytest
+import torch
+
+from linear_cross_entropy_logits_gb300 import build as B
+from linear_cross_entropy_logits_gb300 import inputs as I
+from parity_util import TOL, rel_fro, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.build()
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+@pytest.mark.parametrize("frozen", [False, True])
+def test_autograd_matches_oracle(reduction, frozen):
+    from linear_cross_entropy_logits_gb300.torch_ops import fused_linear_cross_entropy
+    sp = I.spec("frozen_head", BT=320, H=128, V=3000, w_std=0.15, bias_std=0.2, n_ignored=70,
+                reduction=reduction, grad_out="uniform", want_dW=not frozen, z=1e-3)
+    inp = I.generate(sp, seed=40)
+    X = inp["X"].cuda().requires_grad_(True)
+    W = inp["W"].cuda().requires_grad_(not frozen)
+    b = inp["bias"].cuda().requires_grad_(not frozen)
+    t = inp["targets"].cuda()
+    loss = fused_linear_cross_entropy(X, W, t, b, reduction=reduction, z_loss_scale=sp["z"],
+                                      accum_dtype=torch.float32)
+    g = inp["grad_out"].cuda()
+    if reduction == "none":
+        (loss * g).sum().backward()
+        go = inp["grad_out"]
+    else:
+        (loss * 0.7).backward()
+        go = None
+    sp2 = dict(sp, grad_scalar=0.7) if reduction != "none" else sp
+    o = run_oracle(dict(inp, grad_out=go) if reduction == "none" else dict(inp, grad_out=None), sp2)
+    tol = TOL["bf16"]
+    if reduction == "none":
+        ref = o["loss"]
+        assert np.max(np.abs(loss.detach().cpu().numpy() - ref) / np.maximum(np.abs(ref), 1e-3)) <= tol["loss"]
+    else:
+        assert abs(float(loss.detach()) - o["loss"]) <= tol["loss"] * abs(o["loss"])
+    assert rel_fro(X.grad.float().cpu().numpy(), o["dX"]) <= tol["grad"]
+    if not frozen:
+        assert rel_fro(W.grad.float().cpu().numpy(), o["dW"]) <= tol["grad"]
+        assert rel_fro(b.grad.float().cpu().numpy(), o["dbias"]) <= tol["grad"]
+    else:
+        assert W.grad is None and b.grad is None
+
+
+def test_compile_matches_eager():
+    from linear_cross_entropy_logits_gb300.torch_ops import fused_linear_cross_entropy
+    sp = I.spec("llama8b", BT=512, H=256, V=4000, w_std=0.15, z=1e-4)
+    inp = I.generate(sp, seed=41)
+    A = (torch.randn(256, 256, generator=torch.Generator().manual_seed(42)) * 0.05).to(torch.bfloat16)
+
+    def step(x, a, w, t):
+        h = x @ a
+        return fused_linear_cross_entropy(h, w, t, z_loss_scale=1e-4)
+
+    res = []
+    for fn in (step, torch.compile(step, fullgraph=True)):
+        x = inp["X"].cuda()
+        a = A.cuda().requires_grad_(True)
+        w = inp["W"].cuda().requires_grad_(True)
+        loss = fn(x, a, w, inp["targets"].cuda())
+        loss.backward()
+        res.append((loss.detach().float().cpu(), a.grad.float().cpu(), w.grad.float().cpu()))
+    for e, c in zip(res[0], res[1]):
+        assert torch.equal(e, c)
