@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--ref-seconds", type=float, default=100.0,
+                   help="total oracle time budget of the --impl reference arm")
     p.add_argument("--bt", type=int, default=None,
                    help="override BT (smaller cases for profiler captures)")
     return p.parse_args()
@@ -204,6 +206,16 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(value, dist=None, device="cpu"):
+    """Max of a per-rank scalar over all ranks (the bench reports the slowest replica)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------- arms
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
@@ -212,7 +224,7 @@ def run_reference(args):
     sp = workload_spec(args)
     inp = I.generate(sp, seed=0)
     n_lab = int((inp["targets"] != I.IGNORE_INDEX).sum())
-    per_step_seconds = max(2.0, 100.0 / max(args.steps + args.warmup, 1))
+    per_step_seconds = max(min(2.0, args.ref_seconds), args.ref_seconds / max(args.steps + args.warmup, 1))
     for _ in range(args.warmup):
         oracle_sample_rate(sp, inp, per_step_seconds / 4, rng_seed=1)
     rates, rows_total, secs_total = [], 0, 0.0
@@ -312,10 +324,7 @@ def run_ours(args):
     clocks = clk.stop()
     ms_total = e0.elapsed_time(e1)
     stages = prof.read()
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / args.steps
     value = BT * world / (ms_step / 1000.0)
 
@@ -350,10 +359,7 @@ def run_ours(args):
         f1.record(stream)
         torch.cuda.synchronize(dev)
         ms_e2e = f0.elapsed_time(f1) / args.steps
-        if dist:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
+        ms_e2e = max_over_ranks(ms_e2e, dist, dev)
         h2d = Xh.numel() * Xh.element_size() + th.numel() * th.element_size() + \
             (gh.numel() * gh.element_size() if gh is not None else 0)
         e2e = {"value": BT * world / (ms_e2e / 1000.0), "unit": UNIT, "ms_per_step": ms_e2e,
