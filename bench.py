@@ -9,6 +9,8 @@ V=128256, bf16, 16 sequences of 512 rows with the last row of each ignored, mean
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--labelled-fraction F]
   python bench.py --impl reference ...   # the float64 CPU oracle on a bounded row sample
+  python bench.py --op jsd ...           # the fused linear JSD distillation op (student
+                                         # Llama-3.2-1B head vs Llama-3.1-8B teacher head)
 
 Prints one JSON line (rank 0). Under torchrun each rank runs an independent replica on its
 own GPU (the op has no exchange step); value = all ranks' tokens / max-over-ranks time.
@@ -51,6 +53,7 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--op", default="flce", choices=["flce", "jsd"])
     p.add_argument("--workload", default="llama8b", choices=list(I.WORKLOADS))
     p.add_argument("--labelled-fraction", type=float, default=None)
     p.add_argument("--no-e2e", action="store_true")
@@ -422,9 +425,129 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_jsd(args):
+    """The fused linear JSD distillation op on its synthetic workload (rank-local replicas
+    under torchrun, like the cross-entropy op). FLOPs counted: the student and teacher
+    logits GEMMs plus the student dX and dW GEMMs, 2 N V (3 Hs + Ht)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    sp = dict(I.DISTILL)
+    if args.bt is not None:
+        sp["BT"] = args.bt
+    BT, Hs, Ht, V = sp["BT"], sp["Hs"], sp["Ht"], sp["V"]
+    inp = I.generate_distill(sp, seed=rank)
+    n_lab = int((inp["labels"] != I.IGNORE_INDEX).sum())
+    flops = 2.0 * n_lab * V * (3 * Hs + Ht)
+    cfg = {"workload": "distillation: Llama-3.2-1B-shaped student head vs Llama-3.1-8B-shaped "
+                       "teacher head (distill)", "BT": BT, "Hs": Hs, "Ht": Ht, "V": V,
+           "input_dtype": sp["dtype"], "beta": sp["beta"], "temperature": sp["temperature"],
+           "reduction": sp["reduction"], "n_labelled": n_lab}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from oracle import jsd_oracle as jo
+        rng = np.random.default_rng(7)
+        f = I.to_numpy_exact
+        Ws, Wt = f(inp["Ws"]), f(inp["Wt"])
+        done, spent = 0, 0.0
+        budget = args.ref_seconds / max(args.steps + args.warmup, 1) * max(args.steps, 1)
+        while spent < budget:
+            rows = np.sort(rng.choice(BT, size=16, replace=False))
+            idx = torch.from_numpy(rows)
+            t0 = time.perf_counter()
+            jo.jsd_oracle(f(inp["Xs"][idx]), Ws, f(inp["Xt"][idx]), Wt, inp["labels"].numpy()[rows],
+                          beta=sp["beta"], temperature=sp["temperature"])
+            spent += time.perf_counter() - t0
+            done += rows.size
+        value = done / spent
+        print(json.dumps({"impl": "reference", "metric": "fused linear JSD fwd+bwd tokens/s", "value": value,
+                          "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": BT / value * 1000.0, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+                          "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(),
+                                           "kind": "oracle", "sample": f"{done} seeded rows, {spent:.1f} s"},
+                          "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    from linear_cross_entropy_logits_gb300 import build as B
+    B.build()
+    from linear_cross_entropy_logits_gb300 import flce
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    d = {k: v.to(dev) for k, v in inp.items()}
+    dt = I.TORCH_DTYPES[sp["dtype"]]
+    ws_bytes = flce.jsd_workspace_size(BT, Hs, Ht, V, dt, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    dW = torch.zeros(V, Hs, dtype=torch.float32, device=dev)
+    outs = {"loss": torch.empty(1, device=dev), "n_labelled": torch.empty(1, dtype=torch.int32, device=dev),
+            "status": torch.zeros(1, dtype=torch.int32, device=dev), "dX": torch.empty_like(d["Xs"])}
+    prof = flce.Profiler()
+
+    def step(profiler=None):
+        flce.fused_linear_jsd(d["Xs"], d["Ws"], d["Xt"], d["Wt"], d["labels"], beta=sp["beta"],
+                              temperature=sp["temperature"], dW=dW, workspace=ws, outputs=outs,
+                              check=False, profiler=profiler)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = flce.load().flce_get_status(outs["status"].data_ptr(), None, stream.cuda_stream)
+    if st != flce.FLCE_OK:
+        raise RuntimeError(f"warm-up status {flce.status_string(st)}")
+    clk = ClockSampler(dev)
+    clk.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    prof.reset()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(prof)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clocks = clk.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
+    stages = prof.read()
+    peaks, src = load_peaks()
+    tflops = flops / (ms / 1000.0) / 1e12
+    dom = max(("fwd", "dx", "dw"), key=lambda k: stages[k][0])
+    dom_flops = 2.0 * n_lab * V * ((Hs + Ht) if dom == "fwd" else Hs)
+    achieved = dom_flops / (stages[dom][0] / args.steps / 1000.0) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    line = {"op": "fused_linear_jsd", "metric": "fused linear JSD fwd+bwd tokens/s",
+            "value": BT * world / (ms / 1000.0), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": sp["dtype"], "data": "synthetic (seeded torch.Generator)",
+            "config": dict(cfg, workspace_bytes=ws_bytes, chunk_rows=None,
+                           l2="no flush: the heads (0.5 + 1.05 GB) exceed the 129 MB L2"),
+            "tflops": tflops, "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
+                                                     "sustained": tflops / peak, "source": src},
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_kind": f"bf16 sustained ({src})", "traffic": None},
+            "stages": {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+                       for k, v in stages.items() if v[1] > 0},
+            "gpu_launches": int(sum(v[1] for v in stages.values())), "clocks": clocks, "e2e": None}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.op == "jsd":
+        run_jsd(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -164,6 +164,63 @@ FLCE_API int64_t flce_chunk_rows(int64_t BT, int64_t H, int64_t V, int32_t in_dt
  * enqueued (FLCE_ERR_CUDA may follow a partial enqueue if a launch fails). */
 FLCE_API int32_t flce_fwd_bwd(const flce_args* args, void* stream);
 
+/* ----------------------------------------------------------------------------------
+ * Fused linear JSD / KL distillation (same tile engine).
+ *
+ * The pages name this sibling op without defining it (a "fused linear KL" loss with its
+ * own chunk policy on the Liger-Kernel v0.8.3 commit page; test_fused_linear_jsd.py in
+ * "Liger-Kernel PR #1554: skip ignore_index rows", Results). The definition used: teacher
+ * P = softmax(X_t W_t^T / T), student Q = softmax(X_s W_s^T / T) per row over V, and
+ *     0 < beta < 1: loss_i = beta KL(P||M) + (1-beta) KL(Q||M),  M = beta P + (1-beta) Q
+ *     beta = 0:     loss_i = KL(P||Q)        beta = 1:  loss_i = KL(Q||P)
+ * reduced over the rows whose label is not ignore_index (all rows when labels is NULL;
+ * a label's value is otherwise unused) by mean (over those rows), sum or none. Only the
+ * student gets gradients: dX_s = dS W_s, dW_s += dS^T X_s with
+ * dS = c_i / T * dloss_i/dz_s. Neither [BT,V] logits nor probabilities reach HBM; the
+ * workspace holds two [R, V] slabs (student, teacher) per chunk of R rows.
+ * Memory, ownership, errors and threading as for flce_fwd_bwd.
+ * ---------------------------------------------------------------------------------- */
+typedef struct flce_jsd_args {
+  int64_t BT;               /* rows                                                      */
+  int64_t Hs;               /* student hidden size                                       */
+  int64_t Ht;               /* teacher hidden size                                       */
+  int64_t V;                /* vocabulary size (shared)                                  */
+  int32_t in_dtype;         /* flce_dtype of Xs, Ws, Xt, Wt and dX                        */
+  int32_t reduction;        /* flce_reduction                                            */
+  const void* Xs;           /* [BT,Hs] student rows                                      */
+  const void* Ws;           /* [V,Hs]  student head                                      */
+  const void* Xt;           /* [BT,Ht] teacher rows                                      */
+  const void* Wt;           /* [V,Ht]  teacher head                                      */
+  const int64_t* labels;    /* [BT] or NULL; rows equal to ignore_index take no part     */
+  int64_t ignore_index;
+  float beta;               /* in [0, 1]                                                 */
+  float temperature;        /* > 0                                                       */
+  const float* grad_out;    /* NULL means 1.0; [1] for mean/sum, [BT] for none           */
+  int32_t want_dX;          /* 1: write dX_s                                             */
+  int32_t want_dW;          /* 1: accumulate dW_s                                        */
+  int32_t dW_dtype;         /* FLCE_F32 or in_dtype                                      */
+  uint32_t flags;           /* FLCE_FLAG_FORCE_SIMT                                      */
+  float* loss;              /* [1] for mean/sum, [BT] for none                           */
+  int32_t* n_labelled;      /* [1] or NULL                                               */
+  void* dX;                 /* [BT,Hs] in_dtype, overwritten (zero on ignored rows)      */
+  void* dW;                 /* [V,Hs] dW_dtype, ACCUMULATED                              */
+  void* workspace;          /* device scratch, 256-byte aligned                          */
+  size_t workspace_bytes;   /* >= flce_jsd_workspace_size(...) for a chosen budget       */
+  int32_t* status;          /* device int or NULL, as in flce_args                       */
+  uint32_t wait_timeout_ms; /* 0 means 4000 ms                                           */
+  flce_profile* profile;    /* NULL, or a profiler (stages as for flce_fwd_bwd; the
+                               divergence and gradient passes count as FLCE_STAGE_GPASS) */
+} flce_jsd_args;
+
+/* Workspace bytes for the distillation op within budget_bytes (0 means 1.5 GiB); 0 when
+ * not even one 128-row chunk fits or on invalid arguments. */
+FLCE_API size_t flce_jsd_workspace_size(int64_t BT, int64_t Hs, int64_t Ht, int64_t V,
+                                        int32_t in_dtype, size_t budget_bytes);
+
+/* Enqueue the fused linear JSD forward+backward on `stream`; host-side errors return at
+ * once with nothing enqueued, device-side ones go to the status word. */
+FLCE_API int32_t flce_fused_linear_jsd(const flce_jsd_args* args, void* stream);
+
 /* Size of the fixed device scratch used by flce_fwd_bwd_noalloc (128 MiB). */
 #define FLCE_NOALLOC_SCRATCH_BYTES ((size_t)128 << 20)
 

@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libflce.so")
-SOURCES = ["flce_api.cu", "flce_kernels.cu", "flce_tc.cu", "flce_noalloc.cu"]
+SOURCES = ["flce_api.cu", "flce_kernels.cu", "flce_tc.cu", "flce_noalloc.cu", "flce_jsd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
           "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

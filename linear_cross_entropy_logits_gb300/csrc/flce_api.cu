@@ -144,39 +144,6 @@ static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 
 extern "C" const char* flce_last_cuda_error(void) { return cudaGetErrorName(g_last_cuda_error); }
 
-struct flce_profile {
-  std::vector<cudaEvent_t> ev;  // pairs: ev[2i] before, ev[2i+1] after launch i
-  std::vector<int> stage;       // stage of pair i
-  std::vector<int> nkern;       // kernels launched by pair i
-  size_t used = 0;              // pairs recorded since the last reset
-};
-
-namespace {
-// Record `launch` on `s`, bracketed by an event pair when profiling.
-template <typename F>
-cudaError_t staged(flce_profile* prof, int stage, int nkern, cudaStream_t s, F&& launch) {
-  if (!prof) return launch();
-  if (prof->used * 2 + 2 > prof->ev.size()) {
-    for (int i = 0; i < 2; ++i) {
-      cudaEvent_t e;
-      cudaError_t r = cudaEventCreate(&e);
-      if (r != cudaSuccess) return r;
-      prof->ev.push_back(e);
-    }
-    prof->stage.push_back(0);
-    prof->nkern.push_back(0);
-  }
-  const size_t i = prof->used++;
-  prof->stage[i] = stage;
-  prof->nkern[i] = nkern;
-  cudaError_t r = cudaEventRecord(prof->ev[2 * i], s);
-  if (r != cudaSuccess) return r;
-  r = launch();
-  if (r != cudaSuccess) return r;
-  return cudaEventRecord(prof->ev[2 * i + 1], s);
-}
-}  // namespace
-
 extern "C" flce_profile* flce_profile_create(void) { return new (std::nothrow) flce_profile(); }
 
 extern "C" void flce_profile_reset(flce_profile* prof) {
@@ -271,6 +238,8 @@ extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
   const uint32_t tmo_ms = x->wait_timeout_ms ? x->wait_timeout_ms : DEFAULT_TIMEOUT_MS;
   a.timeout_ns = (uint64_t)tmo_ms * 1000000ull;
   a.flags = x->flags;
+  a.logit_scale = 1.0f;
+  a.labels_are_masks = 0;
 
   cudaStream_t s = (cudaStream_t)stream;
   const bool tc = !(x->flags & FLCE_FLAG_FORCE_SIMT) && tc_supported(a);

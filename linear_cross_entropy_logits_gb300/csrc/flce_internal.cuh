@@ -9,6 +9,8 @@
 
 #include "../../include/flce.h"
 
+#include <vector>
+
 namespace flce {
 
 // Vocabulary tile of the forward statistics: every forward GEMM (tensor-core or SIMT)
@@ -98,6 +100,8 @@ struct CallArgs {
   Work w;
   uint64_t timeout_ns;
   uint32_t flags;
+  float logit_scale;     // logits = (X W^T) * logit_scale + bias (1/T for distillation)
+  int labels_are_masks;  // 1: any target != ignore_index marks a row (no range check)
 };
 
 // ---- launchers (flce_kernels.cu) ----
@@ -142,3 +146,38 @@ __device__ __forceinline__ bool chunk_bounds(const Ctrl* c, int k, int& row0, in
 constexpr float LOG2E = 1.4426950408889634f;
 
 }  // namespace flce
+
+// Optional per-launch CUDA-event timing (flce_profile_*).
+struct flce_profile {
+  std::vector<cudaEvent_t> ev;  // pairs: ev[2i] before, ev[2i+1] after launch i
+  std::vector<int> stage;       // stage of pair i
+  std::vector<int> nkern;       // kernels launched by pair i
+  size_t used = 0;              // pairs recorded since the last reset
+};
+
+namespace flce {
+// Record `launch` on `s`, bracketed by an event pair when profiling.
+template <typename F>
+inline cudaError_t staged(flce_profile* prof, int stage, int nkern, cudaStream_t s, F&& launch) {
+  if (!prof) return launch();
+  if (prof->used * 2 + 2 > prof->ev.size()) {
+    for (int i = 0; i < 2; ++i) {
+      cudaEvent_t e;
+      cudaError_t r = cudaEventCreate(&e);
+      if (r != cudaSuccess) return r;
+      prof->ev.push_back(e);
+    }
+    prof->stage.push_back(0);
+    prof->nkern.push_back(0);
+  }
+  const size_t i = prof->used++;
+  prof->stage[i] = stage;
+  prof->nkern[i] = nkern;
+  cudaError_t r = cudaEventRecord(prof->ev[2 * i], s);
+  if (r != cudaSuccess) return r;
+  r = launch();
+  if (r != cudaSuccess) return r;
+  return cudaEventRecord(prof->ev[2 * i + 1], s);
+}
+}  // namespace flce
+

@@ -1,0 +1,546 @@
+// Fused linear JSD / KL distillation on the FLCE tile engine.
+//
+// The pages name this sibling op ("fused linear KL" on the Liger-Kernel v0.8.3 commit
+// page; test_fused_linear_jsd.py in "Liger-Kernel PR #1554: skip ignore_index rows",
+// Results) without defining it; the reading used (see include/flce.h) is the generalised
+// Jensen-Shannon divergence between the teacher P = softmax(X_t W_t^T / T) and the student
+// Q = softmax(X_s W_s^T / T), with beta = 0 giving KL(P||Q) and beta = 1 KL(Q||P).
+//
+// Per row chunk: gather student and teacher rows; the forward GEMM twice (student and
+// teacher, logits scaled by 1/T in the epilogue, each writing per-tile statistics and its
+// exp slab); k_jsd_finalize (both lse, per-tile log offsets); k_jsd_terms (per element
+// divergence terms and sum_v Q g, reduced per (row, tile) in a fixed order); k_jsd_rowsum
+// (per row, fixed order); k_jsd_grad (dloss/dz into the student slab in place); then the
+// same dX / dW GEMMs as the cross-entropy op. Nothing of [BT, V] reaches HBM.
+#include <math.h>
+#include <string.h>
+
+#include "flce_internal.cuh"
+
+namespace flce {
+namespace {
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+inline size_t rup_sz(size_t a, size_t b) { return (a + b - 1) / b * b; }
+__host__ __device__ inline int64_t rup64(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+struct JsdPlan {
+  int64_t BT, Hs, Ht, V, Hsp, Htp, nvt, Vp, R, kmax;
+  int esz;
+  size_t off_ctrl, off_idx, off_rloss, off_rz, off_racc;
+  size_t off_xcs, off_xct, off_stm_s, off_sts_s, off_sti_s, off_stm_t, off_sts_t, off_sti_t;
+  size_t off_tgt_s, off_tgt_t, off_lse_s, off_lse_t, off_arow, off_srow;
+  size_t off_slab_s, off_slab_t, off_dxacc;
+  size_t total;
+};
+
+bool jsd_layout(int64_t BT, int64_t Hs, int64_t Ht, int64_t V, int dt, int64_t R, JsdPlan* p) {
+  if (BT <= 0 || Hs <= 0 || Ht <= 0 || V <= 0 || R <= 0) return false;
+  JsdPlan q;
+  q.BT = BT;
+  q.Hs = Hs;
+  q.Ht = Ht;
+  q.V = V;
+  q.esz = dtype_size(dt);
+  q.Hsp = rup(Hs, 64);
+  q.Htp = rup(Ht, 64);
+  q.nvt = cdiv(V, VT);
+  q.Vp = q.nvt * VT;
+  q.R = R;
+  q.kmax = cdiv(BT, R);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = rup_sz(off + bytes, 256);
+    return o;
+  };
+  const size_t st = 4 * (size_t)q.nvt * R;
+  q.off_ctrl = take(sizeof(Ctrl));
+  q.off_idx = take(4 * (size_t)BT);
+  q.off_rloss = take(4 * (size_t)BT);
+  q.off_rz = take(4 * (size_t)BT);
+  q.off_racc = take(4 * (size_t)BT);
+  q.off_xcs = take((size_t)R * q.Hsp * q.esz);
+  q.off_xct = take((size_t)R * q.Htp * q.esz);
+  q.off_stm_s = take(st);
+  q.off_sts_s = take(st);
+  q.off_sti_s = take(st);
+  q.off_stm_t = take(st);
+  q.off_sts_t = take(st);
+  q.off_sti_t = take(st);
+  q.off_tgt_s = take(4 * (size_t)R);
+  q.off_tgt_t = take(4 * (size_t)R);
+  q.off_lse_s = take(4 * (size_t)R);
+  q.off_lse_t = take(4 * (size_t)R);
+  q.off_arow = take(4 * (size_t)R);
+  q.off_srow = take(4 * (size_t)R);
+  q.off_slab_s = take((size_t)R * q.Vp * q.esz);
+  q.off_slab_t = take((size_t)R * q.Vp * q.esz);
+  q.off_dxacc = take(q.esz == 2 ? (size_t)R * Hs * 4 : 0);
+  q.total = off;
+  *p = q;
+  return true;
+}
+
+int64_t jsd_rows_for_bytes(int64_t BT, int64_t Hs, int64_t Ht, int64_t V, int dt, size_t bytes) {
+  JsdPlan p, p2;
+  if (!jsd_layout(BT, Hs, Ht, V, dt, CHUNK_ALIGN, &p) || p.total > bytes) return 0;
+  jsd_layout(BT, Hs, Ht, V, dt, 2 * CHUNK_ALIGN, &p2);
+  const size_t per128 = p2.total - p.total;
+  int64_t R = CHUNK_ALIGN + (int64_t)((bytes - p.total) / (per128 ? per128 : 1)) * CHUNK_ALIGN;
+  const int64_t cap = rup(BT, CHUNK_ALIGN);
+  if (R > cap) R = cap;
+  while (R > CHUNK_ALIGN) {
+    if (jsd_layout(BT, Hs, Ht, V, dt, R, &p) && p.total <= bytes) break;
+    R -= CHUNK_ALIGN;
+  }
+  return R;
+}
+
+// Everything the JSD kernels need: the student and teacher views of the engine, and the
+// distillation parameters.
+struct JsdArgs {
+  CallArgs s, t;
+  float beta, inv_T;
+  float* srow;  // [R] sum_v Q_v g_v per row
+};
+
+__device__ __forceinline__ void lse_merge(float& M, float& S, float M2, float S2) {
+  const float Mn = fmaxf(M, M2);
+  S = Mn == -INFINITY ? 0.0f : S * expf(M - Mn) + S2 * expf(M2 - Mn);
+  M = Mn;
+}
+
+// Row lse of the student and the teacher from their per-tile (max, sum-exp) statistics, in
+// a fixed order; each tile max is then rewritten as the tile's log offset m - lse, so that
+// log Q = log e + offset and Q = e * exp(offset) for the stored e = exp(z - m).
+__global__ void __launch_bounds__(256) k_jsd_finalize(const __grid_constant__ JsdArgs j, int chunk) {
+  int row0, rows;
+  if (!chunk_bounds(j.s.w.ctrl, chunk, row0, rows)) return;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;  // warp-uniform
+  const int nvt = (int)j.s.nvt;
+  float lse2[2];
+#pragma unroll
+  for (int side = 0; side < 2; ++side) {
+    const Work& w = side == 0 ? j.s.w : j.t.w;
+    float* stm = w.stm + (int64_t)r * nvt;
+    const float* sts = w.sts + (int64_t)r * nvt;
+    float M = -INFINITY, S = 0.0f;
+    for (int t = lane; t < nvt; t += 32) lse_merge(M, S, stm[t], sts[t]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
+      const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+      lse_merge(M, S, M2, S2);
+    }
+    const float lse = M + logf(S);
+    for (int t = lane; t < nvt; t += 32) stm[t] -= lse;
+    lse2[side] = lse;
+  }
+  if (lane == 0) {
+    const int row = j.s.w.idx[row0 + r];
+    j.s.w.lse[r] = lse2[0];
+    j.t.w.lse[r] = lse2[1];
+    float ar = 1.0f;
+    if (j.s.reduction == FLCE_NONE && j.s.grad_out != nullptr) ar = j.s.grad_out[row];
+    j.s.w.arow[r] = ar;
+  }
+}
+
+// One element's probabilities and logs. e = exp(z - tile max) as stored (may have
+// underflowed to 0 in the 16-bit slab); logs are clamped so that 0 * log(0) terms vanish.
+// The logs use the hardware log2 approximation (__logf): its absolute error, about 1e-7,
+// is far below the 2^-9 relative rounding of the stored e, and these passes are bound by
+// instruction issue when the full-precision logf is used (three logs per element).
+struct Elem {
+  float Q, P, lQ, lP;
+};
+__device__ __forceinline__ float clamped_log(float x) { return __logf(fmaxf(x, 1e-37f)); }
+__device__ __forceinline__ Elem elem(float es, float et, float lqo, float lpo, float qm, float pm) {
+  Elem e;
+  e.Q = es * qm;
+  e.P = et * pm;
+  e.lQ = clamped_log(es) + lqo;
+  e.lP = clamped_log(et) + lpo;
+  return e;
+}
+
+template <typename T> struct Load8;
+template <> struct Load8<__nv_bfloat16> {
+  __device__ static void run(const __nv_bfloat16* p, float (&f)[8]) {
+    const uint4 u = *(const uint4*)p;
+    const __nv_bfloat162* h = (const __nv_bfloat162*)&u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __bfloat1622float2(h[k]);
+      f[2 * k] = x.x;
+      f[2 * k + 1] = x.y;
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&f)[8]) {
+    uint4 u;
+    __nv_bfloat162* h = (__nv_bfloat162*)&u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+    *(uint4*)p = u;
+  }
+};
+template <> struct Load8<__half> {
+  __device__ static void run(const __half* p, float (&f)[8]) {
+    const uint4 u = *(const uint4*)p;
+    const __half2* h = (const __half2*)&u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __half22float2(h[k]);
+      f[2 * k] = x.x;
+      f[2 * k + 1] = x.y;
+    }
+  }
+  __device__ static void store(__half* p, const float (&f)[8]) {
+    uint4 u;
+    __half2* h = (__half2*)&u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) h[k] = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
+    *(uint4*)p = u;
+  }
+};
+template <> struct Load8<float> {
+  __device__ static void run(const float* p, float (&f)[8]) {
+    const float4 x = *(const float4*)p, y = *(const float4*)(p + 4);
+    f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+    f[4] = y.x; f[5] = y.y; f[6] = y.z; f[7] = y.w;
+  }
+  __device__ static void store(float* p, const float (&f)[8]) {
+    *(float4*)p = make_float4(f[0], f[1], f[2], f[3]);
+    *(float4*)(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
+  }
+};
+
+// Per (row, tile): sum_v of the divergence terms and of Q_v g_v (g = dloss/dQ up to a
+// constant), each thread 8 columns, a warp one row of the tile, xor-butterfly reduction.
+// The partial sums overwrite the student / teacher tile sums (no longer needed).
+template <typename T>
+__global__ void __launch_bounds__(256) k_jsd_terms(const __grid_constant__ JsdArgs j, int chunk,
+                                                   int rows_per_block) {
+  int row0, rows;
+  if (!chunk_bounds(j.s.w.ctrl, chunk, row0, rows)) return;
+  const int t = blockIdx.x;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int rb0 = blockIdx.y * rows_per_block;
+  const int rb1 = min(rb0 + rows_per_block, rows);
+  const int64_t c0 = (int64_t)t * VT + tx * 8;
+  const int64_t nvt = j.s.nvt;
+  const float beta = j.beta;
+  for (int r = rb0 + ty; r < rb1; r += 8) {
+    const float lqo = j.s.w.stm[(int64_t)r * nvt + t], lpo = j.t.w.stm[(int64_t)r * nvt + t];
+    const float qm = expf(lqo), pm = expf(lpo);
+    float es[8], et[8];
+    Load8<T>::run((const T*)j.s.w.slab + (int64_t)r * j.s.Vp + c0, es);
+    Load8<T>::run((const T*)j.t.w.slab + (int64_t)r * j.t.Vp + c0, et);
+    float term = 0.0f, qg = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (c0 + k >= j.s.V) continue;
+      const Elem e = elem(es[k], et[k], lqo, lpo, qm, pm);
+      if (beta == 0.0f) {
+        term += e.P * (e.lP - e.lQ);
+      } else if (beta == 1.0f) {
+        const float x = e.Q * (e.lQ - e.lP);
+        term += x;
+        qg += x;
+      } else {
+        const float Mv = beta * e.P + (1.0f - beta) * e.Q;
+        const float lM = clamped_log(Mv);
+        const float qpart = e.Q * (e.lQ - lM);
+        term += beta * e.P * (e.lP - lM) + (1.0f - beta) * qpart;
+        qg += (1.0f - beta) * qpart;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      term += __shfl_xor_sync(0xffffffffu, term, o);
+      qg += __shfl_xor_sync(0xffffffffu, qg, o);
+    }
+    if (tx == 0) {
+      j.s.w.sts[(int64_t)r * nvt + t] = term;
+      j.t.w.sts[(int64_t)r * nvt + t] = qg;
+    }
+  }
+}
+
+// Per row: loss_i = sum over tiles of the term partials, S_i = sum of the Q g partials
+// (fixed order); per-token and per-labelled-row loss outputs.
+__global__ void __launch_bounds__(256) k_jsd_rowsum(const __grid_constant__ JsdArgs j, int chunk) {
+  int row0, rows;
+  if (!chunk_bounds(j.s.w.ctrl, chunk, row0, rows)) return;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const int64_t nvt = j.s.nvt;
+  const float* lp = j.s.w.sts + (int64_t)r * nvt;
+  const float* sp = j.t.w.sts + (int64_t)r * nvt;
+  float L = 0.0f, S = 0.0f;
+  for (int64_t t = lane; t < nvt; t += 32) {
+    L += lp[t];
+    S += sp[t];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    L += __shfl_xor_sync(0xffffffffu, L, o);
+    S += __shfl_xor_sync(0xffffffffu, S, o);
+  }
+  if (lane == 0) {
+    const int row = j.s.w.idx[row0 + r];
+    j.srow[r] = S;
+    j.s.w.rloss[row0 + r] = L;
+    j.s.w.rz[row0 + r] = 0.0f;
+    j.s.w.racc[row0 + r] = 0.0f;
+    if (j.s.reduction == FLCE_NONE) j.s.loss[row] = L;
+  }
+}
+
+// dS = a_i / T * dloss_i/dz_s written over the student slab (in place); rows past the chunk
+// end up to the next multiple of 64 are zeroed (the dW GEMM reduces over them).
+template <typename T>
+__global__ void __launch_bounds__(256) k_jsd_grad(const __grid_constant__ JsdArgs j, int chunk,
+                                                  int rows_per_block) {
+  int row0, rows;
+  if (!chunk_bounds(j.s.w.ctrl, chunk, row0, rows)) return;
+  const int t = blockIdx.x;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int rlim = (int)rup64(rows, 64);
+  const int rb0 = blockIdx.y * rows_per_block;
+  const int rb1 = min(rb0 + rows_per_block, rlim);
+  const int64_t c0 = (int64_t)t * VT + tx * 8;
+  const int64_t nvt = j.s.nvt;
+  const float beta = j.beta;
+  for (int r = rb0 + ty; r < rb1; r += 8) {
+    T* ps = (T*)j.s.w.slab + (int64_t)r * j.s.Vp + c0;
+    float out[8];
+    if (r < rows) {
+      const float lqo = j.s.w.stm[(int64_t)r * nvt + t], lpo = j.t.w.stm[(int64_t)r * nvt + t];
+      const float qm = expf(lqo), pm = expf(lpo);
+      const float f = j.s.w.arow[r] * j.inv_T;
+      const float S = j.srow[r];
+      float es[8], et[8];
+      Load8<T>::run(ps, es);
+      Load8<T>::run((const T*)j.t.w.slab + (int64_t)r * j.t.Vp + c0, et);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const Elem e = elem(es[k], et[k], lqo, lpo, qm, pm);
+        float dz;
+        if (beta == 0.0f) {
+          dz = e.Q - e.P;
+        } else if (beta == 1.0f) {
+          dz = e.Q * ((e.lQ - e.lP) - S);
+        } else {
+          const float Mv = beta * e.P + (1.0f - beta) * e.Q;
+          const float lM = clamped_log(Mv);
+          dz = e.Q * ((1.0f - beta) * (e.lQ - lM) - S);
+        }
+        out[k] = (c0 + k < j.s.V) ? f * dz : 0.0f;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) out[k] = 0.0f;
+    }
+    Load8<T>::store(ps, out);
+  }
+}
+
+template <typename T>
+cudaError_t launch_jsd_elementwise(const JsdArgs& j, int chunk, cudaStream_t s, bool grad) {
+  const int rpb = 256;
+  dim3 grid((unsigned)j.s.nvt, (unsigned)cdiv(j.s.R, rpb));
+  if (!grad) {
+    k_jsd_terms<T><<<grid, 256, 0, s>>>(j, chunk, rpb);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_jsd_rowsum<<<(unsigned)cdiv(j.s.R, 8), 256, 0, s>>>(j, chunk);
+  } else {
+    k_jsd_grad<T><<<grid, 256, 0, s>>>(j, chunk, rpb);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t jsd_elementwise(const JsdArgs& j, int chunk, cudaStream_t s, bool grad) {
+  switch (j.s.dt) {
+    case FLCE_BF16: return launch_jsd_elementwise<__nv_bfloat16>(j, chunk, s, grad);
+    case FLCE_F16: return launch_jsd_elementwise<__half>(j, chunk, s, grad);
+    default: return launch_jsd_elementwise<float>(j, chunk, s, grad);
+  }
+}
+
+inline bool aligned(const void* p, size_t n) { return ((uintptr_t)p % n) == 0; }
+
+int32_t jsd_validate(const flce_jsd_args* x) {
+  if (!x) return FLCE_ERR_INVALID_ARG;
+  if (x->BT <= 0 || x->Hs <= 0 || x->Ht <= 0 || x->V <= 0) return FLCE_ERR_INVALID_ARG;
+  if (x->BT > 0x7fffffffLL || x->Hs > 0x7fffffffLL || x->Ht > 0x7fffffffLL || x->V > 0x7fffffffLL)
+    return FLCE_ERR_INVALID_ARG;
+  if (x->in_dtype != FLCE_F32 && x->in_dtype != FLCE_BF16 && x->in_dtype != FLCE_F16)
+    return FLCE_ERR_INVALID_ARG;
+  if (x->reduction != FLCE_MEAN && x->reduction != FLCE_SUM && x->reduction != FLCE_NONE)
+    return FLCE_ERR_INVALID_ARG;
+  if (!x->Xs || !x->Ws || !x->Xt || !x->Wt || !x->loss || !x->workspace) return FLCE_ERR_INVALID_ARG;
+  if (!(x->beta >= 0.0f && x->beta <= 1.0f)) return FLCE_ERR_INVALID_ARG;
+  if (!(x->temperature > 0.0f) || x->temperature > 1e30f) return FLCE_ERR_INVALID_ARG;
+  if (x->want_dX && !x->dX) return FLCE_ERR_INVALID_ARG;
+  if (x->want_dW && !x->dW) return FLCE_ERR_INVALID_ARG;
+  if (x->want_dW && x->dW_dtype != FLCE_F32 && x->dW_dtype != x->in_dtype) return FLCE_ERR_UNSUPPORTED;
+  if (!aligned(x->Xs, 16) || !aligned(x->Ws, 16) || !aligned(x->Xt, 16) || !aligned(x->Wt, 16) ||
+      !aligned(x->workspace, 256))
+    return FLCE_ERR_INVALID_ARG;
+  if (x->want_dX && !aligned(x->dX, 16)) return FLCE_ERR_INVALID_ARG;
+  if (x->want_dW && !aligned(x->dW, 16)) return FLCE_ERR_INVALID_ARG;
+  if (x->labels && !aligned(x->labels, 8)) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(x->loss, 4) || (x->status && !aligned(x->status, 4))) return FLCE_ERR_INVALID_ARG;
+  return FLCE_OK;
+}
+
+}  // namespace
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" size_t flce_jsd_workspace_size(int64_t BT, int64_t Hs, int64_t Ht, int64_t V, int32_t in_dtype,
+                                          size_t budget_bytes) {
+  if (BT <= 0 || Hs <= 0 || Ht <= 0 || V <= 0) return 0;
+  if (in_dtype != FLCE_F32 && in_dtype != FLCE_BF16 && in_dtype != FLCE_F16) return 0;
+  const int64_t R = jsd_rows_for_bytes(BT, Hs, Ht, V, in_dtype, budget_bytes ? budget_bytes : DEFAULT_BUDGET);
+  if (R <= 0) return 0;
+  JsdPlan p;
+  if (!jsd_layout(BT, Hs, Ht, V, in_dtype, R, &p)) return 0;
+  return p.total;
+}
+
+extern "C" int32_t flce_fused_linear_jsd(const flce_jsd_args* x, void* stream) {
+  const int32_t v = jsd_validate(x);
+  if (v != FLCE_OK) return v;
+  const int64_t R = jsd_rows_for_bytes(x->BT, x->Hs, x->Ht, x->V, x->in_dtype, x->workspace_bytes);
+  if (R <= 0) return FLCE_ERR_WORKSPACE;
+  JsdPlan p;
+  if (!jsd_layout(x->BT, x->Hs, x->Ht, x->V, x->in_dtype, R, &p)) return FLCE_ERR_INVALID_ARG;
+  char* b = (char*)x->workspace;
+
+  CallArgs s;
+  memset(&s, 0, sizeof(s));
+  s.BT = x->BT;
+  s.V = x->V;
+  s.Vp = p.Vp;
+  s.nvt = p.nvt;
+  s.R = p.R;
+  s.dt = x->in_dtype;
+  s.reduction = x->reduction;
+  s.ignore_index = x->ignore_index;
+  s.grad_out = x->grad_out;
+  s.loss = x->loss;
+  s.n_labelled = x->n_labelled;
+  s.want_dX = x->want_dX ? 1 : 0;
+  s.want_dW = x->want_dW ? 1 : 0;
+  s.dW_dt = x->dW_dtype;
+  s.timeout_ns = (uint64_t)(x->wait_timeout_ms ? x->wait_timeout_ms : DEFAULT_TIMEOUT_MS) * 1000000ull;
+  s.flags = x->flags;
+  s.logit_scale = 1.0f / x->temperature;
+  s.labels_are_masks = 1;
+  // shared workspace regions
+  s.w.ctrl = (Ctrl*)(b + p.off_ctrl);
+  s.w.idx = (int*)(b + p.off_idx);
+  s.w.rloss = (float*)(b + p.off_rloss);
+  s.w.rz = (float*)(b + p.off_rz);
+  s.w.racc = (float*)(b + p.off_racc);
+  s.w.arow = (float*)(b + p.off_arow);
+  s.w.status = x->status ? (int*)x->status : &s.w.ctrl->status;
+  CallArgs t = s;
+  // student view
+  s.H = x->Hs;
+  s.Hp = p.Hsp;
+  s.X = x->Xs;
+  s.W = x->Ws;
+  s.dX = s.want_dX ? x->dX : nullptr;
+  s.dW = s.want_dW ? x->dW : nullptr;
+  s.w.xc = b + p.off_xcs;
+  s.w.stm = (float*)(b + p.off_stm_s);
+  s.w.sts = (float*)(b + p.off_sts_s);
+  s.w.sti = (int*)(b + p.off_sti_s);
+  s.w.tgt = (float*)(b + p.off_tgt_s);
+  s.w.lse = (float*)(b + p.off_lse_s);
+  s.w.slab = b + p.off_slab_s;
+  s.w.dxacc = (float*)(b + p.off_dxacc);
+  // teacher view (forward only)
+  t.H = x->Ht;
+  t.Hp = p.Htp;
+  t.X = x->Xt;
+  t.W = x->Wt;
+  t.want_dX = t.want_dW = 0;
+  t.w.xc = b + p.off_xct;
+  t.w.stm = (float*)(b + p.off_stm_t);
+  t.w.sts = (float*)(b + p.off_sts_t);
+  t.w.sti = (int*)(b + p.off_sti_t);
+  t.w.tgt = (float*)(b + p.off_tgt_t);
+  t.w.lse = (float*)(b + p.off_lse_t);
+  t.w.slab = b + p.off_slab_t;
+  t.w.dxacc = nullptr;
+  // compaction reads the labels; the forward GEMMs gather no target logit
+  CallArgs comp = s;
+  comp.targets = x->labels;
+  s.targets = nullptr;
+  t.targets = nullptr;
+
+  JsdArgs j;
+  j.s = s;
+  j.t = t;
+  j.beta = x->beta;
+  j.inv_T = 1.0f / x->temperature;
+  j.srow = (float*)(b + p.off_srow);
+
+  cudaStream_t st = (cudaStream_t)stream;
+  const bool tc = !(x->flags & FLCE_FLAG_FORCE_SIMT) && tc_supported(s) && tc_supported(t);
+  const bool grads = s.want_dX || s.want_dW;
+#define JSD_TRY(expr)                     \
+  do {                                    \
+    if ((expr) != cudaSuccess) return FLCE_ERR_CUDA; \
+  } while (0)
+  flce_profile* prof = x->profile;
+  JSD_TRY(cudaMemsetAsync(s.w.status, 0, sizeof(int), st));
+  JSD_TRY(staged(prof, FLCE_STAGE_PROLOGUE, 2, st, [&] { return launch_prologue(comp, st); }));
+  for (int k = 0; k < (int)p.kmax; ++k) {
+    JSD_TRY(staged(prof, FLCE_STAGE_GATHER, 2, st, [&] {
+      cudaError_t e = launch_gather(s, k, st);
+      return e != cudaSuccess ? e : launch_gather(t, k, st);
+    }));
+    JSD_TRY(staged(prof, FLCE_STAGE_FWD, 2, st, [&] {
+      cudaError_t e = tc ? launch_fwd_tc(s, k, st) : launch_fwd_simt(s, k, st);
+      return e != cudaSuccess ? e : (tc ? launch_fwd_tc(t, k, st) : launch_fwd_simt(t, k, st));
+    }));
+    JSD_TRY(staged(prof, FLCE_STAGE_FINALIZE, 1, st, [&] {
+      k_jsd_finalize<<<(unsigned)cdiv(p.R, 8), 256, 0, st>>>(j, k);
+      return cudaGetLastError();
+    }));
+    JSD_TRY(staged(prof, FLCE_STAGE_GPASS, grads ? 3 : 2, st, [&] {
+      cudaError_t e = jsd_elementwise(j, k, st, false);
+      return (e != cudaSuccess || !grads) ? e : jsd_elementwise(j, k, st, true);
+    }));
+    if (s.want_dX) {
+      if (tc) {
+        JSD_TRY(staged(prof, FLCE_STAGE_DX, 2, st, [&] {
+          cudaError_t e = cudaMemsetAsync(s.w.dxacc, 0, (size_t)p.R * s.H * 4, st);
+          if (e == cudaSuccess) e = launch_dx_tc(s, k, st);
+          return e != cudaSuccess ? e : launch_dx_store(s, k, st);
+        }));
+      } else {
+        JSD_TRY(staged(prof, FLCE_STAGE_DX, 1, st, [&] { return launch_dx_simt(s, k, st); }));
+      }
+    }
+    if (s.want_dW)
+      JSD_TRY(staged(prof, FLCE_STAGE_DW, 1, st,
+                     [&] { return tc ? launch_dw_tc(s, k, st) : launch_dw_simt(s, k, st); }));
+  }
+  if (s.reduction != FLCE_NONE)
+    JSD_TRY(staged(prof, FLCE_STAGE_REDUCE, 1, st, [&] { return launch_epilogue(s, st); }));
+#undef JSD_TRY
+  return FLCE_OK;
+}

@@ -35,10 +35,14 @@ __global__ void __launch_bounds__(1024) k_compact(const __grid_constant__ CallAr
     const int64_t i = b0 + tid;
     int lab = 0;
     if (i < a.BT) {
-      const int64_t t = a.targets[i];
-      if (t != a.ignore_index) {
-        if (t >= 0 && t < a.V) lab = 1;
-        else bad = 1;
+      if (a.targets == nullptr) {
+        lab = 1;  // no labels: every row takes part
+      } else {
+        const int64_t t = a.targets[i];
+        if (t != a.ignore_index) {
+          if (a.labels_are_masks || (t >= 0 && t < a.V)) lab = 1;
+          else bad = 1;
+        }
       }
     }
     const unsigned m = __ballot_sync(0xffffffffu, lab);
@@ -90,12 +94,13 @@ __global__ void __launch_bounds__(1024) k_compact(const __grid_constant__ CallAr
 
 // Ignored rows: per-token outputs (PR #1554, Details item 1) and a zero dX row.
 __global__ void __launch_bounds__(256) k_ignored(const __grid_constant__ CallArgs a) {
+  if (a.targets == nullptr) return;  // no labels: no ignored rows
   for (int64_t i = blockIdx.x; i < a.BT; i += gridDim.x) {
     const int64_t t = a.targets[i];
-    if (is_labelled(t, a.ignore_index, a.V)) continue;
+    if (a.labels_are_masks ? t != a.ignore_index : is_labelled(t, a.ignore_index, a.V)) continue;
     if (threadIdx.x == 0) {
       if (a.reduction == FLCE_NONE) {
-        a.loss[i] = 0.0f;
+        if (a.loss) a.loss[i] = 0.0f;
         if (a.z_loss) a.z_loss[i] = 0.0f;
         if (a.acc) a.acc[i] = 0.0f;
       }
@@ -416,7 +421,7 @@ __global__ void __launch_bounds__(256) k_fwd_simt(const __grid_constant__ CallAr
     float b = 0.0f;
     if (a.bias != nullptr && v < V) b = to_f<T>(((const T*)a.bias)[v]);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) Ss[i * 257 + tid] = acc[i] + b;
+    for (int i = 0; i < 16; ++i) Ss[i * 257 + tid] = fmaf(acc[i], a.logit_scale, b);
   }
   __syncthreads();
   const int lane = tid & 31, warp = tid >> 5;
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(256) k_fwd_simt(const __grid_constant__ CallAr
   for (int i = warp; i < 16; i += 8) {
     const int rr = mb * 16 + i;
     if (rr >= rows) continue;
-    const int64_t tg = a.targets[a.w.idx[row0 + rr]];
+    const int64_t tg = a.targets ? a.targets[a.w.idx[row0 + rr]] : -1;
     float mx = -INFINITY;
     int ai = t * VT;
     float tl = 0.0f;

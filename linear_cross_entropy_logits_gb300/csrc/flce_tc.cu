@@ -373,8 +373,9 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
   const bool valid = rr < rows;
   const int V = (int)a.V;
   int64_t tg = -1;
-  if (valid) tg = a.targets[a.w.idx[row0 + rr]];
+  if (valid && a.targets != nullptr) tg = a.targets[a.w.idx[row0 + rr]];
   const int v0 = n * VT;
+  const float ls = a.logit_scale;
   const T* bias = (const T*)a.bias;
   float mx = -INFINITY, tl = 0.0f;
   int ai = v0;
@@ -386,7 +387,7 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int v = v0 + cc * 32 + j;
-      float s = __uint_as_float(r[j]);
+      float s = __uint_as_float(r[j]) * ls;
       if (v < V) {
         if (bias != nullptr) s += to_f<T>(bias[v]);
         if (s > mx) {
@@ -421,7 +422,7 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const int v = v0 + c2 * 64 + hh * 32 + j;
-        float s0 = __uint_as_float(r[j]), s1 = __uint_as_float(r[j + 1]);
+        float s0 = __uint_as_float(r[j]) * ls, s1 = __uint_as_float(r[j + 1]) * ls;
         float e0 = 0.0f, e1 = 0.0f;
         if (v < V) {
           if (bias != nullptr) s0 += to_f<T>(bias[v]);

@@ -25,7 +25,8 @@ FLAG_DEBUG_STALL = 0x100
 EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_fwd_bwd_noalloc",
             "flce_get_status",
             "flce_profile_create", "flce_profile_reset", "flce_profile_destroy",
-            "flce_profile_read", "flce_last_cuda_error", "flce_status_string", "flce_abi_version")
+            "flce_profile_read", "flce_last_cuda_error", "flce_status_string", "flce_abi_version",
+            "flce_jsd_workspace_size", "flce_fused_linear_jsd")
 STAGES = ("prologue", "gather", "fwd", "finalize", "gpass", "dx", "dw", "reduce")
 
 
@@ -43,6 +44,23 @@ class FlceArgs(ctypes.Structure):
         ("lse", ctypes.c_void_p), ("pred", ctypes.c_void_p), ("n_labelled", ctypes.c_void_p),
         ("dX", ctypes.c_void_p), ("dW", ctypes.c_void_p), ("dbias", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_uint32),
+        ("profile", ctypes.c_void_p),
+    ]
+
+
+class FlceJsdArgs(ctypes.Structure):
+    """Mirror of ``flce_jsd_args`` (field order and C types must match include/flce.h)."""
+    _fields_ = [
+        ("BT", ctypes.c_int64), ("Hs", ctypes.c_int64), ("Ht", ctypes.c_int64), ("V", ctypes.c_int64),
+        ("in_dtype", ctypes.c_int32), ("reduction", ctypes.c_int32),
+        ("Xs", ctypes.c_void_p), ("Ws", ctypes.c_void_p), ("Xt", ctypes.c_void_p), ("Wt", ctypes.c_void_p),
+        ("labels", ctypes.c_void_p), ("ignore_index", ctypes.c_int64),
+        ("beta", ctypes.c_float), ("temperature", ctypes.c_float), ("grad_out", ctypes.c_void_p),
+        ("want_dX", ctypes.c_int32), ("want_dW", ctypes.c_int32), ("dW_dtype", ctypes.c_int32),
+        ("flags", ctypes.c_uint32),
+        ("loss", ctypes.c_void_p), ("n_labelled", ctypes.c_void_p), ("dX", ctypes.c_void_p),
+        ("dW", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_uint32),
         ("profile", ctypes.c_void_p),
     ]
@@ -75,6 +93,10 @@ def load(path: str | None = None):
     lib.flce_abi_version.restype = ctypes.c_int32
     lib.flce_last_cuda_error.restype = ctypes.c_char_p
     lib.flce_last_cuda_error.argtypes = []
+    lib.flce_jsd_workspace_size.restype = ctypes.c_size_t
+    lib.flce_jsd_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.c_size_t]
+    lib.flce_fused_linear_jsd.restype = ctypes.c_int32
+    lib.flce_fused_linear_jsd.argtypes = [ctypes.POINTER(FlceJsdArgs), ctypes.c_void_p]
     lib.flce_profile_create.restype = ctypes.c_void_p
     lib.flce_profile_create.argtypes = []
     lib.flce_profile_reset.restype = None
@@ -226,6 +248,69 @@ def fwd_bwd(X, W, targets, bias=None, *, ignore_index=-100, reduction="mean",
         raise FlceError(rc, "flce_fwd_bwd")
     o["dW"], o["dbias"] = dW, dbias
     o["workspace"] = workspace
+    if check:
+        o["status_code"] = int(lib.flce_get_status(ctypes.c_void_p(_ptr(o["status"])), None,
+                                                   ctypes.c_void_p(s.cuda_stream)))
+    return o
+
+
+def jsd_workspace_size(BT, Hs, Ht, V, dtype=torch.bfloat16, budget_bytes=0) -> int:
+    return int(load().flce_jsd_workspace_size(BT, Hs, Ht, V, DTYPES[dtype], budget_bytes))
+
+
+def fused_linear_jsd(Xs, Ws, Xt, Wt, labels=None, *, beta=0.5, temperature=1.0, ignore_index=-100,
+                     reduction="mean", grad_out=None, want_dX=True, want_dW=True, dW=None,
+                     workspace=None, budget_bytes=0, flags=0, check=True, stream=None, profiler=None,
+                     outputs=None):
+    """Fused linear JSD / KL distillation forward + backward (student gradients only).
+    Returns a dict with loss, n_labelled, dX, dW (and status_code when ``check``)."""
+    lib = load()
+    BT, Hs = Xs.shape
+    Ht = Xt.shape[1]
+    V = Ws.shape[0]
+    dev = Xs.device
+    nl = BT if reduction == "none" else 1
+    o = dict(outputs or {})
+    if o.get("loss") is None:
+        o["loss"] = torch.empty(nl, dtype=torch.float32, device=dev)
+    if o.get("n_labelled") is None:
+        o["n_labelled"] = torch.empty(1, dtype=torch.int32, device=dev)
+    if o.get("status") is None:
+        o["status"] = torch.zeros(1, dtype=torch.int32, device=dev)
+    if want_dX and o.get("dX") is None:
+        o["dX"] = torch.empty_like(Xs)
+    if want_dW and dW is None:
+        dW = torch.zeros(V, Hs, dtype=torch.float32, device=dev)
+    if workspace is None:
+        nbytes = jsd_workspace_size(BT, Hs, Ht, V, Xs.dtype, budget_bytes)
+        if nbytes == 0:
+            raise FlceError(FLCE_ERR_WORKSPACE, "jsd_workspace_size")
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if grad_out is not None and not torch.is_tensor(grad_out):
+        grad_out = torch.tensor([float(grad_out)], dtype=torch.float32, device=dev)
+    a = FlceJsdArgs()
+    a.BT, a.Hs, a.Ht, a.V = BT, Hs, Ht, V
+    a.in_dtype = DTYPES[Xs.dtype]
+    a.reduction = REDUCTIONS[reduction]
+    a.Xs, a.Ws, a.Xt, a.Wt = _ptr(Xs), _ptr(Ws), _ptr(Xt), _ptr(Wt)
+    a.labels = _ptr(labels)
+    a.ignore_index = ignore_index
+    a.beta, a.temperature = beta, temperature
+    a.grad_out = _ptr(grad_out)
+    a.want_dX, a.want_dW = int(bool(want_dX)), int(bool(want_dW))
+    a.dW_dtype = DTYPES[dW.dtype] if dW is not None else 0
+    a.flags = flags
+    a.loss, a.n_labelled = _ptr(o["loss"]), _ptr(o["n_labelled"])
+    a.dX = _ptr(o.get("dX")) if want_dX else None
+    a.dW = _ptr(dW) if want_dW else None
+    a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+    a.status = _ptr(o["status"])
+    a.profile = profiler.handle if profiler is not None else None
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    rc = lib.flce_fused_linear_jsd(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream))
+    if rc != FLCE_OK:
+        raise FlceError(rc, "flce_fused_linear_jsd")
+    o["dW"] = dW
     if check:
         o["status_code"] = int(lib.flce_get_status(ctypes.c_void_p(_ptr(o["status"])), None,
                                                    ctypes.c_void_p(s.cuda_stream)))

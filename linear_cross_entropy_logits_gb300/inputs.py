@@ -21,6 +21,11 @@ Workloads (shapes after the pages' model heads):
                     k maps to token k-1), sum, dX and fp32 dW.
   * ``frozen_head`` BT=16384, H=4096, V=151936, bf16, bias~N(0,0.01^2), 8192 rows ignored at
                     random, none with a per-token upstream gradient ~U(0.5,1.5), dX only.
+  * ``distill``     fused linear JSD distillation: student Llama-3.2-1B-shaped head (Hs=2048)
+                    against a Llama-3.1-8B-shaped teacher head (Ht=4096), V=128256,
+                    BT=8192, bf16, W~N(0,0.02^2), all rows labelled, beta=0.5, T=1, mean,
+                    student dX and fp32 dW. Drawn by generate_distill: labels, X_s, W_s,
+                    X_t, W_t.
 """
 
 from __future__ import annotations
@@ -50,6 +55,10 @@ WORKLOADS = {
                         bias_std=0.01, targets="uniform", ignore="random", n_ignored=8192,
                         reduction="none", grad_out="uniform", z=0.0, want_dW=False),
 }
+
+DISTILL = dict(name="distill", BT=8192, Hs=2048, Ht=4096, V=128256, dtype="bf16", x_std=1.0,
+               w_std=0.02, ignore="none", beta=0.5, temperature=1.0, reduction="mean",
+               want_dW=True)
 
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
@@ -118,6 +127,23 @@ def generate(sp, seed=0):
     if sp.get("grad_out") == "uniform":
         grad_out = torch.rand(BT, generator=g) + 0.5
     return {"X": X, "W": W, "bias": bias, "targets": targets, "grad_out": grad_out}
+
+
+def generate_distill(sp=None, seed=0):
+    """Draw one distillation problem on the CPU: labels int64 [BT] (ignored rows per
+    ``ignore``/``n_ignored``), Xs [BT,Hs], Ws [V,Hs], Xt [BT,Ht], Wt [V,Ht]."""
+    sp = dict(DISTILL, **(sp or {}))
+    BT, V = sp["BT"], sp["V"]
+    dt = TORCH_DTYPES[sp["dtype"]]
+    g = torch.Generator().manual_seed(seed)
+    labels = torch.randint(0, V, (BT,), generator=g, dtype=torch.int64)
+    if sp.get("ignore") == "random":
+        labels[torch.randperm(BT, generator=g)[:sp["n_ignored"]]] = IGNORE_INDEX
+    Xs = (torch.randn(BT, sp["Hs"], generator=g) * sp["x_std"]).to(dt)
+    Ws = (torch.randn(V, sp["Hs"], generator=g) * sp["w_std"]).to(dt)
+    Xt = (torch.randn(BT, sp["Ht"], generator=g) * sp["x_std"]).to(dt)
+    Wt = (torch.randn(V, sp["Ht"], generator=g) * sp["w_std"]).to(dt)
+    return {"labels": labels, "Xs": Xs, "Ws": Ws, "Xt": Xt, "Wt": Wt}
 
 
 def to_numpy_exact(t):

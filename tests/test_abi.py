@@ -44,11 +44,12 @@ def test_library_exports_every_declared_symbol(lib):
     assert lib.flce_abi_version() == 1
 
 
-def test_struct_layout_matches_c(lib):
-    fields = [f for f, _ in flce.FlceArgs._fields_]
+@pytest.mark.parametrize("cls,cname", [(flce.FlceArgs, "flce_args"), (flce.FlceJsdArgs, "flce_jsd_args")])
+def test_struct_layout_matches_c(lib, cls, cname):
+    fields = [f for f, _ in cls._fields_]
     src = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){",
-           'printf("%zu\\n", sizeof(flce_args));']
-    src += [f'printf("%zu\\n", offsetof(flce_args, {f}));' for f in fields]
+           f'printf("%zu\\n", sizeof({cname}));']
+    src += [f'printf("%zu\\n", offsetof({cname}, {f}));' for f in fields]
     src.append("return 0;}")
     with tempfile.TemporaryDirectory() as d:
         c = os.path.join(d, "layout.c")
@@ -57,9 +58,9 @@ def test_struct_layout_matches_c(lib):
         subprocess.run(["gcc", "-std=c99", "-o", exe, c], check=True)
         vals = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
                                                check=True).stdout.split()]
-    assert vals[0] == ctypes.sizeof(flce.FlceArgs)
+    assert vals[0] == ctypes.sizeof(cls)
     for f, off in zip(fields, vals[1:]):
-        assert getattr(flce.FlceArgs, f).offset == off, f
+        assert getattr(cls, f).offset == off, f
 
 
 @pytest.mark.parametrize("H,V,dt", [(4096, 128256, torch.bfloat16), (5376, 262144, torch.bfloat16),
@@ -136,3 +137,37 @@ def test_torch_custom_op_registers():
     from linear_cross_entropy_logits_gb300 import torch_ops
     assert hasattr(torch.ops.flce_gb300, "fused_linear_cross_entropy")
     assert callable(torch_ops.fused_linear_cross_entropy)
+
+
+def _jsd_args(**kw):
+    a = flce.FlceJsdArgs()
+    a.BT, a.Hs, a.Ht, a.V = 16, 64, 32, 100
+    a.in_dtype, a.reduction = 1, 0
+    a.Xs, a.Ws, a.Xt, a.Wt, a.loss = 0x1000, 0x2000, 0x3000, 0x4000, 0x5000
+    a.beta, a.temperature = 0.5, 1.0
+    a.workspace, a.workspace_bytes = 0x100000, 1 << 30
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Xt=None), flce.FLCE_ERR_INVALID_ARG),
+    (dict(beta=1.5), flce.FLCE_ERR_INVALID_ARG),
+    (dict(beta=-0.1), flce.FLCE_ERR_INVALID_ARG),
+    (dict(temperature=0.0), flce.FLCE_ERR_INVALID_ARG),
+    (dict(Ht=0), flce.FLCE_ERR_INVALID_ARG),
+    (dict(want_dX=1, dX=None), flce.FLCE_ERR_INVALID_ARG),
+    (dict(want_dW=1, dW=0x6000, dW_dtype=2), flce.FLCE_ERR_UNSUPPORTED),
+    (dict(workspace_bytes=2048), flce.FLCE_ERR_WORKSPACE),
+])
+def test_jsd_host_validation(lib, kw, code):
+    a = _jsd_args(**kw)
+    assert lib.flce_fused_linear_jsd(ctypes.byref(a), None) == code
+
+
+def test_jsd_workspace_flat_in_BT(lib):
+    s = {BT: flce.jsd_workspace_size(BT, 2048, 4096, 128256, torch.bfloat16, int(1.5 * 2 ** 30))
+         for BT in (8192, 16384)}
+    assert 0 < s[8192] <= int(1.5 * 2 ** 30)
+    assert abs((s[16384] - s[8192]) - 16 * 8192) <= 4 * 256

@@ -1,0 +1,167 @@
+"""GPU parity of the fused linear JSD / KL distillation op (through the C ABI) against the
+float64 oracle, element by element, at sizes spanning several tiles with ragged tails.
+Tolerances as for the cross-entropy op: bf16 inputs loss rel <= 2e-3 and dX/dW
+rel-Frobenius <= 1e-2; fp32 inputs 1e-5."""
+
+import numpy as np
+import pytest
+import torch
+
+from linear_cross_entropy_logits_gb300 import build as B
+from linear_cross_entropy_logits_gb300 import flce
+from linear_cross_entropy_logits_gb300 import inputs as I
+from oracle import jsd_oracle as jo
+from parity_util import TOL, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.build()
+    flce.load()
+
+
+def _problem(BT, Hs, Ht, V, dt, seed, n_ignored, w_std=0.1):
+    g = torch.Generator().manual_seed(seed)
+    tdt = I.TORCH_DTYPES[dt]
+    labels = torch.randint(0, V, (BT,), generator=g, dtype=torch.int64)
+    labels[torch.randperm(BT, generator=g)[:n_ignored]] = I.IGNORE_INDEX
+    Xs = torch.randn(BT, Hs, generator=g).to(tdt)
+    Ws = (torch.randn(V, Hs, generator=g) * w_std).to(tdt)
+    Xt = torch.randn(BT, Ht, generator=g).to(tdt)
+    Wt = (torch.randn(V, Ht, generator=g) * w_std).to(tdt)
+    go = torch.rand(BT, generator=g) + 0.5
+    return Xs, Ws, Xt, Wt, labels, go
+
+
+def _check(dt, beta, T, reduction, path, BT=300, Hs=192, Ht=256, V=3000, n_ignored=40, seed=60,
+           labels_none=False):
+    Xs, Ws, Xt, Wt, labels, go = _problem(BT, Hs, Ht, V, dt, seed, n_ignored)
+    lab = None if labels_none else labels
+    gcuda = go.cuda() if reduction == "none" else None
+    out = flce.fused_linear_jsd(Xs.cuda(), Ws.cuda(), Xt.cuda(), Wt.cuda(),
+                                None if lab is None else lab.cuda(), beta=beta, temperature=T,
+                                reduction=reduction, grad_out=gcuda,
+                                flags=flce.FLAG_FORCE_SIMT if path == "simt" else 0)
+    assert out["status_code"] == flce.FLCE_OK
+    f = I.to_numpy_exact
+    o = jo.jsd_oracle(f(Xs), f(Ws), f(Xt), f(Wt), None if lab is None else lab.numpy(), beta=beta,
+                      temperature=T, reduction=reduction,
+                      grad_out=go.numpy() if reduction == "none" else None)
+    tol = TOL[dt]
+    loss = out["loss"].cpu().numpy()
+    if reduction == "none":
+        m = o["mask"]
+        assert np.all(loss[~m] == 0)
+        ref = o["loss"][m]
+        err = np.max(np.abs(loss[m] - ref) / np.maximum(np.abs(ref), 1e-3))
+    else:
+        err = abs(float(loss[0]) - o["loss"]) / max(abs(o["loss"]), 1e-6)
+    assert err <= tol["loss"], f"loss rel err {err}"
+    assert int(out["n_labelled"][0]) == o["n_labelled"]
+    dX = out["dX"].float().cpu().numpy()
+    assert rel_fro(dX, o["dX"]) <= tol["grad"]
+    assert np.all(dX[~o["mask"]] == 0)
+    assert rel_fro(out["dW"].cpu().numpy(), o["dW"]) <= tol["grad"]
+
+
+@pytest.mark.parametrize("beta", [0.0, 0.5, 1.0])
+@pytest.mark.parametrize("path", ["tc", "simt"])
+def test_jsd_parity_bf16(beta, path):
+    _check("bf16", beta, 1.0, "mean", path)
+
+
+@pytest.mark.parametrize("beta,T,reduction", [(0.3, 2.0, "sum"), (0.7, 0.5, "none"), (0.0, 3.0, "none")])
+def test_jsd_parity_temperatures_and_reductions(beta, T, reduction):
+    _check("bf16", beta, T, reduction, "tc", BT=260, Hs=136, Ht=520, V=1300, seed=61)
+
+
+def test_jsd_parity_fp32():
+    _check("f32", 0.5, 1.5, "mean", "simt", BT=128, Hs=64, Ht=96, V=1000, n_ignored=13, seed=62)
+
+
+def test_jsd_no_labels_and_multichunk():
+    """labels = NULL: every row counts; a small workspace forces several chunks."""
+    Xs, Ws, Xt, Wt, labels, _ = _problem(700, 128, 64, 2000, "bf16", 63, 0)
+    budget = flce.jsd_workspace_size(128, 128, 64, 2000, torch.bfloat16, 0) + 16 * 700 + 4096
+    out = flce.fused_linear_jsd(Xs.cuda(), Ws.cuda(), Xt.cuda(), Wt.cuda(), None, beta=0.5,
+                                budget_bytes=budget)
+    assert out["status_code"] == flce.FLCE_OK
+    f = I.to_numpy_exact
+    o = jo.jsd_oracle(f(Xs), f(Ws), f(Xt), f(Wt), None, beta=0.5)
+    assert abs(float(out["loss"][0]) - o["loss"]) <= 2e-3 * abs(o["loss"])
+    assert rel_fro(out["dX"].float().cpu().numpy(), o["dX"]) <= 1e-2
+    assert rel_fro(out["dW"].cpu().numpy(), o["dW"]) <= 1e-2
+
+
+def test_jsd_nan_in_ignored_rows_does_not_leak():
+    Xs, Ws, Xt, Wt, labels, _ = _problem(256, 128, 128, 1500, "bf16", 64, 90)
+    args = [t.cuda() for t in (Xs, Ws, Xt, Wt)]
+    clean = flce.fused_linear_jsd(*args, labels.cuda(), beta=0.5, reduction="sum")
+    ign = labels == I.IGNORE_INDEX
+    Xs2, Xt2 = Xs.clone(), Xt.clone()
+    Xs2[ign] = float("nan")
+    Xt2[ign] = float("nan")
+    dirty = flce.fused_linear_jsd(Xs2.cuda(), args[1], Xt2.cuda(), args[3], labels.cuda(), beta=0.5,
+                                  reduction="sum")
+    for k in ("loss", "dX", "dW"):
+        assert torch.equal(clean[k], dirty[k]), k
+
+
+def test_jsd_identical_teacher_gives_zero():
+    Xs, Ws, _, _, labels, _ = _problem(200, 128, 128, 1200, "bf16", 65, 20)
+    a = [Xs.cuda(), Ws.cuda()]
+    out = flce.fused_linear_jsd(a[0], a[1], a[0], a[1], labels.cuda(), beta=0.5, reduction="sum")
+    assert abs(float(out["loss"][0])) < 1e-4
+    assert float(out["dW"].abs().max()) < 1e-4 and float(out["dX"].float().abs().max()) < 1e-4
+
+
+def test_jsd_distill_full_size_sampled():
+    """The distillation workload at full size, in the launch configuration the benchmark
+    times (default workspace budget), checked on what the oracle can compute one row at a
+    time: per-token losses and dX on 32 seeded rows, the mean as the mean of the per-token
+    losses, every dW column summing to zero over the vocabulary (each row's dz sums to
+    zero), and dW exactly on 256 sampled vocabulary rows of a run in which only 48 seeded
+    rows keep their label."""
+    sp = dict(I.DISTILL)
+    inp = I.generate_distill(sp, seed=0)
+    d = {k: v.cuda() for k, v in inp.items()}
+    BT, V = sp["BT"], sp["V"]
+    f = I.to_numpy_exact
+    Xs, Ws, Xt, Wt = f(inp["Xs"]), f(inp["Ws"]), f(inp["Xt"]), f(inp["Wt"])
+    lab = inp["labels"].numpy()
+    N = int((lab != I.IGNORE_INDEX).sum())
+    beta, T = sp["beta"], sp["temperature"]
+    full = flce.fused_linear_jsd(d["Xs"], d["Ws"], d["Xt"], d["Wt"], d["labels"], beta=beta,
+                                 temperature=T, reduction="mean")
+    assert full["status_code"] == flce.FLCE_OK and int(full["n_labelled"][0]) == N
+    per = flce.fused_linear_jsd(d["Xs"], d["Ws"], d["Xt"], d["Wt"], d["labels"], beta=beta,
+                                temperature=T, reduction="none", want_dX=False, want_dW=False)
+    per = per["loss"].cpu().numpy().astype(np.float64)
+    assert abs(float(full["loss"][0]) - per.sum() / N) <= 1e-5 * abs(per.sum() / N)
+
+    rng = np.random.default_rng(4321)
+    rows = np.sort(rng.choice(BT, size=32, replace=False))
+    o = jo.jsd_oracle(Xs[rows], Ws, Xt[rows], Wt, lab[rows], beta=beta, temperature=T,
+                      reduction="none", grad_out=np.full(rows.size, 1.0 / N), want_dW=False)
+    assert np.max(np.abs(per[rows] - o["loss"]) / np.maximum(np.abs(o["loss"]), 1e-3)) <= TOL["bf16"]["loss"]
+    dX = full["dX"][torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    assert rel_fro(dX, o["dX"]) <= TOL["bf16"]["grad"]
+
+    dW = full["dW"].double()
+    assert dW.sum(dim=0).abs().max().item() <= 1e-3 * dW.abs().sum(dim=0).max().item()
+
+    keep = np.sort(rng.choice(BT, size=48, replace=False))
+    lab2 = np.full(BT, I.IGNORE_INDEX, dtype=np.int64)
+    lab2[keep] = lab[keep]
+    g2 = flce.fused_linear_jsd(d["Xs"], d["Ws"], d["Xt"], d["Wt"], torch.from_numpy(lab2).cuda(),
+                               beta=beta, temperature=T, reduction="mean", want_dX=False)
+    assert g2["status_code"] == flce.FLCE_OK
+    o2 = jo.jsd_oracle(Xs[keep], Ws, Xt[keep], Wt, lab2[keep], beta=beta, temperature=T,
+                       reduction="mean", want_dX=False)
+    vs = np.sort(rng.choice(V, size=256, replace=False))
+    got = g2["dW"][torch.from_numpy(vs).cuda()].cpu().numpy()
+    assert rel_fro(got, o2["dW"][vs]) <= TOL["bf16"]["grad"]
