@@ -199,13 +199,16 @@ def traffic_record():
     return rec
 
 
+# The sources the tensor-core GEMM kernel (the dominant kernel) is compiled from.
+GEMM_SOURCES = ("flce_internal.cuh", "flce_tc.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_cross_entropy_logits_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for name in GEMM_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()
 
 

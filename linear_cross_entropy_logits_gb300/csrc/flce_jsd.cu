@@ -150,29 +150,27 @@ __global__ void __launch_bounds__(256) k_jsd_finalize(const __grid_constant__ Js
   }
 }
 
-// One element's probabilities and logs. e = exp(z - tile max) as stored (may have
-// underflowed to 0 in the 16-bit slab); logs are clamped so that 0 * log(0) terms vanish.
-// The logs use the hardware log2 approximation (__logf): its absolute error, about 1e-7,
-// is far below the 2^-9 relative rounding of the stored e, and these passes are bound by
-// instruction issue when the full-precision logf is used (three logs per element).
-struct Elem {
-  float Q, P, lQ, lP;
-};
-__device__ __forceinline__ float clamped_log(float x) { return __logf(fmaxf(x, 1e-37f)); }
-__device__ __forceinline__ Elem elem(float es, float et, float lqo, float lpo, float qm, float pm) {
-  Elem e;
-  e.Q = es * qm;
-  e.P = et * pm;
-  e.lQ = clamped_log(es) + lqo;
-  e.lP = clamped_log(et) + lpo;
-  return e;
+// Logs in base 2, from the hardware approximation (lg2.approx.ftz: absolute error about
+// 2^-22 near 1, relative error a few ulp elsewhere), far below the 2^-9 relative rounding
+// of the stored e. Arguments are clamped to a normal float so that 0 * log(0) terms vanish
+// (e underflows to 0 in the 16-bit slab for very unlikely tokens). Working in base 2 and
+// scaling the per-tile sums by ln 2 once keeps these passes to three special-function
+// operations per element.
+__device__ __forceinline__ float lg2_clamped(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(fmaxf(x, 1e-37f)));
+  return y;
 }
+constexpr float LN2 = 0.6931471805599453f;
 
+// Eight consecutive slab elements: a raw 16-byte (32-byte for fp32) vector load, kept packed
+// in registers until it is converted, and the matching converting store.
 template <typename T> struct Load8;
 template <> struct Load8<__nv_bfloat16> {
-  __device__ static void run(const __nv_bfloat16* p, float (&f)[8]) {
-    const uint4 u = *(const uint4*)p;
-    const __nv_bfloat162* h = (const __nv_bfloat162*)&u;
+  struct Raw { uint4 u; };
+  __device__ static Raw load(const __nv_bfloat16* p) { return Raw{*(const uint4*)p}; }
+  __device__ static void cvt(const Raw& r, float (&f)[8]) {
+    const __nv_bfloat162* h = (const __nv_bfloat162*)&r.u;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float2 x = __bfloat1622float2(h[k]);
@@ -189,9 +187,10 @@ template <> struct Load8<__nv_bfloat16> {
   }
 };
 template <> struct Load8<__half> {
-  __device__ static void run(const __half* p, float (&f)[8]) {
-    const uint4 u = *(const uint4*)p;
-    const __half2* h = (const __half2*)&u;
+  struct Raw { uint4 u; };
+  __device__ static Raw load(const __half* p) { return Raw{*(const uint4*)p}; }
+  __device__ static void cvt(const Raw& r, float (&f)[8]) {
+    const __half2* h = (const __half2*)&r.u;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float2 x = __half22float2(h[k]);
@@ -208,10 +207,11 @@ template <> struct Load8<__half> {
   }
 };
 template <> struct Load8<float> {
-  __device__ static void run(const float* p, float (&f)[8]) {
-    const float4 x = *(const float4*)p, y = *(const float4*)(p + 4);
-    f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
-    f[4] = y.x; f[5] = y.y; f[6] = y.z; f[7] = y.w;
+  struct Raw { float4 a, b; };
+  __device__ static Raw load(const float* p) { return Raw{*(const float4*)p, *(const float4*)(p + 4)}; }
+  __device__ static void cvt(const Raw& r, float (&f)[8]) {
+    f[0] = r.a.x; f[1] = r.a.y; f[2] = r.a.z; f[3] = r.a.w;
+    f[4] = r.b.x; f[5] = r.b.y; f[6] = r.b.z; f[7] = r.b.w;
   }
   __device__ static void store(float* p, const float (&f)[8]) {
     *(float4*)p = make_float4(f[0], f[1], f[2], f[3]);
@@ -221,7 +221,12 @@ template <> struct Load8<float> {
 
 // Per (row, tile): sum_v of the divergence terms and of Q_v g_v (g = dloss/dQ up to a
 // constant), each thread 8 columns, a warp one row of the tile, xor-butterfly reduction.
-// The partial sums overwrite the student / teacher tile sums (no longer needed).
+// Each warp takes RU rows per iteration (loads for all of them issued first) so that
+// enough bytes are in flight to cover DRAM latency. The slab's pad columns (v >= V) hold
+// exact zeros, whose terms vanish, so no column test is needed. The partial sums
+// overwrite the student / teacher tile sums (no longer needed).
+constexpr int RU = 4;
+
 template <typename T>
 __global__ void __launch_bounds__(256) k_jsd_terms(const __grid_constant__ JsdArgs j, int chunk,
                                                    int rows_per_block) {
@@ -233,40 +238,66 @@ __global__ void __launch_bounds__(256) k_jsd_terms(const __grid_constant__ JsdAr
   const int rb1 = min(rb0 + rows_per_block, rows);
   const int64_t c0 = (int64_t)t * VT + tx * 8;
   const int64_t nvt = j.s.nvt;
-  const float beta = j.beta;
-  for (int r = rb0 + ty; r < rb1; r += 8) {
-    const float lqo = j.s.w.stm[(int64_t)r * nvt + t], lpo = j.t.w.stm[(int64_t)r * nvt + t];
-    const float qm = expf(lqo), pm = expf(lpo);
-    float es[8], et[8];
-    Load8<T>::run((const T*)j.s.w.slab + (int64_t)r * j.s.Vp + c0, es);
-    Load8<T>::run((const T*)j.t.w.slab + (int64_t)r * j.t.Vp + c0, et);
-    float term = 0.0f, qg = 0.0f;
+  const float beta = j.beta, omb = 1.0f - beta;
+  for (int r = rb0 + ty; r < rb1; r += 8 * RU) {
+    typename Load8<T>::Raw rs[RU], rt[RU];
+    float lqo[RU], lpo[RU];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (c0 + k >= j.s.V) continue;
-      const Elem e = elem(es[k], et[k], lqo, lpo, qm, pm);
-      if (beta == 0.0f) {
-        term += e.P * (e.lP - e.lQ);
-      } else if (beta == 1.0f) {
-        const float x = e.Q * (e.lQ - e.lP);
-        term += x;
-        qg += x;
-      } else {
-        const float Mv = beta * e.P + (1.0f - beta) * e.Q;
-        const float lM = clamped_log(Mv);
-        const float qpart = e.Q * (e.lQ - lM);
-        term += beta * e.P * (e.lP - lM) + (1.0f - beta) * qpart;
-        qg += (1.0f - beta) * qpart;
+    for (int u = 0; u < RU; ++u) {
+      // rows past the block's end re-read the block's first row (always valid); their
+      // sums are discarded
+      const int rr = r + 8 * u < rb1 ? r + 8 * u : r;
+      lqo[u] = j.s.w.stm[(int64_t)rr * nvt + t];
+      lpo[u] = j.t.w.stm[(int64_t)rr * nvt + t];
+      rs[u] = Load8<T>::load((const T*)j.s.w.slab + (int64_t)rr * j.s.Vp + c0);
+      rt[u] = Load8<T>::load((const T*)j.t.w.slab + (int64_t)rr * j.t.Vp + c0);
+    }
+    float term[RU], qg[RU];
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      float es[8], et[8];
+      Load8<T>::cvt(rs[u], es);
+      Load8<T>::cvt(rt[u], et);
+      const float qm = expf(lqo[u]), pm = expf(lpo[u]);
+      const float lq2 = lqo[u] * LOG2E, lp2 = lpo[u] * LOG2E;
+      float tm = 0.0f, g = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float Q = es[k] * qm, P = et[k] * pm;
+        const float lQ = lg2_clamped(es[k]) + lq2, lP = lg2_clamped(et[k]) + lp2;
+        if (beta == 0.0f) {
+          tm = fmaf(P, lP - lQ, tm);
+        } else if (beta == 1.0f) {
+          const float x = Q * (lQ - lP);
+          tm += x;
+          g += x;
+        } else {
+          const float lM = lg2_clamped(fmaf(beta, P, omb * Q));
+          const float qpart = omb * Q * (lQ - lM);
+          tm = fmaf(beta * P, lP - lM, tm + qpart);
+          g += qpart;
+        }
       }
+      term[u] = tm * LN2;
+      qg[u] = g * LN2;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      term += __shfl_xor_sync(0xffffffffu, term, o);
-      qg += __shfl_xor_sync(0xffffffffu, qg, o);
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+        term[u] += __shfl_xor_sync(0xffffffffu, term[u], o);
+        qg[u] += __shfl_xor_sync(0xffffffffu, qg[u], o);
+      }
     }
     if (tx == 0) {
-      j.s.w.sts[(int64_t)r * nvt + t] = term;
-      j.t.w.sts[(int64_t)r * nvt + t] = qg;
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+        const int rr = r + 8 * u;
+        if (rr < rb1) {
+          j.s.w.sts[(int64_t)rr * nvt + t] = term[u];
+          j.t.w.sts[(int64_t)rr * nvt + t] = qg[u];
+        }
+      }
     }
   }
 }
@@ -303,7 +334,8 @@ __global__ void __launch_bounds__(256) k_jsd_rowsum(const __grid_constant__ JsdA
 }
 
 // dS = a_i / T * dloss_i/dz_s written over the student slab (in place); rows past the chunk
-// end up to the next multiple of 64 are zeroed (the dW GEMM reduces over them).
+// end up to the next multiple of 64 are zeroed (the dW GEMM reduces over them). RU rows per
+// warp iteration, as in k_jsd_terms; pad columns stay zero (Q = P = 0 there).
 template <typename T>
 __global__ void __launch_bounds__(256) k_jsd_grad(const __grid_constant__ JsdArgs j, int chunk,
                                                   int rows_per_block) {
@@ -316,38 +348,51 @@ __global__ void __launch_bounds__(256) k_jsd_grad(const __grid_constant__ JsdArg
   const int rb1 = min(rb0 + rows_per_block, rlim);
   const int64_t c0 = (int64_t)t * VT + tx * 8;
   const int64_t nvt = j.s.nvt;
-  const float beta = j.beta;
-  for (int r = rb0 + ty; r < rb1; r += 8) {
-    T* ps = (T*)j.s.w.slab + (int64_t)r * j.s.Vp + c0;
-    float out[8];
-    if (r < rows) {
-      const float lqo = j.s.w.stm[(int64_t)r * nvt + t], lpo = j.t.w.stm[(int64_t)r * nvt + t];
-      const float qm = expf(lqo), pm = expf(lpo);
-      const float f = j.s.w.arow[r] * j.inv_T;
-      const float S = j.srow[r];
+  const float beta = j.beta, omb = 1.0f - beta;
+  // dz in base-2 logs: (1 - beta) (lQ - lM) = (1 - beta) ln2 (lQ2 - lM2)
+  const float cg = (beta == 1.0f ? 1.0f : omb) * LN2;
+  for (int r = rb0 + ty; r < rb1; r += 8 * RU) {
+    typename Load8<T>::Raw rs[RU], rt[RU];
+    float lqo[RU], lpo[RU], f[RU], S[RU];
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      // rows in [rows, rlim) are written as exact zeros (below) and read the chunk's first
+      // row instead; rows at or past rb1 are skipped
+      const int rr = r + 8 * u < rows ? r + 8 * u : 0;
+      lqo[u] = j.s.w.stm[(int64_t)rr * nvt + t];
+      lpo[u] = j.t.w.stm[(int64_t)rr * nvt + t];
+      f[u] = r + 8 * u < rows ? j.s.w.arow[rr] * j.inv_T : 0.0f;
+      S[u] = j.srow[rr];
+      rs[u] = Load8<T>::load((const T*)j.s.w.slab + (int64_t)rr * j.s.Vp + c0);
+      rt[u] = Load8<T>::load((const T*)j.t.w.slab + (int64_t)rr * j.t.Vp + c0);
+    }
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      const int rr = r + 8 * u;
+      if (rr >= rb1) continue;
+      const bool live = rr < rows;
       float es[8], et[8];
-      Load8<T>::run(ps, es);
-      Load8<T>::run((const T*)j.t.w.slab + (int64_t)r * j.t.Vp + c0, et);
+      Load8<T>::cvt(rs[u], es);
+      Load8<T>::cvt(rt[u], et);
+      const float qm = expf(lqo[u]), pm = expf(lpo[u]);
+      const float lq2 = lqo[u] * LOG2E, lp2 = lpo[u] * LOG2E;
+      float out[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const Elem e = elem(es[k], et[k], lqo, lpo, qm, pm);
+        const float Q = es[k] * qm, P = et[k] * pm;
         float dz;
         if (beta == 0.0f) {
-          dz = e.Q - e.P;
-        } else if (beta == 1.0f) {
-          dz = e.Q * ((e.lQ - e.lP) - S);
+          dz = Q - P;
         } else {
-          const float Mv = beta * e.P + (1.0f - beta) * e.Q;
-          const float lM = clamped_log(Mv);
-          dz = e.Q * ((1.0f - beta) * (e.lQ - lM) - S);
+          const float lQ = lg2_clamped(es[k]) + lq2;
+          const float lR = beta == 1.0f ? lg2_clamped(et[k]) + lp2
+                                        : lg2_clamped(fmaf(beta, P, omb * Q));
+          dz = Q * fmaf(cg, lQ - lR, -S[u]);
         }
-        out[k] = (c0 + k < j.s.V) ? f * dz : 0.0f;
+        out[k] = live ? f[u] * dz : 0.0f;
       }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) out[k] = 0.0f;
+      Load8<T>::store((T*)j.s.w.slab + (int64_t)rr * j.s.Vp + c0, out);
     }
-    Load8<T>::store(ps, out);
   }
 }
 
