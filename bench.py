@@ -176,6 +176,28 @@ def oracle_sample_rate(sp, inp, seconds, rows_per_call=32, rng_seed=99):
     return rate_lab * sp["BT"] / max(lab.size, 1), done, spent
 
 
+def jsd_oracle_sample_rate(sp, inp, seconds, rows_per_call=16, rng_seed=7):
+    """Time the float64 JSD oracle (as it stands) on seeded samples of labelled rows of the
+    distillation workload until about `seconds` of CPU work; returns (BT-tokens per second,
+    rows, seconds), scaled by BT / n_labelled as for the cross-entropy op."""
+    from oracle import jsd_oracle as jo
+    lab_all = inp["labels"].numpy()
+    lab = np.nonzero(lab_all != I.IGNORE_INDEX)[0]
+    Ws, Wt = I.to_numpy_exact(inp["Ws"]), I.to_numpy_exact(inp["Wt"])
+    rng = np.random.default_rng(rng_seed)
+    done, spent = 0, 0.0
+    while spent < seconds and done < lab.size:
+        rows = np.sort(rng.choice(lab, size=min(rows_per_call, lab.size), replace=False))
+        idx = torch.from_numpy(rows)
+        xs, xt = I.to_numpy_exact(inp["Xs"][idx]), I.to_numpy_exact(inp["Xt"][idx])
+        t0 = time.perf_counter()
+        jo.jsd_oracle(xs, Ws, xt, Wt, lab_all[rows], beta=sp["beta"], temperature=sp["temperature"],
+                      reduction=sp["reduction"], want_dX=True, want_dW=sp["want_dW"])
+        spent += time.perf_counter() - t0
+        done += rows.size
+    return done / spent * sp["BT"] / max(lab.size, 1), done, spent
+
+
 def cpu_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -445,30 +467,22 @@ def run_jsd(args):
                        "teacher head (distill)", "BT": BT, "Hs": Hs, "Ht": Ht, "V": V,
            "input_dtype": sp["dtype"], "beta": sp["beta"], "temperature": sp["temperature"],
            "reduction": sp["reduction"], "n_labelled": n_lab}
+    metric = "fused linear JSD fwd+bwd tokens/s"
     if args.impl == "reference":
         if rank != 0:
             return
-        from oracle import jsd_oracle as jo
-        rng = np.random.default_rng(7)
-        f = I.to_numpy_exact
-        Ws, Wt = f(inp["Ws"]), f(inp["Wt"])
-        done, spent = 0, 0.0
-        budget = args.ref_seconds / max(args.steps + args.warmup, 1) * max(args.steps, 1)
-        while spent < budget:
-            rows = np.sort(rng.choice(BT, size=16, replace=False))
-            idx = torch.from_numpy(rows)
-            t0 = time.perf_counter()
-            jo.jsd_oracle(f(inp["Xs"][idx]), Ws, f(inp["Xt"][idx]), Wt, inp["labels"].numpy()[rows],
-                          beta=sp["beta"], temperature=sp["temperature"])
-            spent += time.perf_counter() - t0
-            done += rows.size
-        value = done / spent
-        print(json.dumps({"impl": "reference", "metric": "fused linear JSD fwd+bwd tokens/s", "value": value,
+        per_step = max(min(2.0, args.ref_seconds), args.ref_seconds / max(args.steps + args.warmup, 1))
+        jsd_oracle_sample_rate(sp, inp, per_step * args.warmup)
+        value, done, spent = jsd_oracle_sample_rate(sp, inp, per_step * args.steps)
+        print(json.dumps({"impl": "reference", "op": "fused_linear_jsd", "metric": metric, "value": value,
                           "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                           "ms_per_step": BT / value * 1000.0, "higher_is_better": True, "scaling": "weak",
-                          "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.Generator)",
+                          "config": cfg,
                           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(),
-                                           "kind": "oracle", "sample": f"{done} seeded rows, {spent:.1f} s"},
+                                           "kind": "oracle",
+                                           "sample": f"{done} seeded labelled rows, {spent:.1f} s of float64 "
+                                                     f"oracle work (both heads' logits, loss, dX, dW)"},
                           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}), flush=True)
         return
@@ -520,13 +534,45 @@ def run_jsd(args):
     clocks = clk.stop()
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
     stages = prof.read()
+
+    # end to end through the public API: both heads' token rows and the labels copied in
+    # from pinned host memory, the loss read back, every step (head weights stay resident)
+    e2e = None
+    if not args.no_e2e:
+        hx = {k: inp[k].pin_memory() for k in ("Xs", "Xt", "labels")}
+        dx = {k: torch.empty_like(d[k]) for k in hx}
+        lh = torch.empty(1, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            for k in hx:
+                dx[k].copy_(hx[k], non_blocking=True)
+            flce.fused_linear_jsd(dx["Xs"], d["Ws"], dx["Xt"], d["Wt"], dx["labels"], beta=sp["beta"],
+                                  temperature=sp["temperature"], dW=dW, workspace=ws, outputs=outs,
+                                  check=False)
+            lh.copy_(outs["loss"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = max_over_ranks(f0.elapsed_time(f1) / args.steps, dist, dev)
+        e2e = {"value": BT * world / (ms_e2e / 1000.0), "unit": UNIT, "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hx.values())),
+               "d2h_bytes_per_step": 4}
     peaks, src = load_peaks()
     tflops = flops / (ms / 1000.0) / 1e12
     dom = max(("fwd", "dx", "dw"), key=lambda k: stages[k][0])
     dom_flops = 2.0 * n_lab * V * ((Hs + Ht) if dom == "fwd" else Hs)
     achieved = dom_flops / (stages[dom][0] / args.steps / 1000.0) / 1e12
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    line = {"op": "fused_linear_jsd", "metric": "fused linear JSD fwd+bwd tokens/s",
+    line = {"op": "fused_linear_jsd", "metric": metric,
             "value": BT * world / (ms / 1000.0), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": sp["dtype"], "data": "synthetic (seeded torch.Generator)",
@@ -539,7 +585,12 @@ def run_jsd(args):
                          "peak_kind": f"bf16 sustained ({src})", "traffic": None},
             "stages": {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                        for k, v in stages.items() if v[1] > 0},
-            "gpu_launches": int(sum(v[1] for v in stages.values())), "clocks": clocks, "e2e": None}
+            "gpu_launches": int(sum(v[1] for v in stages.values())), "clocks": clocks, "e2e": e2e}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows_done, secs = jsd_oracle_sample_rate(sp, inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                                "sample": f"{rows_done} seeded labelled rows, {secs:.1f} s of float64 oracle "
+                                          f"work (both heads' logits, loss, dX, dW)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:

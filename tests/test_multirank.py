@@ -34,7 +34,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_gloo_world_size_2():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         assert dict(out) == {0: 3.5, 1: 3.5}
