@@ -320,9 +320,9 @@ def run_ours(args):
     dbias = torch.zeros(V, dtype=torch.float32, device=dev) if (sp["want_dW"] and bias is not None) else None
     prof = flce.Profiler()
 
-    def step(Xd=X, tgd=tg, profiler=None):
+    def step(Xd=X, tgd=tg, god=go, profiler=None):
         flce.fwd_bwd(Xd, W, tgd, bias, reduction=sp["reduction"], z_loss_scale=sp.get("z", 0.0),
-                     grad_out=go, want_dX=True, want_dW=sp["want_dW"], dW=dW, dbias=dbias,
+                     grad_out=god, want_dX=True, want_dW=sp["want_dW"], dW=dW, dbias=dbias,
                      workspace=ws, outputs=outs, check=False, profiler=profiler)
 
     stream = torch.cuda.current_stream(dev)
@@ -356,42 +356,44 @@ def run_ours(args):
     ms_step = ms_total / args.steps
     value = BT * world / (ms_step / 1000.0)
 
-    # ---- end to end through the public API with pinned host inputs / outputs
+    # ---- end to end through the public API with pinned host inputs / outputs: every step
+    # copies its token rows, targets (and per-token gradient) in from pinned host memory and
+    # reads the loss back; the copy of step k+1 overlaps step k on a copy stream
+    # (DoubleBufferedInputs), as a training loop feeding the op would run
     e2e = None
     if not args.no_e2e:
-        Xh = inp["X"].pin_memory()
-        th = inp["targets"].pin_memory()
-        gh = inp["grad_out"].pin_memory() if inp["grad_out"] is not None else None
+        from linear_cross_entropy_logits_gb300.feeder import DoubleBufferedInputs
+        host = {"X": inp["X"].pin_memory(), "t": inp["targets"].pin_memory()}
+        if inp["grad_out"] is not None:
+            host["g"] = inp["grad_out"].pin_memory()
         lh = torch.empty(nl, dtype=torch.float32).pin_memory()
-        Xd = torch.empty_like(X)
-        tgd = torch.empty_like(tg)
+        feed = DoubleBufferedInputs(host, dev)
 
-        def e2e_step():
-            Xd.copy_(Xh, non_blocking=True)
-            tgd.copy_(th, non_blocking=True)
-            if gh is not None:
-                go.copy_(gh, non_blocking=True)
-            step(Xd, tgd)
-            lh.copy_(outs["loss"], non_blocking=True)
+        def e2e_run(n, start=None):
+            slot = feed.stage(host, after=start)
+            for k in range(n):
+                nxt = feed.stage(host) if k + 1 < n else None
+                dv = feed.acquire(slot, stream)
+                step(dv["X"], dv["t"], dv.get("g"))
+                feed.release(slot, stream)
+                lh.copy_(outs["loss"], non_blocking=True)
+                slot = nxt
 
-        for _ in range(2):
-            e2e_step()
+        e2e_run(2)
         torch.cuda.synchronize(dev)
         if dist:
             dist.barrier()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        e2e_run(args.steps, start=f0)
         f1.record(stream)
         torch.cuda.synchronize(dev)
         ms_e2e = f0.elapsed_time(f1) / args.steps
         ms_e2e = max_over_ranks(ms_e2e, dist, dev)
-        h2d = Xh.numel() * Xh.element_size() + th.numel() * th.element_size() + \
-            (gh.numel() * gh.element_size() if gh is not None else 0)
         e2e = {"value": BT * world / (ms_e2e / 1000.0), "unit": UNIT, "ms_per_step": ms_e2e,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(lh.numel() * 4)}
+               "h2d_bytes_per_step": int(feed.h2d_bytes), "d2h_bytes_per_step": int(lh.numel() * 4),
+               "copies": "H2D of step k+1 on a copy stream overlapping step k (double-buffered)"}
 
     # ---- roofline of the dominant kernel (per-stage CUDA events on the launching stream)
     peaks, peak_src = load_peaks()
@@ -539,33 +541,36 @@ def run_jsd(args):
     # from pinned host memory, the loss read back, every step (head weights stay resident)
     e2e = None
     if not args.no_e2e:
-        hx = {k: inp[k].pin_memory() for k in ("Xs", "Xt", "labels")}
-        dx = {k: torch.empty_like(d[k]) for k in hx}
+        from linear_cross_entropy_logits_gb300.feeder import DoubleBufferedInputs
+        host = {k: inp[k].pin_memory() for k in ("Xs", "Xt", "labels")}
         lh = torch.empty(1, dtype=torch.float32).pin_memory()
+        feed = DoubleBufferedInputs(host, dev)
 
-        def e2e_step():
-            for k in hx:
-                dx[k].copy_(hx[k], non_blocking=True)
-            flce.fused_linear_jsd(dx["Xs"], d["Ws"], dx["Xt"], d["Wt"], dx["labels"], beta=sp["beta"],
-                                  temperature=sp["temperature"], dW=dW, workspace=ws, outputs=outs,
-                                  check=False)
-            lh.copy_(outs["loss"], non_blocking=True)
+        def e2e_run(n, start=None):
+            slot = feed.stage(host, after=start)
+            for k in range(n):
+                nxt = feed.stage(host) if k + 1 < n else None
+                dv = feed.acquire(slot, stream)
+                flce.fused_linear_jsd(dv["Xs"], d["Ws"], dv["Xt"], d["Wt"], dv["labels"], beta=sp["beta"],
+                                      temperature=sp["temperature"], dW=dW, workspace=ws, outputs=outs,
+                                      check=False)
+                feed.release(slot, stream)
+                lh.copy_(outs["loss"], non_blocking=True)
+                slot = nxt
 
-        for _ in range(2):
-            e2e_step()
+        e2e_run(2)
         torch.cuda.synchronize(dev)
         if dist:
             dist.barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        e2e_run(args.steps, start=f0)
         f1.record(stream)
         torch.cuda.synchronize(dev)
         ms_e2e = max_over_ranks(f0.elapsed_time(f1) / args.steps, dist, dev)
         e2e = {"value": BT * world / (ms_e2e / 1000.0), "unit": UNIT, "ms_per_step": ms_e2e,
-               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hx.values())),
-               "d2h_bytes_per_step": 4}
+               "h2d_bytes_per_step": int(feed.h2d_bytes), "d2h_bytes_per_step": 4,
+               "copies": "H2D of step k+1 on a copy stream overlapping step k (double-buffered)"}
     peaks, src = load_peaks()
     tflops = flops / (ms / 1000.0) / 1e12
     dom = max(("fwd", "dx", "dw"), key=lambda k: stages[k][0])
