@@ -83,6 +83,9 @@ typedef enum flce_dtype { FLCE_F32 = 0, FLCE_BF16 = 1, FLCE_F16 = 2 } flce_dtype
 /* flce_args.flags */
 #define FLCE_FLAG_FORCE_SIMT 0x1u /* run the three GEMMs on SIMT fp32-FMA kernels even for
                                      bf16/f16 inputs (fp32 inputs always use them)       */
+#define FLCE_FLAG_NO_ROW_REF 0x2u /* always normalise the gradient slab per vocabulary tile
+                                     (a full pass over it) instead of the default one-scale-
+                                     per-row form of bf16 tensor-core calls without dbias   */
 #define FLCE_FLAG_DEBUG_STALL 0x100u /* testing only: the tensor-core forward GEMM leaves
                                      one pipeline stage unfilled so that its bounded waits
                                      run out; the call must then report FLCE_ERR_TIMEOUT */

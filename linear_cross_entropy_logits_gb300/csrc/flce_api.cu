@@ -53,6 +53,7 @@ bool plan_layout(int64_t BT, int64_t H, int64_t V, int dt, int64_t R, Plan* p) {
   q.off_tgt = take(4 * (size_t)R);
   q.off_lse = take(4 * (size_t)R);
   q.off_arow = take(4 * (size_t)R);
+  q.off_rsc = take(4 * (size_t)R);
   q.off_slab = take((size_t)R * q.Vp * q.esz);
   // fp32 dX accumulator of the tensor-core path (16-bit inputs only)
   q.off_dxacc = take(q.esz == 2 ? (size_t)R * H * 4 : 0);
@@ -93,6 +94,7 @@ Work make_work(const Plan& p, void* ws, int32_t* user_status) {
   w.tgt = (float*)(b + p.off_tgt);
   w.lse = (float*)(b + p.off_lse);
   w.arow = (float*)(b + p.off_arow);
+  w.rsc = (float*)(b + p.off_rsc);
   w.slab = b + p.off_slab;
   w.dxacc = (float*)(b + p.off_dxacc);
   w.status = user_status ? (int*)user_status : &w.ctrl->status;
@@ -257,18 +259,38 @@ extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
   flce_profile* prof = x->profile;
   FLCE_TRY(cudaMemsetAsync(a.w.status, 0, sizeof(int), s));
   FLCE_TRY(staged(prof, FLCE_STAGE_PROLOGUE, 2, s, [&] { return launch_prologue(a, s); }));
+  // Row-reference mode (bf16 tensor-core calls with gradients and no dbias): the forward
+  // stores exp(s), finalize turns it into G up to one scale per row, and the gradient pass
+  // over the slab is skipped. A chunk with a row outside the window is redone per tile by
+  // three launches that do nothing otherwise (run_if = the chunk's flag).
+  const bool ref = tc && grads && a.dt == FLCE_BF16 && a.dbias == nullptr &&
+                   !(x->flags & FLCE_FLAG_NO_ROW_REF);
+  CallArgs ar = a;
+  ar.ref_mode = ref ? 1 : 0;
+  CallArgs afb = a;
+  afb.run_if = &a.w.ctrl->fb;
   for (int k = 0; k < (int)p.kmax; ++k) {
     FLCE_TRY(staged(prof, FLCE_STAGE_GATHER, 1, s, [&] { return launch_gather(a, k, s); }));
     FLCE_TRY(staged(prof, FLCE_STAGE_FWD, 1, s,
-                    [&] { return tc ? launch_fwd_tc(a, k, s) : launch_fwd_simt(a, k, s); }));
-    FLCE_TRY(staged(prof, FLCE_STAGE_FINALIZE, 1, s, [&] { return launch_finalize(a, k, s); }));
-    if (grads) FLCE_TRY(staged(prof, FLCE_STAGE_GPASS, 1, s, [&] { return launch_gpass(a, k, s); }));
+                    [&] { return tc ? launch_fwd_tc(ar, k, s) : launch_fwd_simt(a, k, s); }));
+    FLCE_TRY(staged(prof, FLCE_STAGE_FINALIZE, 1, s, [&] { return launch_finalize(ar, k, s); }));
+    if (ref) {
+      FLCE_TRY(staged(prof, FLCE_STAGE_GPASS, a.want_dW ? 4 : 3, s, [&] {
+        cudaError_t e = a.want_dW ? launch_scale_x(ar, k, s) : cudaSuccess;
+        if (e == cudaSuccess) e = launch_fwd_tc(afb, k, s);
+        if (e == cudaSuccess) e = launch_finalize(afb, k, s);
+        if (e == cudaSuccess) e = launch_gpass(afb, k, s);
+        return e;
+      }));
+    } else if (grads) {
+      FLCE_TRY(staged(prof, FLCE_STAGE_GPASS, 1, s, [&] { return launch_gpass(a, k, s); }));
+    }
     if (a.want_dX) {
       if (tc) {
         FLCE_TRY(staged(prof, FLCE_STAGE_DX, 2, s, [&] {
           cudaError_t e = cudaMemsetAsync(a.w.dxacc, 0, (size_t)a.R * a.H * 4, s);
           if (e != cudaSuccess) return e;
-          e = launch_dx_tc(a, k, s);
+          e = launch_dx_tc(ar, k, s);
           if (e != cudaSuccess) return e;
           return launch_dx_store(a, k, s);
         }));

@@ -33,7 +33,8 @@ struct Ctrl {
   int status;     // status word used when the caller passes none
   float cbar;     // uniform gradient factor: g/n_lab (mean), g (sum), 1 (none)
   float inv_n;    // 1/n_lab for mean (0 when n_lab == 0), 1 for sum
-  int pad[2];
+  int fb;         // row-reference mode: 1 when a row of the current chunk left the window
+  int pad;
 };
 
 // Workspace layout for one call; every region is 256-byte aligned.
@@ -46,7 +47,7 @@ struct Plan {
   int64_t R;     // max rows per chunk (multiple of 128)
   int64_t kmax;  // chunks the host enqueues = cdiv(BT, R)
   size_t off_ctrl, off_idx, off_rloss, off_rz, off_racc;
-  size_t off_xc, off_stm, off_sts, off_sti, off_tgt, off_lse, off_arow, off_slab, off_dxacc;
+  size_t off_xc, off_stm, off_sts, off_sti, off_tgt, off_lse, off_arow, off_rsc, off_slab, off_dxacc;
   size_t total;
 };
 
@@ -68,7 +69,9 @@ struct Work {
   float* tgt;      // [R] target logit
   float* lse;      // [R] row logsumexp
   float* arow;     // [R] per-row factor a_i (g_i for none, 1 otherwise)
-  void* slab;      // [R, Vp] exp(s - tile max), then G, in the input dtype
+  float* rsc;      // [R] row-reference mode: G row scale a_i (1 + 2 z lse_i) exp(-lse_i)
+  void* slab;      // [R, Vp] exp(s - tile max) (row-reference mode: exp(s)), then G, in the
+                   // input dtype
   float* dxacc;    // [R, H] fp32 dX accumulator of the tensor-core path (stream-K halves)
   int* status;     // device status word
 };
@@ -102,7 +105,20 @@ struct CallArgs {
   uint32_t flags;
   float logit_scale;     // logits = (X W^T) * logit_scale + bias (1/T for distillation)
   int labels_are_masks;  // 1: any target != ignore_index marks a row (no range check)
+  // Row-reference mode (bf16 tensor-core path): the forward stores exp(s) instead of
+  // exp(s - tile max), so that G = rsc_i * slab' with one scale per row (slab' = the slab
+  // with the target element patched by finalize); dX applies rsc in its epilogue and dW
+  // reads Xc pre-scaled by rsc. No gradient pass over the slab.
+  int ref_mode;
+  const int* run_if;     // when set, the kernel does nothing unless *run_if != 0
 };
+
+// Row-reference window: the row max m must satisfy |m| <= REF_WINDOW so that exp(s) and
+// its sums stay in the normal fp32/bf16 range, and the row scale must lie in
+// [exp(-REF_SCALE_LOG), exp(REF_SCALE_LOG)] (or be 0) so that the pre-scaled Xc rows stay
+// normal. A row outside sets Ctrl::fb and the chunk is redone with per-tile maxima.
+constexpr float REF_WINDOW = 60.0f;
+constexpr float REF_SCALE_LOG = 70.0f;
 
 // ---- launchers (flce_kernels.cu) ----
 cudaError_t launch_prologue(const CallArgs& a, cudaStream_t s);          // compact + ignored rows
@@ -110,6 +126,7 @@ cudaError_t launch_gather(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_fwd_simt(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_finalize(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_gpass(const CallArgs& a, int chunk, cudaStream_t s);
+cudaError_t launch_scale_x(const CallArgs& a, int chunk, cudaStream_t s);  // Xc rows *= rsc
 cudaError_t launch_dx_simt(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_dw_simt(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_epilogue(const CallArgs& a, cudaStream_t s);          // reductions

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(256) k_ignored(const __grid_constant__ CallArg
 __global__ void __launch_bounds__(256) k_gather(const __grid_constant__ CallArgs a, int chunk) {
   int row0, rows;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.w.ctrl->fb = 0;  // row-reference window flag
   const int lim = (int)rup64(rows, CHUNK_ALIGN);
   const int esz = a.dt == FLCE_F32 ? 4 : 2;
   const int64_t src_bytes = a.H * esz, dst_bytes = a.Hp * esz;
@@ -166,7 +167,16 @@ __device__ __forceinline__ void lse_combine(float& M, float& S, int& am, float M
   S = Sn;
 }
 
+// Row-reference mode: the tile sums are all relative to the same reference (0), so they
+// add; the maxima only decide the argmax and the window.
+__device__ __forceinline__ void ref_combine(float& M, float& S, int& am, float M2, float S2, int a2) {
+  am = M > M2 ? am : (M2 > M ? a2 : min(am, a2));
+  M = fmaxf(M, M2);
+  S += S2;
+}
+
 __global__ void __launch_bounds__(256) k_finalize(const __grid_constant__ CallArgs a, int chunk) {
+  if (a.run_if != nullptr && *a.run_if == 0) return;
   int row0, rows;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
   const int lane = threadIdx.x & 31;
@@ -179,23 +189,52 @@ __global__ void __launch_bounds__(256) k_finalize(const __grid_constant__ CallAr
 
   float M = -INFINITY, S = 0.0f;
   int am = 0x7fffffff;
-  for (int t = lane; t < nvt; t += 32) lse_combine(M, S, am, stm[t], sts[t], sti[t]);
+  if (a.ref_mode) {
+    for (int t = lane; t < nvt; t += 32) ref_combine(M, S, am, stm[t], sts[t], sti[t]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
-    const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
-    const int a2 = __shfl_xor_sync(0xffffffffu, am, o);
-    lse_combine(M, S, am, M2, S2, a2);
+    for (int o = 16; o > 0; o >>= 1) {
+      const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
+      const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+      const int a2 = __shfl_xor_sync(0xffffffffu, am, o);
+      ref_combine(M, S, am, M2, S2, a2);
+    }
+  } else {
+    for (int t = lane; t < nvt; t += 32) lse_combine(M, S, am, stm[t], sts[t], sti[t]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
+      const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+      const int a2 = __shfl_xor_sync(0xffffffffu, am, o);
+      lse_combine(M, S, am, M2, S2, a2);
+    }
   }
-  const float lse = M + logf(S);
+  const float lse = a.ref_mode ? logf(S) : M + logf(S);
 
   const int row = a.w.idx[row0 + r];
   const int64_t tg = a.targets[row];
   float ar = 1.0f;
   if (a.reduction == FLCE_NONE && a.grad_out != nullptr) ar = a.grad_out[row];
-  const float f = ar * (1.0f + 2.0f * a.z * lse);
-  for (int t = lane; t < nvt; t += 32) stm[t] = f * expf(stm[t] - lse);
-  if (lane != 0) return;
+  const float zf = 1.0f + 2.0f * a.z * lse;
+  if (a.ref_mode) {
+    // G_iv = rsc_i * slab'_iv with rsc_i = a_i (1 + 2 z lse_i) exp(-lse_i); the target
+    // element becomes exp(s_t) - exp(lse_i) / (1 + 2 z lse_i), so that rsc_i times it is
+    // a_i ((1 + 2 z lse_i) p_t - 1). Rows outside the window flag the chunk.
+    const float sc = ar * zf * expf(-lse);
+    const bool ok = fabsf(M) <= REF_WINDOW && S > 0.0f && isfinite(S) && fabsf(zf) >= 1e-3f &&
+                    (sc == 0.0f || fabsf(logf(fabsf(sc))) <= REF_SCALE_LOG);
+    if (lane != 0) return;
+    if (!ok) {
+      a.w.ctrl->fb = 1;
+    } else {
+      a.w.rsc[r] = sc;
+      ((__nv_bfloat16*)a.w.slab)[(int64_t)r * a.Vp + tg] =
+          __float2bfloat16_rn(expf(a.w.tgt[r]) - expf(lse) / zf);
+    }
+  } else {
+    const float f = ar * zf;
+    for (int t = lane; t < nvt; t += 32) stm[t] = f * expf(stm[t] - lse);
+    if (lane != 0) return;
+  }
   const float zl = a.z * lse * lse;
   const float loss = (lse - a.w.tgt[r]) + zl;
   const float accv = ((int64_t)am == tg) ? 1.0f : 0.0f;
@@ -273,6 +312,7 @@ template <> struct Vec8<float> {
 template <typename T>
 __global__ void __launch_bounds__(256) k_gpass(const __grid_constant__ CallArgs a, int chunk,
                                                int rows_per_block, int do_dbias) {
+  if (a.run_if != nullptr && *a.run_if == 0) return;
   int row0, rows;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
   const int t = blockIdx.x;
@@ -323,6 +363,25 @@ __global__ void __launch_bounds__(256) k_gpass(const __grid_constant__ CallArgs 
           db[v] = from_f<T>(to_f<T>(db[v]) + cb * s);
         }
       }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Row-reference mode: Xc rows *= rsc (bf16, in place) for the dW GEMM, unless the chunk
+// left the window (then Xc stays as gathered for the per-tile redo). One block per row.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_scale_x(const __grid_constant__ CallArgs a, int chunk) {
+  int row0, rows;
+  if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  if (a.w.ctrl->fb) return;
+  __nv_bfloat162* x = (__nv_bfloat162*)a.w.xc;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const float sc = a.w.rsc[r];
+    __nv_bfloat162* xr = x + (int64_t)r * (a.Hp / 2);
+    for (int64_t j = threadIdx.x; j < (a.H + 1) / 2; j += blockDim.x) {  // pad column is 0
+      const float2 v = __bfloat1622float2(xr[j]);
+      xr[j] = __floats2bfloat162_rn(v.x * sc, v.y * sc);
     }
   }
 }
@@ -603,6 +662,12 @@ cudaError_t launch_prologue(const CallArgs& a, cudaStream_t s) {
 cudaError_t launch_gather(const CallArgs& a, int chunk, cudaStream_t s) {
   const int64_t blocks = a.R < 4LL * num_sms() ? a.R : 4LL * num_sms();
   k_gather<<<(unsigned)blocks, 256, 0, s>>>(a, chunk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_x(const CallArgs& a, int chunk, cudaStream_t s) {
+  const int64_t blocks = a.R < 4096 ? a.R : 4096;
+  k_scale_x<<<(unsigned)blocks, 256, 0, s>>>(a, chunk);
   return cudaGetLastError();
 }
 

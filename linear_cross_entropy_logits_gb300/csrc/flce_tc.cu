@@ -406,7 +406,7 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
   // by one TMA bulk tensor store (whole lines; rows past the chunk hold values nothing
   // reads, rows past R are clipped by the TMA unit)
   float sum = 0.0f;
-  const float mxl = mx * LOG2E;
+  const float mxl = a.ref_mode ? 0.0f : mx * LOG2E;  // row-reference mode stores exp(s)
   uint8_t* row = nullptr;
 #pragma unroll 1
   for (int c2 = 0; c2 < BN / 64; ++c2) {
@@ -458,7 +458,7 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
 }
 
 // dst tile += cbar * acc through TMA reduce-add (dst = dW for DW, the fp32 dX accumulator
-// for DX). Each epilogue warp owns 32 rows (its TMEM lane quadrant) and stages 32 columns
+// for DX; in row-reference mode each dX row is also scaled by its rsc). Each epilogue warp owns 32 rows (its TMEM lane quadrant) and stages 32 columns
 // at a time (32 x 128 B, 128-byte swizzle: 16-byte chunk j of row r sits at chunk
 // j ^ (r % 8)), alternating two buffers; the TMA unit adds the box into dst in L2. A dW
 // element gets exactly one add per launch (one owning pair); a dX accumulator element at
@@ -466,10 +466,11 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
 // Boxes past the destination's extent are clipped by the TMA unit.
 __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtensorMap* tmC, uint8_t* stg,
                                                 int mrow, int n, int ylimit, uint32_t taddr, int q,
-                                                int lane, float cb, uint32_t& epi_it) {
+                                                int lane, float cb, const float* rsc, uint32_t& epi_it) {
   const int H = (int)a.H;
   const int y = mrow + q * 32;
   if (y >= ylimit) return;  // this warp's 32 rows lie past the destination (warp-uniform)
+  if (rsc != nullptr) cb *= rsc[y + lane];  // y + lane < ylimit = R (multiples of 32)
 #pragma unroll 1
   for (int cc = 0; cc < BN / 32; ++cc) {
     const int x = n * BN + cc * 32;
@@ -537,6 +538,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CallArgs a,
               const int chunk) {
   constexpr int STAGES = stages_of<MODE>();
+  if (a.run_if != nullptr && *a.run_if == 0) return;  // both CTAs of a pair read the same word
   int row0 = 0, rows = 0;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
   const TileSpace ts = tile_space<MODE>(a, rows);
@@ -687,6 +689,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------- epilogue warps 2..5 (both CTAs)
     const int q = warp & 3;
     const float cb = MODE == FWD ? 0.0f : a.w.ctrl->cbar;
+    const float* rsc = (MODE == DX && a.ref_mode && a.w.ctrl->fb == 0) ? a.w.rsc : nullptr;
     uint8_t* stg = epi_stage + (warp - 2) * 2 * EPI_BUF_BYTES;
     uint32_t epi_it = 0;
     int it = 0;
@@ -705,7 +708,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * BN);
       if (MODE == FWD) epilogue_fwd<T>(a, &tmC, stg, row0, rows, mrow, n, taddr, q, lane, epi_it);
       else if (MODE == DW && a.dW_dt != FLCE_F32) epilogue_dw_same_dtype<T>(a, mrow, n * BN, taddr, q, lane, cb);
-      else epilogue_reduce(a, &tmC, stg, mrow, n, MODE == DX ? (int)a.R : (int)a.V, taddr, q, lane, cb, epi_it);
+      else epilogue_reduce(a, &tmC, stg, mrow, n, MODE == DX ? (int)a.R : (int)a.V, taddr, q, lane, cb, rsc, epi_it);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

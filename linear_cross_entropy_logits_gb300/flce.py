@@ -21,6 +21,7 @@ NOALLOC_SCRATCH_BYTES = 128 << 20
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 FLAG_FORCE_SIMT = 0x1
+FLAG_NO_ROW_REF = 0x2
 FLAG_DEBUG_STALL = 0x100
 EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_fwd_bwd_noalloc",
             "flce_get_status",
