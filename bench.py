@@ -198,6 +198,15 @@ def jsd_oracle_sample_rate(sp, inp, seconds, rows_per_call=16, rng_seed=7):
     return done / spent * sp["BT"] / max(lab.size, 1), done, spent
 
 
+def step_percentiles(evs):
+    """Median, p20 and p80 of the per-step device times between consecutive events."""
+    t = sorted(a.elapsed_time(b) for a, b in zip(evs[:-1], evs[1:]))
+
+    def pct(q):
+        return float(np.percentile(np.asarray(t), q))
+    return {"p20": pct(20), "median": pct(50), "p80": pct(80), "steps": len(t)}
+
+
 def cpu_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -340,17 +349,21 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     prof.reset()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem0 = torch.cuda.memory_allocated(dev)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
         step(profiler=prof)
-    e1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
     clocks = clk.stop()
-    ms_total = e0.elapsed_time(e1)
+    ms_total = evs[0].elapsed_time(evs[-1])
+    per_step = step_percentiles(evs)
+    transient = {"workspace_bytes": ws_bytes,
+                 "allocated_in_timed_region_bytes": int(torch.cuda.max_memory_allocated(dev) - mem0)}
     stages = prof.read()
     ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / args.steps
@@ -429,6 +442,8 @@ def run_ours(args):
             "l2": f"no flush: W ({V * H * I.TORCH_DTYPES[sp['dtype']].itemsize / 1e9:.2f} GB) and the "
                   f"per-chunk slab exceed the 129 MB L2",
             "workspace_bytes": ws_bytes, "chunk_rows": R}),
+        "ms_per_step_percentiles": per_step,
+        "transient": transient,
         "tokens_per_s_labelled": n_lab * world / (ms_step / 1000.0),
         "tflops": tflops, "flops_per_step": flops,
         "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
@@ -525,16 +540,21 @@ def run_jsd(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     prof.reset()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem0 = torch.cuda.memory_allocated(dev)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
         step(prof)
-    e1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
     clocks = clk.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
+    ms = max_over_ranks(evs[0].elapsed_time(evs[-1]), dist, dev) / args.steps
+    per_step = step_percentiles(evs)
+    transient = {"workspace_bytes": ws_bytes,
+                 "allocated_in_timed_region_bytes": int(torch.cuda.max_memory_allocated(dev) - mem0)}
     stages = prof.read()
 
     # end to end through the public API: both heads' token rows and the labels copied in
@@ -583,6 +603,7 @@ def run_jsd(args):
             "vs_baseline": None, "dtype": sp["dtype"], "data": "synthetic (seeded torch.Generator)",
             "config": dict(cfg, workspace_bytes=ws_bytes, chunk_rows=None,
                            l2="no flush: the heads (0.5 + 1.05 GB) exceed the 129 MB L2"),
+            "ms_per_step_percentiles": per_step, "transient": transient,
             "tflops": tflops, "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
                                                      "sustained": tflops / peak, "source": src},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,

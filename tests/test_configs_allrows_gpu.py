@@ -1,0 +1,71 @@
+"""Forward outputs of every row at the workloads' full sizes, against the float64 oracle.
+
+The oracle's row-blocked forward (logits in float64 over the whole vocabulary, then the
+per-row lse, loss and argmax) runs on every labelled row of the Llama-3.2-1B,
+Llama-3.1-8B and frozen-head workloads, in the launch configuration the benchmark times
+(default workspace, gradients on; reduction "none" so that every per-token loss is
+returned). Every row is compared: lse and per-token loss within the bf16 tolerance (2e-3
+relative), the prediction bit exact outside the fp32 tie band, and the ignored-row outputs
+bit exact. The large-vocab workload (92 TFLOP of float64 forward) stays on sampled rows.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from linear_cross_entropy_logits_gb300 import build as B
+from linear_cross_entropy_logits_gb300 import flce
+from linear_cross_entropy_logits_gb300 import inputs as I
+from oracle import flce_oracle as orc
+from parity_util import TOL, pred_ok
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = [("llama1b", {}), ("llama8b", dict(labelled_fraction=1.0)), ("frozen_head", {})]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.build()
+    flce.load()
+
+
+@pytest.mark.parametrize("base,ov", CONFIGS, ids=[c[0] for c in CONFIGS])
+def test_every_row_forward(base, ov):
+    sp = I.spec(base, **ov)
+    inp = I.generate(sp, seed=0)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    BT, H, V = sp["BT"], sp["H"], sp["V"]
+    z = sp.get("z", 0.0)
+    dW = torch.zeros(V, H, dtype=torch.float32, device="cuda") if sp["want_dW"] else None
+    go = d["grad_out"] if d["grad_out"] is not None else torch.ones(BT, device="cuda")
+    out = flce.fwd_bwd(d["X"], d["W"], d["targets"], d["bias"], reduction="none", z_loss_scale=z,
+                       grad_out=go, want_dX=True, want_dW=sp["want_dW"], dW=dW)
+    assert out["status_code"] == flce.FLCE_OK
+    lse = out["lse"].cpu().numpy()
+    loss = out["loss"].cpu().numpy()
+    pred = out["pred"].cpu().numpy()
+    del out, dW
+
+    t = inp["targets"].numpy()
+    mask = t != I.IGNORE_INDEX
+    assert np.all(pred[~mask] == -1) and np.all(lse[~mask] == 0) and np.all(loss[~mask] == 0)
+    X = I.to_numpy_exact(inp["X"])
+    W64 = I.to_numpy_exact(inp["W"]).astype(np.float64)
+    b = I.to_numpy_exact(inp["bias"])
+    tol = TOL[sp["dtype"]]["loss"]
+    rows = np.nonzero(mask)[0]
+    worst_lse = worst_loss = 0.0
+    for k0 in range(0, rows.size, 1024):
+        r = rows[k0:k0 + 1024]
+        s = orc.logits_rows(X[r], W64, b)
+        o_lse, o_loss, _, o_pred, _, _ = orc.rows_forward(s, t[r], z)
+        del s
+        worst_lse = max(worst_lse, float(np.max(np.abs(lse[r] - o_lse) / np.abs(o_lse))))
+        worst_loss = max(worst_loss, float(np.max(np.abs(loss[r] - o_loss) / np.maximum(np.abs(o_loss), 1e-3))))
+        ok, where = pred_ok(pred[r], o_pred, X, W64, b, r, mask[r])
+        assert ok, f"argmax mismatch outside the tie band at row {where}"
+    assert worst_lse <= tol, f"lse rel err {worst_lse}"
+    assert worst_loss <= tol, f"per-token loss rel err {worst_loss}"
