@@ -55,8 +55,8 @@ bool plan_layout(int64_t BT, int64_t H, int64_t V, int dt, int64_t R, Plan* p) {
   q.off_arow = take(4 * (size_t)R);
   q.off_rsc = take(4 * (size_t)R);
   q.off_slab = take((size_t)R * q.Vp * q.esz);
-  // fp32 dX accumulator of the tensor-core path (16-bit inputs only)
-  q.off_dxacc = take(q.esz == 2 ? (size_t)R * H * 4 : 0);
+  // two fp32 dX accumulator buffers of the tensor-core path (16-bit inputs only)
+  q.off_dxacc = take(q.esz == 2 ? 2 * (size_t)R * H * 4 : 0);
   q.total = off;
   *p = q;
   return true;
@@ -288,7 +288,7 @@ extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
     if (a.want_dX) {
       if (tc) {
         FLCE_TRY(staged(prof, FLCE_STAGE_DX, 2, s, [&] {
-          cudaError_t e = cudaMemsetAsync(a.w.dxacc, 0, (size_t)a.R * a.H * 4, s);
+          cudaError_t e = cudaMemsetAsync(a.w.dxacc, 0, 2 * (size_t)a.R * a.H * 4, s);
           if (e != cudaSuccess) return e;
           e = launch_dx_tc(ar, k, s);
           if (e != cudaSuccess) return e;

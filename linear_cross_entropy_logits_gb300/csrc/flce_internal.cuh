@@ -72,7 +72,8 @@ struct Work {
   float* rsc;      // [R] row-reference mode: G row scale a_i (1 + 2 z lse_i) exp(-lse_i)
   void* slab;      // [R, Vp] exp(s - tile max) (row-reference mode: exp(s)), then G, in the
                    // input dtype
-  float* dxacc;    // [R, H] fp32 dX accumulator of the tensor-core path (stream-K halves)
+  float* dxacc;    // [2, R, H] fp32 dX accumulator buffers of the tensor-core path (K
+                   // splits 0-1 add into the first, 2-3 into the second)
   int* status;     // device status word
 };
 Work make_work(const Plan& p, void* ws, int32_t* user_status);

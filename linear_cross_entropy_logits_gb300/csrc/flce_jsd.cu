@@ -77,7 +77,7 @@ bool jsd_layout(int64_t BT, int64_t Hs, int64_t Ht, int64_t V, int dt, int64_t R
   q.off_srow = take(4 * (size_t)R);
   q.off_slab_s = take((size_t)R * q.Vp * q.esz);
   q.off_slab_t = take((size_t)R * q.Vp * q.esz);
-  q.off_dxacc = take(q.esz == 2 ? (size_t)R * Hs * 4 : 0);
+  q.off_dxacc = take(q.esz == 2 ? 2 * (size_t)R * Hs * 4 : 0);  // two fp32 buffers
   q.total = off;
   *p = q;
   return true;
@@ -572,7 +572,7 @@ extern "C" int32_t flce_fused_linear_jsd(const flce_jsd_args* x, void* stream) {
     if (s.want_dX) {
       if (tc) {
         JSD_TRY(staged(prof, FLCE_STAGE_DX, 2, st, [&] {
-          cudaError_t e = cudaMemsetAsync(s.w.dxacc, 0, (size_t)p.R * s.H * 4, st);
+          cudaError_t e = cudaMemsetAsync(s.w.dxacc, 0, 2 * (size_t)p.R * s.H * 4, st);
           if (e == cudaSuccess) e = launch_dx_tc(s, k, st);
           return e != cudaSuccess ? e : launch_dx_store(s, k, st);
         }));

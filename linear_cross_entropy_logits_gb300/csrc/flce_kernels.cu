@@ -628,10 +628,14 @@ __global__ void __launch_bounds__(256) k_dx_store(const __grid_constant__ CallAr
   const int64_t H = a.H;
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const float* src = a.w.dxacc + (int64_t)r * H;
+    const float* src2 = src + a.R * H;  // second accumulator buffer (K splits 2-3)
     T* dst = (T*)a.dX + (int64_t)a.w.idx[row0 + r] * H;
     for (int64_t j = (int64_t)threadIdx.x * 8; j < H; j += (int64_t)blockDim.x * 8) {
-      float f[8];
+      float f[8], g[8];
       Vec8<float>::load(src + j, f);
+      Vec8<float>::load(src2 + j, g);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f[k] += g[k];
       Vec8<T>::store(dst + j, f);
     }
   }

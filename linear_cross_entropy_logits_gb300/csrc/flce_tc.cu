@@ -47,32 +47,68 @@ namespace flce {
 namespace tc {
 
 constexpr int BM = 128;                            // rows of A per CTA (pair tile M = 256)
-constexpr int BN = 256;                            // pair tile N (each CTA holds BN/2 of B)
+constexpr int BN = 256;                            // N of one MMA (each CTA holds BN/2 of B)
 constexpr int BK = 64;
-// Pipeline depth: 6 stages of 32 KB (192 KB); DX and DW add 32 KB of epilogue staging.
-template <int MODE>
-constexpr int stages_of() {
-  return 6;
-}
-constexpr int MAX_STAGES = 6;
-constexpr int A_BYTES = BM * BK * 2;               // 16 KB
-constexpr int B_BYTES = (BN / 2) * BK * 2;         // 16 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB per CTA
-constexpr int BOX_BYTES = 64 * 64 * 2;             // one 64x64 MN-major TMA box (8 KB)
-constexpr int NUM_THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tfull[2], tempty[2], drain
-// Epilogue staging: per epilogue warp, two 32-row x 128-byte buffers that feed TMA bulk
-// tensor stores (FWD: the exp slab) or reduce-adds (DX/DW: the L2 performs dst += tile;
-// no register read-modify-write).
-constexpr int EPI_BUF_BYTES = 32 * 128;
-constexpr int EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;   // 32 KB
-template <int MODE>
-constexpr int smem_bytes() {
-  return stages_of<MODE>() * STAGE_BYTES + EPI_BYTES + 1024 + 512;
-}
 
 enum Mode { FWD = 0, DX = 1, DW = 2 };
+
+// Pair tile width in 256-column sub-tiles. NB = 2: a 256 x 512 pair tile whose two MMAs
+// per K step share the A stage (37% more FLOPs per operand byte than 256 x 256; the GEMMs
+// are bound by the operand feed), with one 512-column TMEM accumulator and eight epilogue
+// warps (one per TMEM lane quadrant and sub-tile). NB = 1: 256 x 256 tiles with two
+// 256-column accumulators, so that a tile's epilogue overlaps the next tile's mainloop.
+#ifndef FLCE_TC_NB_FWD
+#define FLCE_TC_NB_FWD 1
+#endif
+#ifndef FLCE_TC_NB_DX
+#define FLCE_TC_NB_DX 2
+#endif
+#ifndef FLCE_TC_NB_DW
+#define FLCE_TC_NB_DW 2
+#endif
+template <int MODE>
+__host__ __device__ constexpr int nb_of() {
+  return MODE == FWD ? FLCE_TC_NB_FWD : (MODE == DX ? FLCE_TC_NB_DX : FLCE_TC_NB_DW);
+}
+constexpr int A_BYTES = BM * BK * 2;               // 16 KB
+constexpr int B_BYTES = (BN / 2) * BK * 2;         // 16 KB per 256-column sub-tile
+template <int MODE>
+__host__ __device__ constexpr int stage_bytes() {
+  return A_BYTES + nb_of<MODE>() * B_BYTES;        // 32 or 48 KB per CTA
+}
+// Pipeline depth: 192 KB of stages (6 x 32 KB or 4 x 48 KB) next to 32 KB of epilogue
+// staging.
+template <int MODE>
+__host__ __device__ constexpr int stages_of() {
+  return nb_of<MODE>() == 1 ? 6 : 4;
+}
+template <int MODE>
+__host__ __device__ constexpr int nacc_of() {      // TMEM accumulators (512 columns in all)
+  return nb_of<MODE>() == 1 ? 2 : 1;
+}
+template <int MODE>
+__host__ __device__ constexpr int epi_warps_of() {
+  return 4 * nb_of<MODE>();
+}
+constexpr int MAX_STAGES = 6;
+constexpr int BOX_BYTES = 64 * 64 * 2;             // one 64x64 MN-major TMA box (8 KB)
+constexpr int NUM_THREADS = 320;                   // producer, MMA, 8 epilogue warps
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tfull[2], tempty[2], drain
+// Epilogue staging: 32 KB, split over the active epilogue warps: 32-row x 128-byte
+// buffers (two per warp with four warps, one with eight) that feed TMA bulk tensor stores
+// (FWD: the exp slab) or reduce-adds (DX/DW: the L2 performs dst += tile; no register
+// read-modify-write).
+constexpr int EPI_BUF_BYTES = 32 * 128;
+constexpr int EPI_BYTES = 8 * EPI_BUF_BYTES;       // 32 KB
+template <int MODE>
+__host__ __device__ constexpr int epi_nbuf_of() {
+  return 8 / epi_warps_of<MODE>();
+}
+template <int MODE>
+constexpr int smem_bytes() {
+  return stages_of<MODE>() * stage_bytes<MODE>() + EPI_BYTES + 1024 + 512;
+}
 
 __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -212,8 +248,10 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_le1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+// Wait until at most N bulk groups of this thread still read their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -288,6 +326,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+// 64 consecutive fp32 columns (two 32-column loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,"
+      "%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]),
+        "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]),
+        "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]),
+        "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]),
+        "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + 32u)
+      : "memory");
+}
+
 template <typename T> __device__ __forceinline__ uint32_t pack2(float x, float y);
 template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float x, float y) {
   __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
@@ -299,30 +359,32 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float x, float y) 
 }
 
 // ------------------------------------------------------------------ tile space
+// Pair tiles: m indexes 256-row blocks of the output, n blocks of NB 256-column sub-tiles
+// (sub-tile index n * NB + j). nsub = the output's 256-column sub-tiles.
 struct TileSpace {
-  int mt, nt, nkb;
+  int mt, nt, nkb, nsub;
 };
 template <int MODE>
 __device__ __forceinline__ TileSpace tile_space(const CallArgs& a, int rows) {
   TileSpace t;
   if (MODE == FWD) {
     t.mt = cdiv(rows, 2 * BM);
-    t.nt = (int)a.nvt;
+    t.nsub = (int)a.nvt;
     t.nkb = cdiv((int)a.H, BK);
   } else if (MODE == DX) {
     t.mt = cdiv(rows, 2 * BM);
-    t.nt = cdiv((int)a.H, BN);
+    t.nsub = cdiv((int)a.H, BN);
     t.nkb = cdiv((int)a.V, BK);
   } else {
     t.mt = cdiv((int)a.V, 2 * BM);
-    t.nt = cdiv((int)a.H, BN);
+    t.nsub = cdiv((int)a.H, BN);
     t.nkb = cdiv(rows, BK);
   }
+  t.nt = cdiv(t.nsub, nb_of<MODE>());
   return t;
 }
-// Pair tiles: m indexes 256-row blocks of the output, n 256-column blocks. FWD walks m
-// fastest (the pairs in flight share W tiles); DX and DW walk n fastest (the pairs in
-// flight share the slab rows / columns).
+// FWD walks m fastest (the pairs in flight share W tiles); DX and DW walk n fastest (the
+// pairs in flight share the slab rows / columns).
 template <int MODE>
 __device__ __forceinline__ void tile_coords(const TileSpace& ts, int tile, int& m, int& n) {
   if (MODE == FWD) {
@@ -334,38 +396,131 @@ __device__ __forceinline__ void tile_coords(const TileSpace& ts, int tile, int& 
   }
 }
 
-// Work items of one pair: (pair tile, k-block range), taken round-robin over the pairs so
-// that the pairs in flight walk the same k-blocks in step and share operand tiles in L2.
-// FWD and DW take whole tiles. DX (few, long tiles: K = V) may split each tile's K range
-// in two halves (items ordered split-major: all first halves, then all second halves)
-// when that fills the last wave better; the two partial sums are added into a zeroed
-// buffer, so the result does not depend on their order.
-__device__ __forceinline__ int dx_splits(int ntiles, int npairs) {
-  const int w1 = (ntiles + npairs - 1) / npairs, w2 = (2 * ntiles + npairs - 1) / npairs;
-  // wave efficiency ntiles*S / (waves*P): compare ntiles/w1 with 2*ntiles/w2
-  return (2 * ntiles) * w1 > ntiles * w2 + (ntiles * w2) / 50 ? 2 : 1;
+// Work items of one pair: (pair tile, k-block range, split), taken round-robin over the
+// pairs so that the pairs in flight walk the same k-blocks in step and share operand tiles
+// in L2. FWD and DW take whole tiles. DX (few, long tiles: K = V) may split each tile's K
+// range in S <= 4 parts (items ordered split-major) when that fills the last wave better.
+// Split s adds its partial sum into fp32 buffer s / 2, zeroed beforehand, so each buffer
+// element receives at most two adds onto zero: the result does not depend on their order.
+constexpr int DX_MAX_SPLITS = 4;
+__device__ __forceinline__ int dx_splits(int ntiles, int npairs, int nkb) {
+  // wave efficiency e(S) = ntiles*S / (waves(S)*P); take the smallest S within 2% of the
+  // best (fewer splits add fewer partial sums)
+  int best = 1;
+  float eb = 0.0f;
+  float e[DX_MAX_SPLITS + 1];
+  for (int S = 1; S <= DX_MAX_SPLITS && S <= nkb; ++S) {
+    const int items = ntiles * S, waves = (items + npairs - 1) / npairs;
+    e[S] = (float)items / (float)(waves * npairs);
+    if (e[S] > eb) eb = e[S];
+  }
+  for (int S = 1; S <= DX_MAX_SPLITS && S <= nkb; ++S)
+    if (e[S] >= 0.98f * eb) {
+      best = S;
+      break;
+    }
+  return best;
 }
 template <int MODE>
 struct Items {
   int i, nitems, npairs, ntiles, nkb, S;
   __device__ __forceinline__ Items(int pair, int npairs_, int ntiles_, int nkb_)
       : i(pair), npairs(npairs_), ntiles(ntiles_), nkb(nkb_) {
-    S = (MODE == DX && nkb_ >= 2) ? dx_splits(ntiles_, npairs_) : 1;
+    S = MODE == DX ? dx_splits(ntiles_, npairs_, nkb_) : 1;
     nitems = S * ntiles_;
   }
-  __device__ __forceinline__ bool next(int& t, int& k0, int& k1) {
+  __device__ __forceinline__ bool next(int& t, int& k0, int& k1, int& split) {
     if (i >= nitems) return false;
-    const int s = i / ntiles;
-    t = i - s * ntiles;
-    k0 = (int)((int64_t)nkb * s / S);
-    k1 = (int)((int64_t)nkb * (s + 1) / S);
+    split = i / ntiles;
+    t = i - split * ntiles;
+    k0 = (int)((int64_t)nkb * split / S);
+    k1 = (int)((int64_t)nkb * (split + 1) / S);
     i += npairs;
     return true;
   }
 };
 
 // ------------------------------------------------------------------ epilogues
-template <typename T>
+// Row-reference forward epilogue: exp(s) needs no tile max, so one pass over TMEM gives
+// the max / lowest-index argmax / target logit and the staged exp values (64 columns per
+// TMEM wait), written to the slab by TMA bulk tensor stores as in the per-tile form.
+template <typename T, int NBUF>
+__device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, const CUtensorMap* tmS, uint8_t* stg,
+                                                 int row0, int rows, int mrow, int n, uint32_t taddr,
+                                                 int q, int lane, uint32_t& epi_it) {
+  const int rr = mrow + q * 32 + lane;  // row within the chunk
+  const bool valid = rr < rows;
+  const int V = (int)a.V;
+  int64_t tg = -1;
+  if (valid && a.targets != nullptr) tg = a.targets[a.w.idx[row0 + rr]];
+  const int v0 = n * VT;
+  const float ls = a.logit_scale;
+  const T* bias = (const T*)a.bias;
+  float mx = -INFINITY, tl = 0.0f, sum = 0.0f;
+  int ai = v0;
+  bool ht = false;
+#pragma unroll 1
+  for (int c2 = 0; c2 < BN / 64; ++c2) {
+    uint32_t r[64];
+    tmem_ld64(taddr + c2 * 64, r);
+    uint8_t* buf = stg + (epi_it % NBUF) * EPI_BUF_BYTES;
+    uint8_t* row = buf + lane * 128;
+    if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last read this buffer is done
+    __syncwarp();
+    uint32_t pk[32];
+#pragma unroll
+    for (int jj = 0; jj < 64; jj += 2) {
+      const int v = v0 + c2 * 64 + jj;
+      float s0 = __uint_as_float(r[jj]) * ls, s1 = __uint_as_float(r[jj + 1]) * ls;
+      float e0 = 0.0f, e1 = 0.0f;
+      if (v < V) {
+        if (bias != nullptr) s0 += to_f<T>(bias[v]);
+        if (s0 > mx) {
+          mx = s0;
+          ai = v;
+        }
+        if (v == tg) {
+          tl = s0;
+          ht = true;
+        }
+        e0 = exp2f(s0 * LOG2E);
+      }
+      if (v + 1 < V) {
+        if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
+        if (s1 > mx) {
+          mx = s1;
+          ai = v + 1;
+        }
+        if (v + 1 == tg) {
+          tl = s1;
+          ht = true;
+        }
+        e1 = exp2f(s1 * LOG2E);
+      }
+      sum += e0 + e1;
+      pk[jj / 2] = pack2<T>(e0, e1);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *(uint4*)(row + ((j ^ (lane & 7)) << 4)) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmS, smem_u32(buf), v0 + c2 * 64, mrow + q * 32);
+      bulk_commit();
+    }
+    ++epi_it;
+  }
+  if (valid) {
+    const int64_t o = (int64_t)rr * a.nvt + n;
+    a.w.stm[o] = mx;
+    a.w.sts[o] = sum;
+    a.w.sti[o] = ai;
+    if (ht) a.w.tgt[rr] = tl;
+  }
+}
+
+template <typename T, int NBUF>
 __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMap* tmS, uint8_t* stg,
                                              int row0, int rows, int mrow, int n, uint32_t taddr, int q,
                                              int lane, uint32_t& epi_it) {
@@ -410,9 +565,9 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
   uint8_t* row = nullptr;
 #pragma unroll 1
   for (int c2 = 0; c2 < BN / 64; ++c2) {
-    uint8_t* buf = stg + (epi_it & 1u) * EPI_BUF_BYTES;
+    uint8_t* buf = stg + (epi_it % NBUF) * EPI_BUF_BYTES;
     row = buf + lane * 128;
-    if (lane == 0) bulk_wait_read_le1();  // the store that last read this buffer is done
+    if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last read this buffer is done
     __syncwarp();
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
@@ -457,16 +612,19 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
   }
 }
 
-// dst tile += cbar * acc through TMA reduce-add (dst = dW for DW, the fp32 dX accumulator
-// for DX; in row-reference mode each dX row is also scaled by its rsc). Each epilogue warp owns 32 rows (its TMEM lane quadrant) and stages 32 columns
-// at a time (32 x 128 B, 128-byte swizzle: 16-byte chunk j of row r sits at chunk
-// j ^ (r % 8)), alternating two buffers; the TMA unit adds the box into dst in L2. A dW
-// element gets exactly one add per launch (one owning pair); a dX accumulator element at
-// most two (stream-K), added to zero: either way the result does not depend on timing.
+// dst tile += cbar * acc through TMA reduce-add (dst = dW for DW; for DX the fp32
+// accumulator buffer starting at row yoff; in row-reference mode each dX row is also
+// scaled by its rsc). Each epilogue warp owns 32 rows (its TMEM lane quadrant) and stages
+// 32 columns at a time (32 x 128 B, 128-byte swizzle: 16-byte chunk j of row r sits at
+// chunk j ^ (r % 8)) in NBUF rotating buffers; the TMA unit adds the box into dst in L2.
+// A dW element gets exactly one add per launch (one owning pair); a dX buffer element at
+// most two (K splits), added to zero: either way the result does not depend on timing.
 // Boxes past the destination's extent are clipped by the TMA unit.
+template <int NBUF>
 __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtensorMap* tmC, uint8_t* stg,
-                                                int mrow, int n, int ylimit, uint32_t taddr, int q,
-                                                int lane, float cb, const float* rsc, uint32_t& epi_it) {
+                                                int mrow, int n, int ylimit, int yoff, uint32_t taddr,
+                                                int q, int lane, float cb, const float* rsc,
+                                                uint32_t& epi_it) {
   const int H = (int)a.H;
   const int y = mrow + q * 32;
   if (y >= ylimit) return;  // this warp's 32 rows lie past the destination (warp-uniform)
@@ -477,8 +635,8 @@ __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtenso
     if (x >= H) break;  // warp-uniform
     uint32_t r[32];
     tmem_ld32(taddr + cc * 32, r);
-    uint8_t* buf = stg + (epi_it & 1u) * EPI_BUF_BYTES;
-    if (lane == 0) bulk_wait_read_le1();  // the reduce that last read this buffer is done
+    uint8_t* buf = stg + (epi_it % NBUF) * EPI_BUF_BYTES;
+    if (lane == 0) bulk_wait_read<NBUF - 1>();  // the reduce that last read this buffer is done
     __syncwarp();
     uint8_t* row = buf + lane * 128;
 #pragma unroll
@@ -490,7 +648,7 @@ __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtenso
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_reduce_add_2d(tmC, smem_u32(buf), x, y);
+      tma_reduce_add_2d(tmC, smem_u32(buf), x, y + yoff);
       bulk_commit();
     }
     ++epi_it;
@@ -538,6 +696,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CallArgs a,
               const int chunk) {
   constexpr int STAGES = stages_of<MODE>();
+  constexpr int SBYTES = stage_bytes<MODE>();
+  constexpr int NB = nb_of<MODE>();
+  constexpr int NACC = nacc_of<MODE>();
+  constexpr int NEPI = epi_warps_of<MODE>();
+  constexpr int NBUF = epi_nbuf_of<MODE>();
   if (a.run_if != nullptr && *a.run_if == 0) return;  // both CTAs of a pair read the same word
   int row0 = 0, rows = 0;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
@@ -551,8 +714,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
-  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE_BYTES + EPI_BYTES);
+  uint8_t* epi_stage = smem + STAGES * SBYTES;
+  uint64_t* bars = (uint64_t*)(smem + STAGES * SBYTES + EPI_BYTES);
   uint32_t* tmem_slot = (uint32_t*)(bars + NUM_BARS);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   int* copies = (int*)(tmem_slot + 2);  // per stage: phases this CTA's producer filled / armed
@@ -573,8 +736,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       copies[s] = 0;
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(tfull_bar(s), 1);   // one MMA commit per tile (multicast)
-      mbar_init(tempty_bar(s), 8);  // leader: 4 local + 4 peer epilogue warps
+      mbar_init(tfull_bar(s), 1);             // one MMA commit per tile (multicast)
+      mbar_init(tempty_bar(s), 2 * NEPI);     // leader: local + peer epilogue warps
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -600,33 +763,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int s = 0;
       uint32_t ph = 0;
       const bool stall = (a.flags & FLCE_FLAG_DEBUG_STALL) && MODE == FWD && leader;
-      const int half = (int)rank * BM;  // this CTA's 128-row half of A and of B
+      const int half = (int)rank * BM;  // this CTA's 128-row half of A and of each B sub-tile
       Items<MODE> items(pair, npairs, ntiles, ts.nkb);
-      int tile, k0, k1;
+      int tile, k0, k1, split;
       bool first = true;
-      while (items.next(tile, k0, k1)) {
+      while (items.next(tile, k0, k1, split)) {
         int m, n;
         tile_coords<MODE>(ts, tile, m, n);
         int kb = k0;
         for (; kb < k1; ++kb) {
           if (!wait_bounded(empty_bar(s), ph ^ 1u, ab, true)) break;
           const uint32_t fb = leader ? full_bar(s) : mapa(full_bar(s), 0);
-          if (leader) mbar_expect_tx(full_bar(s), 2 * STAGE_BYTES);
+          if (leader) mbar_expect_tx(full_bar(s), 2 * SBYTES);
           if (!(stall && first && kb == k1 - 1)) {
-            const uint32_t adst = smem_u32(smem + s * STAGE_BYTES);
+            const uint32_t adst = smem_u32(smem + s * SBYTES);
             const uint32_t bdst = adst + A_BYTES;
             if (MODE == FWD) {
               tma_load_2d(adst, &tmA, fb, kb * BK, m * 2 * BM + half);
-              tma_load_2d(bdst, &tmB, fb, kb * BK, n * BN + half);
+#pragma unroll
+              for (int j = 0; j < NB; ++j)
+                tma_load_2d(bdst + j * B_BYTES, &tmB, fb, kb * BK, (n * NB + j) * BN + half);
             } else if (MODE == DX) {
               tma_load_2d(adst, &tmA, fb, kb * BK, m * 2 * BM + half);
 #pragma unroll
-              for (int j = 0; j < 2; ++j) tma_load_2d(bdst + j * BOX_BYTES, &tmB, fb, n * BN + half + j * 64, kb * BK);
+              for (int j = 0; j < NB; ++j)
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+                  tma_load_2d(bdst + j * B_BYTES + jj * BOX_BYTES, &tmB, fb,
+                              (n * NB + j) * BN + half + jj * 64, kb * BK);
             } else {
 #pragma unroll
-              for (int j = 0; j < 2; ++j) tma_load_2d(adst + j * BOX_BYTES, &tmA, fb, m * 2 * BM + half + j * 64, kb * BK);
+              for (int jj = 0; jj < 2; ++jj)
+                tma_load_2d(adst + jj * BOX_BYTES, &tmA, fb, m * 2 * BM + half + jj * 64, kb * BK);
 #pragma unroll
-              for (int j = 0; j < 2; ++j) tma_load_2d(bdst + j * BOX_BYTES, &tmB, fb, n * BN + half + j * 64, kb * BK);
+              for (int j = 0; j < NB; ++j)
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+                  tma_load_2d(bdst + j * B_BYTES + jj * BOX_BYTES, &tmB, fb,
+                              (n * NB + j) * BN + half + jj * 64, kb * BK);
             }
           }
           copies[s] += 1;  // leader: phases armed; peer: phases filled
@@ -648,29 +822,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int it = 0;
       bool ok = true;
       Items<MODE> items(pair, npairs, ntiles, ts.nkb);
-      int tile, k0, k1;
-      for (; ok && items.next(tile, k0, k1); ++it) {
-        const int as = it & 1;
-        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      int tile, k0, k1, split;
+      for (; ok && items.next(tile, k0, k1, split); ++it) {
+        const int as = it % NACC;
+        const uint32_t aph = (uint32_t)(it / NACC) & 1u;
         if (!wait_bounded(tempty_bar(as), aph ^ 1u, ab, true)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(as * BN);
+        const uint32_t d = tmem_base + (uint32_t)(as * NB * BN);
         for (int kb = k0; kb < k1; ++kb) {
           if (!wait_bounded(full_bar(s), ph, ab, true)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t abase = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t abase = smem_u32(smem + s * SBYTES);
           const uint32_t bbase = abase + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = MODE == DW ? sdesc(abase + k * 2048, 8192, 1024) : sdesc(abase + k * 32, 16, 1024);
-            const uint64_t bd = MODE == FWD ? sdesc(bbase + k * 32, 16, 1024) : sdesc(bbase + k * 2048, 8192, 1024);
-            mma_f16(d, ad, bd, idesc, (kb != k0 || k != 0) ? 1u : 0u);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              const uint32_t bj = bbase + j * B_BYTES;
+              const uint64_t bd = MODE == FWD ? sdesc(bj + k * 32, 16, 1024) : sdesc(bj + k * 2048, 8192, 1024);
+              mma_f16(d + (uint32_t)(j * BN), ad, bd, idesc, (kb != k0 || k != 0) ? 1u : 0u);
+            }
           }
           mma_commit_pair(empty_bar(s));
           if (++s == STAGES) {
@@ -685,30 +863,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mma_commit_local(drain_bar);
       wait_bounded(drain_bar, 0u, ab, false);
     }
-  } else {
-    // ---------------- epilogue warps 2..5 (both CTAs)
+  } else if (warp - 2 < NEPI) {
+    // ---------------- epilogue warps (both CTAs): warp w reads TMEM lane quadrant w % 4
+    // of sub-tile (w - 2) / 4
     const int q = warp & 3;
+    const int j = (warp - 2) >> 2;
     const float cb = MODE == FWD ? 0.0f : a.w.ctrl->cbar;
     const float* rsc = (MODE == DX && a.ref_mode && a.w.ctrl->fb == 0) ? a.w.rsc : nullptr;
-    uint8_t* stg = epi_stage + (warp - 2) * 2 * EPI_BUF_BYTES;
+    uint8_t* stg = epi_stage + (warp - 2) * NBUF * EPI_BUF_BYTES;
     uint32_t epi_it = 0;
     int it = 0;
     Items<MODE> items(pair, npairs, ntiles, ts.nkb);
-    int tile, k0, k1;
-    for (; items.next(tile, k0, k1); ++it) {
-      const int as = it & 1;
-      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+    int tile, k0, k1, split;
+    for (; items.next(tile, k0, k1, split); ++it) {
+      const int as = it % NACC;
+      const uint32_t aph = (uint32_t)(it / NACC) & 1u;
       bool ok = wait_bounded(tfull_bar(as), aph, ab, true);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       int m, n;
       tile_coords<MODE>(ts, tile, m, n);
+      const int nsub = n * NB + j;  // this warp's 256-column sub-tile of the output
       const int mrow = m * 2 * BM + (int)rank * BM;
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(as * BN);
-      if (MODE == FWD) epilogue_fwd<T>(a, &tmC, stg, row0, rows, mrow, n, taddr, q, lane, epi_it);
-      else if (MODE == DW && a.dW_dt != FLCE_F32) epilogue_dw_same_dtype<T>(a, mrow, n * BN, taddr, q, lane, cb);
-      else epilogue_reduce(a, &tmC, stg, mrow, n, MODE == DX ? (int)a.R : (int)a.V, taddr, q, lane, cb, rsc, epi_it);
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((as * NB + j) * BN);
+      if (nsub < ts.nsub) {
+        if (MODE == FWD && a.ref_mode)
+          epilogue_fwd_ref<T, NBUF>(a, &tmC, stg, row0, rows, mrow, nsub, taddr, q, lane, epi_it);
+        else if (MODE == FWD)
+          epilogue_fwd<T, NBUF>(a, &tmC, stg, row0, rows, mrow, nsub, taddr, q, lane, epi_it);
+        else if (MODE == DW && a.dW_dt != FLCE_F32)
+          epilogue_dw_same_dtype<T>(a, mrow, nsub * BN, taddr, q, lane, cb);
+        else
+          epilogue_reduce<NBUF>(a, &tmC, stg, mrow, nsub, MODE == DX ? (int)a.R : (int)a.V,
+                                MODE == DX ? (split >> 1) * (int)a.R : 0, taddr, q, lane, cb, rsc, epi_it);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -734,10 +923,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int peer = (int)ld_cluster_u32(mapa(smem_u32(&copies[s]), 1));
       int last = mine;
       if (peer > mine) {
-        mbar_expect_tx(full_bar(s), STAGE_BYTES);  // arm the phase only the peer filled
+        mbar_expect_tx(full_bar(s), SBYTES);  // arm the phase only the peer filled
         last = peer;
       } else if (peer < mine) {
-        mbar_complete_tx(full_bar(s), STAGE_BYTES);  // the peer's half never came
+        mbar_complete_tx(full_bar(s), SBYTES);  // the peer's half never came
       }
       if (last > 0) wait_bounded(full_bar(s), (uint32_t)(last - 1) & 1u, ab, false);
     }
@@ -855,7 +1044,7 @@ cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 128)) return cudaErrorInvalidValue;
   CUtensorMap C;  // the exp slab, written by the epilogue
   if (!tc::make_map(&C, a.w.slab, a.dt, a.Vp, a.R, a.Vp * esz, 64, 32)) return cudaErrorInvalidValue;
-  const int64_t tiles = ((a.R + 255) / 256) * a.nvt;
+  const int64_t tiles = ((a.R + 255) / 256) * ((a.nvt + tc::nb_of<tc::FWD>() - 1) / tc::nb_of<tc::FWD>());
   return tc::launch_mode<tc::FWD>(a, chunk, s, A, B, C, tiles);
 }
 
@@ -864,9 +1053,10 @@ cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 64)) return cudaErrorInvalidValue;
-  CUtensorMap C;
-  if (!tc::make_map(&C, a.w.dxacc, FLCE_F32, a.H, a.R, a.H * 4, 32, 32)) return cudaErrorInvalidValue;
-  const int64_t tiles = 2 * ((a.R + 255) / 256) * ((a.H + 255) / 256);  // up to 2 K halves
+  CUtensorMap C;  // the two fp32 accumulator buffers [2R, H] (K splits 0-1 and 2-3)
+  if (!tc::make_map(&C, a.w.dxacc, FLCE_F32, a.H, 2 * a.R, a.H * 4, 32, 32)) return cudaErrorInvalidValue;
+  constexpr int nb = tc::nb_of<tc::DX>();
+  const int64_t tiles = tc::DX_MAX_SPLITS * ((a.R + 255) / 256) * (((a.H + 255) / 256 + nb - 1) / nb);
   return tc::launch_mode<tc::DX>(a, chunk, s, A, B, C, tiles);
 }
 
@@ -881,7 +1071,8 @@ cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   } else {
     C = A;
   }
-  const int64_t tiles = ((a.V + 255) / 256) * ((a.H + 255) / 256);
+  constexpr int nb = tc::nb_of<tc::DW>();
+  const int64_t tiles = ((a.V + 255) / 256) * (((a.H + 255) / 256 + nb - 1) / nb);
   return tc::launch_mode<tc::DW>(a, chunk, s, A, B, C, tiles);
 }
 
