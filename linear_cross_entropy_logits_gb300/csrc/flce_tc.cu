@@ -348,6 +348,15 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "memory");
 }
 
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error about 2^-22, results
+// below 2^-126 flushed to zero), far finer than the 2^-9 rounding of the 16-bit slab the
+// values are stored in; the accurate library exp2f made the epilogue arithmetic-bound.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename T> __device__ __forceinline__ uint32_t pack2(float x, float y);
 template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float x, float y) {
   __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
@@ -468,38 +477,49 @@ __device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, const CUtens
     if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last read this buffer is done
     __syncwarp();
     uint32_t pk[32];
+    // four independent max / argmax chains (merged below with lowest-index ties), so the
+    // compare-select latency of one chain does not serialise the 64 columns
+    float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
+    int a4[4] = {ai, 0x7fffffff, 0x7fffffff, 0x7fffffff};
 #pragma unroll
     for (int jj = 0; jj < 64; jj += 2) {
       const int v = v0 + c2 * 64 + jj;
       float s0 = __uint_as_float(r[jj]) * ls, s1 = __uint_as_float(r[jj + 1]) * ls;
-      float e0 = 0.0f, e1 = 0.0f;
-      if (v < V) {
-        if (bias != nullptr) s0 += to_f<T>(bias[v]);
-        if (s0 > mx) {
-          mx = s0;
-          ai = v;
-        }
-        if (v == tg) {
-          tl = s0;
-          ht = true;
-        }
-        e0 = exp2f(s0 * LOG2E);
+      const bool ok0 = v < V, ok1 = v + 1 < V;
+      if (bias != nullptr) {
+        if (ok0) s0 += to_f<T>(bias[v]);
+        if (ok1) s1 += to_f<T>(bias[v + 1]);
       }
-      if (v + 1 < V) {
-        if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
-        if (s1 > mx) {
-          mx = s1;
-          ai = v + 1;
-        }
-        if (v + 1 == tg) {
-          tl = s1;
-          ht = true;
-        }
-        e1 = exp2f(s1 * LOG2E);
+      const int u = 2 * ((jj >> 1) & 1);
+      if (ok0 && s0 > m4[u]) {
+        m4[u] = s0;
+        a4[u] = v;
       }
+      if (ok1 && s1 > m4[u + 1]) {
+        m4[u + 1] = s1;
+        a4[u + 1] = v + 1;
+      }
+      if (v == tg) {
+        tl = s0;
+        ht = true;
+      }
+      if (v + 1 == tg) {
+        tl = s1;
+        ht = true;
+      }
+      const float e0 = ok0 ? ex2_fast(s0 * LOG2E) : 0.0f;
+      const float e1 = ok1 ? ex2_fast(s1 * LOG2E) : 0.0f;
       sum += e0 + e1;
       pk[jj / 2] = pack2<T>(e0, e1);
     }
+#pragma unroll
+    for (int k = 1; k < 4; ++k)
+      if (m4[k] > m4[0] || (m4[k] == m4[0] && a4[k] < a4[0])) {
+        m4[0] = m4[k];
+        a4[0] = a4[k];
+      }
+    mx = m4[0];
+    ai = a4[0];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       *(uint4*)(row + ((j ^ (lane & 7)) << 4)) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
@@ -581,11 +601,11 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
         float e0 = 0.0f, e1 = 0.0f;
         if (v < V) {
           if (bias != nullptr) s0 += to_f<T>(bias[v]);
-          e0 = exp2f(fmaf(s0, LOG2E, -mxl));
+          e0 = ex2_fast(fmaf(s0, LOG2E, -mxl));
         }
         if (v + 1 < V) {
           if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
-          e1 = exp2f(fmaf(s1, LOG2E, -mxl));
+          e1 = ex2_fast(fmaf(s1, LOG2E, -mxl));
         }
         sum += e0 + e1;
         pk[j / 2] = pack2<T>(e0, e1);
