@@ -151,7 +151,7 @@ typedef struct flce_args {
 } flce_args;
 
 /* Workspace bytes for a problem, choosing the row-chunk so that the workspace stays
- * within budget_bytes (0 means 1.5 GiB). The result grows with BT only by 16 bytes per
+ * within budget_bytes (0 means 3 GiB). The result grows with BT only by 16 bytes per
  * row (the compaction index and per-row loss terms) and is capped by the budget. Returns 0
  * on invalid arguments or when not even one 128-row chunk fits in the budget. */
 FLCE_API size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V, int32_t in_dtype,
@@ -215,7 +215,7 @@ typedef struct flce_jsd_args {
                                divergence and gradient passes count as FLCE_STAGE_GPASS) */
 } flce_jsd_args;
 
-/* Workspace bytes for the distillation op within budget_bytes (0 means 1.5 GiB); 0 when
+/* Workspace bytes for the distillation op within budget_bytes (0 means 3 GiB); 0 when
  * not even one 128-row chunk fits or on invalid arguments. */
 FLCE_API size_t flce_jsd_workspace_size(int64_t BT, int64_t Hs, int64_t Ht, int64_t V,
                                         int32_t in_dtype, size_t budget_bytes);

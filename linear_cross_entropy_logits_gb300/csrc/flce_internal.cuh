@@ -18,7 +18,10 @@ namespace flce {
 constexpr int VT = 256;
 constexpr int CHUNK_ALIGN = 128;   // row-chunk granularity (one tensor-core M tile)
 constexpr uint32_t DEFAULT_TIMEOUT_MS = 4000;
-constexpr size_t DEFAULT_BUDGET = (size_t)3 << 29;  // 1.5 GiB
+// Default workspace budget: 3 GiB, about 1% of a GB300's 288 GB of HBM. It holds the
+// whole 8192-row chunk of a Llama-3.1-8B head (one pass of W per GEMM, one dW
+// read-modify-write per call); callers that need less transient memory pass a budget.
+constexpr size_t DEFAULT_BUDGET = (size_t)3 << 30;
 
 // Device status bits (1 << flce_status).
 constexpr int ST_TARGET_RANGE = 1 << FLCE_ERR_TARGET_RANGE;

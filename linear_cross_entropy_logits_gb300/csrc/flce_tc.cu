@@ -640,7 +640,12 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
 // A dW element gets exactly one add per launch (one owning pair); a dX buffer element at
 // most two (K splits), added to zero: either way the result does not depend on timing.
 // Boxes past the destination's extent are clipped by the TMA unit.
-template <int NBUF>
+//
+// HALF (the eight-warp epilogue of the wide tiles, 4 KB of staging per warp): two 2 KB
+// buffers of 32 rows x 16 columns (64-byte swizzle: 16-byte chunk j of row r at chunk
+// j ^ ((r / 2) % 4)), so that a warp stages the next half while the TMA unit still reads
+// the previous one; the map's box is then {16, 32}.
+template <int NBUF, bool HALF>
 __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtensorMap* tmC, uint8_t* stg,
                                                 int mrow, int n, int ylimit, int yoff, uint32_t taddr,
                                                 int q, int lane, float cb, const float* rsc,
@@ -649,6 +654,38 @@ __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtenso
   const int y = mrow + q * 32;
   if (y >= ylimit) return;  // this warp's 32 rows lie past the destination (warp-uniform)
   if (rsc != nullptr) cb *= rsc[y + lane];  // y + lane < ylimit = R (multiples of 32)
+  if (HALF) {
+#pragma unroll 1
+    for (int cc = 0; cc < BN / 32; ++cc) {
+      const int x = n * BN + cc * 32;
+      if (x >= H) break;  // warp-uniform
+      uint32_t r[32];
+      tmem_ld32(taddr + cc * 32, r);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (x + 16 * h >= H) break;  // warp-uniform
+        uint8_t* buf = stg + (epi_it & 1u) * (EPI_BUF_BYTES / 2);
+        if (lane == 0) bulk_wait_read<1>();  // the reduce that last read this buffer is done
+        __syncwarp();
+        uint8_t* row = buf + lane * 64;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 16 * h + 4 * j;
+          float4 v = make_float4(cb * __uint_as_float(r[c + 0]), cb * __uint_as_float(r[c + 1]),
+                                 cb * __uint_as_float(r[c + 2]), cb * __uint_as_float(r[c + 3]));
+          *(float4*)(row + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_2d(tmC, smem_u32(buf), x + 16 * h, y + yoff);
+          bulk_commit();
+        }
+        ++epi_it;
+      }
+    }
+    return;
+  }
 #pragma unroll 1
   for (int cc = 0; cc < BN / 32; ++cc) {
     const int x = n * BN + cc * 32;
@@ -915,7 +952,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         else if (MODE == DW && a.dW_dt != FLCE_F32)
           epilogue_dw_same_dtype<T>(a, mrow, nsub * BN, taddr, q, lane, cb);
         else
-          epilogue_reduce<NBUF>(a, &tmC, stg, mrow, nsub, MODE == DX ? (int)a.R : (int)a.V,
+          epilogue_reduce<NBUF, (NB == 2)>(a, &tmC, stg, mrow, nsub, MODE == DX ? (int)a.R : (int)a.V,
                                 MODE == DX ? (split >> 1) * (int)a.R : 0, taddr, q, lane, cb, rsc, epi_it);
       }
       tc_fence_before();
@@ -982,7 +1019,8 @@ EncodeTiledFn encode_fn() {
 // 2-D tiled map over a row-major matrix [outer, inner] with row pitch `pitch_bytes`;
 // 128-byte swizzle, zero fill outside the matrix.
 bool make_map(CUtensorMap* m, const void* ptr, int dt, uint64_t inner, uint64_t outer,
-              uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+              uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const CUtensorMapDataType ty = dt == FLCE_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -993,7 +1031,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int dt, uint64_t inner, uint64_t 
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t es[2] = {1, 1};
   return enc(m, ty, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1074,8 +1112,10 @@ cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 64)) return cudaErrorInvalidValue;
   CUtensorMap C;  // the two fp32 accumulator buffers [2R, H] (K splits 0-1 and 2-3)
-  if (!tc::make_map(&C, a.w.dxacc, FLCE_F32, a.H, 2 * a.R, a.H * 4, 32, 32)) return cudaErrorInvalidValue;
   constexpr int nb = tc::nb_of<tc::DX>();
+  if (!tc::make_map(&C, a.w.dxacc, FLCE_F32, a.H, 2 * a.R, a.H * 4, nb == 2 ? 16 : 32, 32,
+                    nb == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   const int64_t tiles = tc::DX_MAX_SPLITS * ((a.R + 255) / 256) * (((a.H + 255) / 256 + nb - 1) / nb);
   return tc::launch_mode<tc::DX>(a, chunk, s, A, B, C, tiles);
 }
@@ -1086,12 +1126,14 @@ cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 64)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 64)) return cudaErrorInvalidValue;
   CUtensorMap C;  // fp32 dW for TMA reduce-add; unused (a copy of A) for same-dtype dW
+  constexpr int nb = tc::nb_of<tc::DW>();
   if (a.dW_dt == FLCE_F32) {
-    if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, 32, 32)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, nb == 2 ? 16 : 32, 32,
+                      nb == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
   } else {
     C = A;
   }
-  constexpr int nb = tc::nb_of<tc::DW>();
   const int64_t tiles = ((a.V + 255) / 256) * (((a.H + 255) / 256 + nb - 1) / nb);
   return tc::launch_mode<tc::DW>(a, chunk, s, A, B, C, tiles);
 }

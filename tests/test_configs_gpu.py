@@ -1,5 +1,5 @@
 """Parity at the workloads' full sizes, in the launch configuration the benchmark times
-(default 1.5 GiB workspace budget).
+(default workspace budget; the large-vocab workload's own 1.5 GiB cap).
 
 The oracle cannot evaluate every row of these problems in seconds, so each check is
 either on sampled outputs the oracle computes one by one, or on a property that holds at
