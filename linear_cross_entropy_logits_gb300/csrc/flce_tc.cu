@@ -57,38 +57,30 @@ enum Mode { FWD = 0, DX = 1, DW = 2 };
 // are bound by the operand feed), with one 512-column TMEM accumulator and eight epilogue
 // warps (one per TMEM lane quadrant and sub-tile). NB = 1: 256 x 256 tiles with two
 // 256-column accumulators, so that a tile's epilogue overlaps the next tile's mainloop.
-#ifndef FLCE_TC_NB_FWD
-#define FLCE_TC_NB_FWD 1
-#endif
-#ifndef FLCE_TC_NB_DX
-#define FLCE_TC_NB_DX 2
-#endif
-#ifndef FLCE_TC_NB_DW
-#define FLCE_TC_NB_DW 2
-#endif
-template <int MODE>
-__host__ __device__ constexpr int nb_of() {
-  return MODE == FWD ? FLCE_TC_NB_FWD : (MODE == DX ? FLCE_TC_NB_DX : FLCE_TC_NB_DW);
-}
+// The forward takes NB = 1 (its epilogue must overlap: the wide forward tile measured
+// slower); dX takes NB = 2 (K = V, the epilogue is negligible); dW takes NB = 2 when a
+// chunk holds at least DW_WIDE_MIN_ROWS rows (K long enough to amortise the exposed
+// reduce-add epilogue) and NB = 1 below that.
+constexpr int DW_WIDE_MIN_ROWS = 4096;
 constexpr int A_BYTES = BM * BK * 2;               // 16 KB
 constexpr int B_BYTES = (BN / 2) * BK * 2;         // 16 KB per 256-column sub-tile
-template <int MODE>
+template <int NB>
 __host__ __device__ constexpr int stage_bytes() {
-  return A_BYTES + nb_of<MODE>() * B_BYTES;        // 32 or 48 KB per CTA
+  return A_BYTES + NB * B_BYTES;                   // 32 or 48 KB per CTA
 }
 // Pipeline depth: 192 KB of stages (6 x 32 KB or 4 x 48 KB) next to 32 KB of epilogue
 // staging.
-template <int MODE>
+template <int NB>
 __host__ __device__ constexpr int stages_of() {
-  return nb_of<MODE>() == 1 ? 6 : 4;
+  return NB == 1 ? 6 : 4;
 }
-template <int MODE>
+template <int NB>
 __host__ __device__ constexpr int nacc_of() {      // TMEM accumulators (512 columns in all)
-  return nb_of<MODE>() == 1 ? 2 : 1;
+  return NB == 1 ? 2 : 1;
 }
-template <int MODE>
+template <int NB>
 __host__ __device__ constexpr int epi_warps_of() {
-  return 4 * nb_of<MODE>();
+  return 4 * NB;
 }
 constexpr int MAX_STAGES = 6;
 constexpr int BOX_BYTES = 64 * 64 * 2;             // one 64x64 MN-major TMA box (8 KB)
@@ -101,13 +93,13 @@ constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tfull[2], tem
 // read-modify-write).
 constexpr int EPI_BUF_BYTES = 32 * 128;
 constexpr int EPI_BYTES = 8 * EPI_BUF_BYTES;       // 32 KB
-template <int MODE>
+template <int NB>
 __host__ __device__ constexpr int epi_nbuf_of() {
-  return 8 / epi_warps_of<MODE>();
+  return 8 / epi_warps_of<NB>();
 }
-template <int MODE>
+template <int NB>
 constexpr int smem_bytes() {
-  return stages_of<MODE>() * stage_bytes<MODE>() + EPI_BYTES + 1024 + 512;
+  return stages_of<NB>() * stage_bytes<NB>() + EPI_BYTES + 1024 + 512;
 }
 
 __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -373,7 +365,7 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float x, float y) 
 struct TileSpace {
   int mt, nt, nkb, nsub;
 };
-template <int MODE>
+template <int MODE, int NB>
 __device__ __forceinline__ TileSpace tile_space(const CallArgs& a, int rows) {
   TileSpace t;
   if (MODE == FWD) {
@@ -389,7 +381,7 @@ __device__ __forceinline__ TileSpace tile_space(const CallArgs& a, int rows) {
     t.nsub = cdiv((int)a.H, BN);
     t.nkb = cdiv(rows, BK);
   }
-  t.nt = cdiv(t.nsub, nb_of<MODE>());
+  t.nt = cdiv(t.nsub, NB);
   return t;
 }
 // FWD walks m fastest (the pairs in flight share W tiles); DX and DW walk n fastest (the
@@ -747,21 +739,20 @@ __device__ __forceinline__ void epilogue_dw_same_dtype(const CallArgs& a, int mr
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int MODE, typename T>
+template <int MODE, typename T, int NB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CallArgs a,
               const int chunk) {
-  constexpr int STAGES = stages_of<MODE>();
-  constexpr int SBYTES = stage_bytes<MODE>();
-  constexpr int NB = nb_of<MODE>();
-  constexpr int NACC = nacc_of<MODE>();
-  constexpr int NEPI = epi_warps_of<MODE>();
-  constexpr int NBUF = epi_nbuf_of<MODE>();
+  constexpr int STAGES = stages_of<NB>();
+  constexpr int SBYTES = stage_bytes<NB>();
+  constexpr int NACC = nacc_of<NB>();
+  constexpr int NEPI = epi_warps_of<NB>();
+  constexpr int NBUF = epi_nbuf_of<NB>();
   if (a.run_if != nullptr && *a.run_if == 0) return;  // both CTAs of a pair read the same word
   int row0 = 0, rows = 0;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
-  const TileSpace ts = tile_space<MODE>(a, rows);
+  const TileSpace ts = tile_space<MODE, NB>(a, rows);
   const int ntiles = ts.mt * ts.nt;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
@@ -1037,11 +1028,11 @@ bool make_map(CUtensorMap* m, const void* ptr, int dt, uint64_t inner, uint64_t 
 
 // Launch as clusters of 2 CTAs, one pair per pair tile up to the number of pairs that fit
 // the GPU at once (persistent).
-template <int MODE, typename T>
+template <int MODE, typename T, int NB>
 cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
                      const CUtensorMap& B, const CUtensorMap& C, int64_t pair_tiles_max) {
-  auto kern = k_gemm_tc<MODE, T>;
-  constexpr int smem = smem_bytes<MODE>();
+  auto kern = k_gemm_tc<MODE, T, NB>;
+  constexpr int smem = smem_bytes<NB>();
   static int max_pairs[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1079,11 +1070,11 @@ cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtenso
   return cudaGetLastError();
 }
 
-template <int MODE>
+template <int MODE, int NB>
 cudaError_t launch_mode(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
                         const CUtensorMap& B, const CUtensorMap& C, int64_t tiles_max) {
-  if (a.dt == FLCE_BF16) return launch_t<MODE, __nv_bfloat16>(a, chunk, s, A, B, C, tiles_max);
-  return launch_t<MODE, __half>(a, chunk, s, A, B, C, tiles_max);
+  if (a.dt == FLCE_BF16) return launch_t<MODE, __nv_bfloat16, NB>(a, chunk, s, A, B, C, tiles_max);
+  return launch_t<MODE, __half, NB>(a, chunk, s, A, B, C, tiles_max);
 }
 
 }  // namespace tc
@@ -1102,8 +1093,8 @@ cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 128)) return cudaErrorInvalidValue;
   CUtensorMap C;  // the exp slab, written by the epilogue
   if (!tc::make_map(&C, a.w.slab, a.dt, a.Vp, a.R, a.Vp * esz, 64, 32)) return cudaErrorInvalidValue;
-  const int64_t tiles = ((a.R + 255) / 256) * ((a.nvt + tc::nb_of<tc::FWD>() - 1) / tc::nb_of<tc::FWD>());
-  return tc::launch_mode<tc::FWD>(a, chunk, s, A, B, C, tiles);
+  const int64_t tiles = ((a.R + 255) / 256) * a.nvt;
+  return tc::launch_mode<tc::FWD, 1>(a, chunk, s, A, B, C, tiles);
 }
 
 cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
@@ -1112,12 +1103,10 @@ cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 64)) return cudaErrorInvalidValue;
   CUtensorMap C;  // the two fp32 accumulator buffers [2R, H] (K splits 0-1 and 2-3)
-  constexpr int nb = tc::nb_of<tc::DX>();
-  if (!tc::make_map(&C, a.w.dxacc, FLCE_F32, a.H, 2 * a.R, a.H * 4, nb == 2 ? 16 : 32, 32,
-                    nb == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!tc::make_map(&C, a.w.dxacc, FLCE_F32, a.H, 2 * a.R, a.H * 4, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  const int64_t tiles = tc::DX_MAX_SPLITS * ((a.R + 255) / 256) * (((a.H + 255) / 256 + nb - 1) / nb);
-  return tc::launch_mode<tc::DX>(a, chunk, s, A, B, C, tiles);
+  const int64_t tiles = tc::DX_MAX_SPLITS * ((a.R + 255) / 256) * (((a.H + 255) / 256 + 1) / 2);
+  return tc::launch_mode<tc::DX, 2>(a, chunk, s, A, B, C, tiles);
 }
 
 cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
@@ -1126,16 +1115,17 @@ cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 64)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 64)) return cudaErrorInvalidValue;
   CUtensorMap C;  // fp32 dW for TMA reduce-add; unused (a copy of A) for same-dtype dW
-  constexpr int nb = tc::nb_of<tc::DW>();
+  const bool wide = a.R >= tc::DW_WIDE_MIN_ROWS;
   if (a.dW_dt == FLCE_F32) {
-    if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, nb == 2 ? 16 : 32, 32,
-                      nb == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, wide ? 16 : 32, 32,
+                      wide ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   } else {
     C = A;
   }
-  const int64_t tiles = ((a.V + 255) / 256) * (((a.H + 255) / 256 + nb - 1) / nb);
-  return tc::launch_mode<tc::DW>(a, chunk, s, A, B, C, tiles);
+  const int64_t vt = (a.V + 255) / 256, ht = (a.H + 255) / 256;
+  if (wide) return tc::launch_mode<tc::DW, 2>(a, chunk, s, A, B, C, vt * ((ht + 1) / 2));
+  return tc::launch_mode<tc::DW, 1>(a, chunk, s, A, B, C, vt * ht);
 }
 
 }  // namespace flce

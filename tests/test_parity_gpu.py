@@ -242,3 +242,15 @@ def test_guard_bands_untouched():
     assert o["status_code"] == flce.FLCE_OK
     for raw in [b[0] for b in bufs.values()] + [dW_raw, db_raw, ws_raw]:
         assert torch.all(raw[:G] == sentinel) and torch.all(raw[-G:] == sentinel)
+
+
+@pytest.mark.parametrize("H", [136, 520])
+def test_wide_dw_tile_ragged(H):
+    """Chunks of at least 4096 rows take the 256 x 512 dW tile; H = 136 leaves the second
+    256-column sub-tile wholly past the output, H = 520 a third sub-tile partly past it.
+    Every output against the oracle."""
+    sp = I.spec("llama1b", BT=4300, H=H, V=1300, w_std=0.2, ignore="random", n_ignored=100)
+    inp = I.generate(sp, seed=21)
+    assert flce.chunk_rows(sp["BT"], H, sp["V"], torch.bfloat16,
+                           flce.workspace_size(sp["BT"], H, sp["V"], torch.bfloat16, 0)) >= 4096
+    compare_full(run_gpu(inp, sp), run_oracle(inp, sp), inp, sp)
