@@ -55,6 +55,13 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--op", default="flce", choices=["flce", "jsd"])
     p.add_argument("--workload", default="llama8b", choices=list(I.WORKLOADS))
+    p.add_argument("--dtype", default=None, choices=["bf16", "f16"],
+                   help="override the workload's input dtype")
+    p.add_argument("--dw-dtype", default="f32", choices=["f32", "same"],
+                   help="dW / dbias accumulation dtype: fp32, or the input dtype")
+    p.add_argument("--api", default="abi", choices=["abi", "torch"],
+                   help="abi: the C ABI through the ctypes binding; torch: the autograd op "
+                        "(loss = fused_linear_cross_entropy(X, W, targets); loss.backward())")
     p.add_argument("--labelled-fraction", type=float, default=None)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -72,6 +79,8 @@ def workload_spec(args):
         ov["labelled_fraction"] = args.labelled_fraction
     if args.bt is not None:
         ov["BT"] = args.bt
+    if getattr(args, "dtype", None) is not None:
+        ov["dtype"] = args.dtype
     return I.spec(args.workload, **ov)
 
 
@@ -325,14 +334,36 @@ def run_ours(args):
             "n_labelled": torch.empty(1, dtype=torch.int32, device=dev),
             "status": torch.zeros(1, dtype=torch.int32, device=dev),
             "dX": torch.empty(BT, H, dtype=dt, device=dev)}
-    dW = torch.zeros(V, H, dtype=torch.float32, device=dev) if sp["want_dW"] else None
-    dbias = torch.zeros(V, dtype=torch.float32, device=dev) if (sp["want_dW"] and bias is not None) else None
+    acc_dt = torch.float32 if args.dw_dtype == "f32" else dt
+    dW = torch.zeros(V, H, dtype=acc_dt, device=dev) if sp["want_dW"] else None
+    dbias = torch.zeros(V, dtype=acc_dt, device=dev) if (sp["want_dW"] and bias is not None) else None
     prof = flce.Profiler()
 
-    def step(Xd=X, tgd=tg, god=go, profiler=None):
-        flce.fwd_bwd(Xd, W, tgd, bias, reduction=sp["reduction"], z_loss_scale=sp.get("z", 0.0),
-                     grad_out=god, want_dX=True, want_dW=sp["want_dW"], dW=dW, dbias=dbias,
-                     workspace=ws, outputs=outs, check=False, profiler=profiler)
+    if args.api == "torch":
+        from linear_cross_entropy_logits_gb300.torch_ops import fused_linear_cross_entropy
+        Xp = X.detach().clone().requires_grad_(True)
+        Wp = W.detach().clone().requires_grad_(sp["want_dW"])
+        bp = bias.detach().clone().requires_grad_(sp["want_dW"]) if bias is not None else None
+
+        def step(Xd=X, tgd=tg, god=go, profiler=None):
+            # a training step's view: fresh .grad tensors each step
+            Xp.grad = None
+            Wp.grad = None
+            if bp is not None:
+                bp.grad = None
+            loss = fused_linear_cross_entropy(Xp, Wp, tgd, bp, reduction=sp["reduction"],
+                                              z_loss_scale=sp.get("z", 0.0),
+                                              accum_dtype=acc_dt)
+            if sp["reduction"] == "none":
+                loss.backward(god)
+            else:
+                loss.backward()
+            outs["loss"] = loss.detach().reshape(-1)
+    else:
+        def step(Xd=X, tgd=tg, god=go, profiler=None):
+            flce.fwd_bwd(Xd, W, tgd, bias, reduction=sp["reduction"], z_loss_scale=sp.get("z", 0.0),
+                         grad_out=god, want_dX=True, want_dW=sp["want_dW"], dW=dW, dbias=dbias,
+                         workspace=ws, outputs=outs, check=False, profiler=profiler)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(args.warmup, 3)):
@@ -374,7 +405,7 @@ def run_ours(args):
     # reads the loss back; the copy of step k+1 overlaps step k on a copy stream
     # (DoubleBufferedInputs), as a training loop feeding the op would run
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.api == "abi":
         from linear_cross_entropy_logits_gb300.feeder import DoubleBufferedInputs
         host = {"X": inp["X"].pin_memory(), "t": inp["targets"].pin_memory()}
         if inp["grad_out"] is not None:
@@ -418,7 +449,10 @@ def run_ours(args):
     stage_summary = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                      for k, v in stages.items() if v[1] > 0}
     rec = traffic_record()
-    if dom in ("fwd", "dx", "dw"):
+    if args.api == "torch":
+        # the autograd op takes no profiler: whole-step numbers only
+        roof = None
+    elif dom in ("fwd", "dx", "dw"):
         achieved = gemm_flops / (per_step_dom_ms / 1000.0) / 1e12
         peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
@@ -441,7 +475,8 @@ def run_ours(args):
             "parallelism": f"replicas x{world} (no exchange step)",
             "l2": f"no flush: W ({V * H * I.TORCH_DTYPES[sp['dtype']].itemsize / 1e9:.2f} GB) and the "
                   f"per-chunk slab exceed the 129 MB L2",
-            "workspace_bytes": ws_bytes, "chunk_rows": R}),
+            "workspace_bytes": ws_bytes, "chunk_rows": R, "api": args.api,
+            "dW_dtype": "f32" if args.dw_dtype == "f32" else sp["dtype"]}),
         "ms_per_step_percentiles": per_step,
         "transient": transient,
         "tokens_per_s_labelled": n_lab * world / (ms_step / 1000.0),
@@ -451,7 +486,7 @@ def run_ours(args):
                               "source": peak_src},
         "roofline": roof,
         "stages": stage_summary,
-        "gpu_launches": int(sum(v[1] for v in stages.values())),
+        "gpu_launches": int(sum(v[1] for v in stages.values())) if args.api == "abi" else None,
         "clocks": clocks,
         "e2e": e2e,
         "context_vs_h200_public_default_ms": 53.039 if sp["name"] == "llama8b" else None,
@@ -611,7 +646,7 @@ def run_jsd(args):
                          "peak_kind": f"bf16 sustained ({src})", "traffic": None},
             "stages": {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                        for k, v in stages.items() if v[1] > 0},
-            "gpu_launches": int(sum(v[1] for v in stages.values())), "clocks": clocks, "e2e": e2e}
+            "gpu_launches": int(sum(v[1] for v in stages.values())) if args.api == "abi" else None, "clocks": clocks, "e2e": e2e}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, rows_done, secs = jsd_oracle_sample_rate(sp, inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",

@@ -86,6 +86,9 @@ typedef enum flce_dtype { FLCE_F32 = 0, FLCE_BF16 = 1, FLCE_F16 = 2 } flce_dtype
 #define FLCE_FLAG_NO_ROW_REF 0x2u /* always normalise the gradient slab per vocabulary tile
                                      (a full pass over it) instead of the default one-scale-
                                      per-row form of bf16 tensor-core calls without dbias   */
+#define FLCE_FLAG_DW_OVERWRITE 0x4u /* dW and dbias receive this call's gradient instead of
+                                     accumulating it (no need to zero them first); with no
+                                     labelled row they are set to zero                      */
 #define FLCE_FLAG_DEBUG_STALL 0x100u /* testing only: the tensor-core forward GEMM leaves
                                      one pipeline stage unfilled so that its bounded waits
                                      run out; the call must then report FLCE_ERR_TIMEOUT */
@@ -214,6 +217,16 @@ typedef struct flce_jsd_args {
   flce_profile* profile;    /* NULL, or a profiler (stages as for flce_fwd_bwd; the
                                divergence and gradient passes count as FLCE_STAGE_GPASS) */
 } flce_jsd_args;
+
+/* x[i] *= *g for 0 <= i < n, unless *g == 1 exactly: g is read on the device, so scaling
+ * by an upstream gradient that lives on the GPU needs no host synchronisation and costs
+ * nothing in the common case g == 1 (the torch autograd op scales the gradients it
+ * computed in the forward this way). x: device array of n elements of `dtype`
+ * (FLCE_F32, FLCE_BF16 or FLCE_F16), scaled in place; g: device pointer to one float.
+ * Enqueued on `stream`; returns FLCE_ERR_INVALID_ARG for null pointers, n < 0 or an
+ * unknown dtype, FLCE_ERR_CUDA if the launch fails. No counterpart on the pages: it is
+ * plumbing for the autograd binding. */
+FLCE_API int32_t flce_scale_by(void* x, int64_t n, int32_t dtype, const float* g, void* stream);
 
 /* Workspace bytes for the distillation op within budget_bytes (0 means 3 GiB); 0 when
  * not even one 128-row chunk fits or on invalid arguments. */

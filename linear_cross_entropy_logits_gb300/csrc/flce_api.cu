@@ -304,7 +304,21 @@ extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
   }
   if (a.reduction != FLCE_NONE)
     FLCE_TRY(staged(prof, FLCE_STAGE_REDUCE, 1, s, [&] { return launch_epilogue(a, s); }));
+  if (a.want_dW && (x->flags & FLCE_FLAG_DW_OVERWRITE))
+    FLCE_TRY(staged(prof, FLCE_STAGE_REDUCE, 1, s, [&] { return launch_zero_if_empty(a, s); }));
 #undef FLCE_TRY
+  return FLCE_OK;
+}
+
+extern "C" int32_t flce_scale_by(void* x, int64_t n, int32_t dtype, const float* g, void* stream) {
+  if (x == nullptr || g == nullptr || n < 0) return FLCE_ERR_INVALID_ARG;
+  if (dtype != FLCE_F32 && dtype != FLCE_BF16 && dtype != FLCE_F16) return FLCE_ERR_INVALID_ARG;
+  if (n == 0) return FLCE_OK;
+  const cudaError_t e = launch_scale_by(x, n, dtype, g, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = e;
+    return FLCE_ERR_CUDA;
+  }
   return FLCE_OK;
 }
 

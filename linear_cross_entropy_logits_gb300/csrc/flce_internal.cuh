@@ -131,6 +131,8 @@ cudaError_t launch_fwd_simt(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_finalize(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_gpass(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_scale_x(const CallArgs& a, int chunk, cudaStream_t s);  // Xc rows *= rsc
+cudaError_t launch_zero_if_empty(const CallArgs& a, cudaStream_t s);     // dW overwrite, N = 0
+cudaError_t launch_scale_by(void* x, int64_t n, int dtype, const float* g, cudaStream_t s);
 cudaError_t launch_dx_simt(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_dw_simt(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_epilogue(const CallArgs& a, cudaStream_t s);          // reductions

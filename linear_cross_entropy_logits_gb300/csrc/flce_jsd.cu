@@ -586,6 +586,8 @@ extern "C" int32_t flce_fused_linear_jsd(const flce_jsd_args* x, void* stream) {
   }
   if (s.reduction != FLCE_NONE)
     JSD_TRY(staged(prof, FLCE_STAGE_REDUCE, 1, st, [&] { return launch_epilogue(s, st); }));
+  if (s.want_dW && (x->flags & FLCE_FLAG_DW_OVERWRITE))
+    JSD_TRY(staged(prof, FLCE_STAGE_REDUCE, 1, st, [&] { return launch_zero_if_empty(s, st); }));
 #undef JSD_TRY
   return FLCE_OK;
 }

@@ -356,11 +356,13 @@ __global__ void __launch_bounds__(256) k_gpass(const __grid_constant__ CallArgs 
       for (int y = 0; y < 8; ++y) s += red[y][c];
       const int64_t v = (int64_t)t * VT + c;
       if (v < a.V) {
+        const bool ovw = (a.flags & FLCE_FLAG_DW_OVERWRITE) && chunk == 0;
         if (a.dW_dt == FLCE_F32) {
-          ((float*)a.dbias)[v] += cb * s;
+          float* db = (float*)a.dbias;
+          db[v] = ovw ? cb * s : db[v] + cb * s;
         } else {
           T* db = (T*)a.dbias;  // same-dtype accumulation
-          db[v] = from_f<T>(to_f<T>(db[v]) + cb * s);
+          db[v] = from_f<T>(ovw ? cb * s : to_f<T>(db[v]) + cb * s);
         }
       }
     }
@@ -384,6 +386,31 @@ __global__ void __launch_bounds__(256) k_scale_x(const __grid_constant__ CallArg
       xr[j] = __floats2bfloat162_rn(v.x * sc, v.y * sc);
     }
   }
+}
+
+// ---------------------------------------------------------------------------------------
+// dW / dbias overwrite with no labelled row: no chunk ran, so the destinations are zeroed
+// here (every block returns at once when n_lab > 0).
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_zero_if_empty(const __grid_constant__ CallArgs a) {
+  if (a.w.ctrl->n_lab > 0) return;
+  const int esz = a.dW_dt == FLCE_F32 ? 4 : 2;
+  const int64_t nw = a.V * a.H * esz, nb = a.dbias ? a.V * esz : 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nw; i += stride)
+    ((char*)a.dW)[i] = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nb; i += stride)
+    ((char*)a.dbias)[i] = 0;
+}
+
+// x[i] *= *g unless *g == 1 (device-side test; see flce_scale_by).
+template <typename T>
+__global__ void __launch_bounds__(256) k_scale_by(T* x, int64_t n, const float* g) {
+  const float f = *g;
+  if (f == 1.0f) return;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    x[i] = from_f<T>(to_f<T>(x[i]) * f);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -546,6 +573,8 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(256) k_gemm_simt(const __grid_constant__ CallArgs a, int chunk) {
   int row0, rows;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  // dW overwrite: the first chunk stores, later chunks accumulate
+  const bool ovw = (a.flags & FLCE_FLAG_DW_OVERWRITE) && chunk == 0;
   const int64_t M = MODE == 0 ? rows : a.V;
   const int64_t N = a.H;
   const int64_t K = MODE == 0 ? a.V : rows;
@@ -610,10 +639,11 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const __grid_constant__ CallA
         const int64_t orow = a.w.idx[row0 + m];
         ((T*)a.dX)[orow * a.H + n] = from_f<T>(cb * acc[i][j]);
       } else if (a.dW_dt == FLCE_F32) {
-        ((float*)a.dW)[m * a.H + n] += cb * acc[i][j];
+        float* w = (float*)a.dW + m * a.H + n;
+        *w = ovw ? cb * acc[i][j] : *w + cb * acc[i][j];
       } else {
         T* w = (T*)a.dW + m * a.H + n;  // same-dtype accumulation
-        *w = from_f<T>(to_f<T>(*w) + cb * acc[i][j]);
+        *w = from_f<T>(ovw ? cb * acc[i][j] : to_f<T>(*w) + cb * acc[i][j]);
       }
     }
   }
@@ -666,6 +696,21 @@ cudaError_t launch_prologue(const CallArgs& a, cudaStream_t s) {
 cudaError_t launch_gather(const CallArgs& a, int chunk, cudaStream_t s) {
   const int64_t blocks = a.R < 4LL * num_sms() ? a.R : 4LL * num_sms();
   k_gather<<<(unsigned)blocks, 256, 0, s>>>(a, chunk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_if_empty(const CallArgs& a, cudaStream_t s) {
+  k_zero_if_empty<<<(unsigned)(2 * num_sms()), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_by(void* x, int64_t n, int dtype, const float* g, cudaStream_t s) {
+  const unsigned blocks = (unsigned)(4 * num_sms());
+  switch (dtype) {
+    case FLCE_F32: k_scale_by<float><<<blocks, 256, 0, s>>>((float*)x, n, g); break;
+    case FLCE_BF16: k_scale_by<__nv_bfloat16><<<blocks, 256, 0, s>>>((__nv_bfloat16*)x, n, g); break;
+    default: k_scale_by<__half><<<blocks, 256, 0, s>>>((__half*)x, n, g); break;
+  }
   return cudaGetLastError();
 }
 

@@ -633,20 +633,25 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
 // most two (K splits), added to zero: either way the result does not depend on timing.
 // Boxes past the destination's extent are clipped by the TMA unit.
 //
-// HALF (the eight-warp epilogue of the wide tiles, 4 KB of staging per warp): two 2 KB
-// buffers of 32 rows x 16 columns (64-byte swizzle: 16-byte chunk j of row r at chunk
-// j ^ ((r / 2) % 4)), so that a warp stages the next half while the TMA unit still reads
-// the previous one; the map's box is then {16, 32}.
-template <int NBUF, bool HALF>
+// HALF (the eight-warp epilogue of the wide tiles, 4 KB of staging per warp, and every
+// 16-bit destination): two 2 KB buffers of 32 rows x 64 bytes (64-byte swizzle: 16-byte
+// chunk j of row r at chunk j ^ ((r / 2) % 4)), so that a warp stages the next box while
+// the TMA unit still reads the previous one. A box is 16 fp32 columns, or 32 columns of a
+// 16-bit destination D (same-dtype dW: the L2 adds in D), the map's box accordingly
+// {16, 32} or {32, 32}. STORE: the box overwrites dst instead of adding to it (the first
+// chunk of a call with FLCE_FLAG_DW_OVERWRITE).
+template <int NBUF, bool HALF, typename D>
 __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtensorMap* tmC, uint8_t* stg,
                                                 int mrow, int n, int ylimit, int yoff, uint32_t taddr,
-                                                int q, int lane, float cb, const float* rsc,
+                                                int q, int lane, float cb, const float* rsc, bool store,
                                                 uint32_t& epi_it) {
   const int H = (int)a.H;
   const int y = mrow + q * 32;
   if (y >= ylimit) return;  // this warp's 32 rows lie past the destination (warp-uniform)
   if (rsc != nullptr) cb *= rsc[y + lane];  // y + lane < ylimit = R (multiples of 32)
-  if (HALF) {
+  constexpr bool F32 = std::is_same<D, float>::value;
+  if (HALF || !F32) {
+    constexpr int BOX = F32 ? 16 : 32;  // columns per 64-byte box row
 #pragma unroll 1
     for (int cc = 0; cc < BN / 32; ++cc) {
       const int x = n * BN + cc * 32;
@@ -654,23 +659,35 @@ __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtenso
       uint32_t r[32];
       tmem_ld32(taddr + cc * 32, r);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (x + 16 * h >= H) break;  // warp-uniform
+      for (int h = 0; h < 32 / BOX; ++h) {
+        if (x + BOX * h >= H) break;  // warp-uniform
         uint8_t* buf = stg + (epi_it & 1u) * (EPI_BUF_BYTES / 2);
-        if (lane == 0) bulk_wait_read<1>();  // the reduce that last read this buffer is done
+        if (lane == 0) bulk_wait_read<1>();  // the op that last read this buffer is done
         __syncwarp();
         uint8_t* row = buf + lane * 64;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int c = 16 * h + 4 * j;
-          float4 v = make_float4(cb * __uint_as_float(r[c + 0]), cb * __uint_as_float(r[c + 1]),
-                                 cb * __uint_as_float(r[c + 2]), cb * __uint_as_float(r[c + 3]));
-          *(float4*)(row + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+          uint4 v;
+          if constexpr (F32) {
+            const int c = 16 * h + 4 * j;
+            v = make_uint4(__float_as_uint(cb * __uint_as_float(r[c + 0])),
+                           __float_as_uint(cb * __uint_as_float(r[c + 1])),
+                           __float_as_uint(cb * __uint_as_float(r[c + 2])),
+                           __float_as_uint(cb * __uint_as_float(r[c + 3])));
+          } else {
+            const int c = 8 * j;
+            v = make_uint4(pack2<D>(cb * __uint_as_float(r[c + 0]), cb * __uint_as_float(r[c + 1])),
+                           pack2<D>(cb * __uint_as_float(r[c + 2]), cb * __uint_as_float(r[c + 3])),
+                           pack2<D>(cb * __uint_as_float(r[c + 4]), cb * __uint_as_float(r[c + 5])),
+                           pack2<D>(cb * __uint_as_float(r[c + 6]), cb * __uint_as_float(r[c + 7])));
+          }
+          *(uint4*)(row + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_2d(tmC, smem_u32(buf), x + 16 * h, y + yoff);
+          if (store) tma_store_2d(tmC, smem_u32(buf), x + BOX * h, y + yoff);
+          else tma_reduce_add_2d(tmC, smem_u32(buf), x + BOX * h, y + yoff);
           bulk_commit();
         }
         ++epi_it;
@@ -697,44 +714,11 @@ __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtenso
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_reduce_add_2d(tmC, smem_u32(buf), x, y + yoff);
+      if (store) tma_store_2d(tmC, smem_u32(buf), x, y + yoff);
+      else tma_reduce_add_2d(tmC, smem_u32(buf), x, y + yoff);
       bulk_commit();
     }
     ++epi_it;
-  }
-}
-
-// Same-dtype dW (bf16/fp16 destination): dW[v, h] = round(dW[v, h] + cbar * acc) by the
-// thread that owns row v of the tile (one read-modify-write per element per launch, by the
-// owning pair: deterministic). 8 columns per 16-byte access.
-template <typename T>
-__device__ __forceinline__ void epilogue_dw_same_dtype(const CallArgs& a, int mrow, int x0, uint32_t taddr,
-                                                       int q, int lane, float cb) {
-  const int H = (int)a.H;
-  const int v = mrow + q * 32 + lane;
-  const bool valid = v < (int)a.V;
-  T* wrow = (T*)a.dW + (int64_t)(valid ? v : 0) * a.H;
-#pragma unroll 1
-  for (int cc = 0; cc < BN / 32; ++cc) {
-    const int h0 = x0 + cc * 32;
-    if (h0 >= H) break;  // warp-uniform
-    uint32_t r[32];
-    tmem_ld32(taddr + cc * 32, r);
-    if (!valid) continue;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      if (h0 + g * 8 < H) {
-        uint4* p = (uint4*)(wrow + h0 + g * 8);
-        uint4 u = *p;
-        T* t = (T*)&u;
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          o[j] = pack2<T>(to_f<T>(t[2 * j]) + cb * __uint_as_float(r[g * 8 + 2 * j]),
-                          to_f<T>(t[2 * j + 1]) + cb * __uint_as_float(r[g * 8 + 2 * j + 1]));
-        *p = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
   }
 }
 
@@ -918,6 +902,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int j = (warp - 2) >> 2;
     const float cb = MODE == FWD ? 0.0f : a.w.ctrl->cbar;
     const float* rsc = (MODE == DX && a.ref_mode && a.w.ctrl->fb == 0) ? a.w.rsc : nullptr;
+    // dW overwrite: the first chunk of the call stores its tiles, later chunks add
+    const bool ovw = MODE == DW && (a.flags & FLCE_FLAG_DW_OVERWRITE) && chunk == 0;
     uint8_t* stg = epi_stage + (warp - 2) * NBUF * EPI_BUF_BYTES;
     uint32_t epi_it = 0;
     int it = 0;
@@ -941,10 +927,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         else if (MODE == FWD)
           epilogue_fwd<T, NBUF>(a, &tmC, stg, row0, rows, mrow, nsub, taddr, q, lane, epi_it);
         else if (MODE == DW && a.dW_dt != FLCE_F32)
-          epilogue_dw_same_dtype<T>(a, mrow, nsub * BN, taddr, q, lane, cb);
+          epilogue_reduce<NBUF, (NB == 2), T>(a, &tmC, stg, mrow, nsub, (int)a.V, 0, taddr, q, lane, cb,
+                                              nullptr, ovw, epi_it);
         else
-          epilogue_reduce<NBUF, (NB == 2)>(a, &tmC, stg, mrow, nsub, MODE == DX ? (int)a.R : (int)a.V,
-                                MODE == DX ? (split >> 1) * (int)a.R : 0, taddr, q, lane, cb, rsc, epi_it);
+          epilogue_reduce<NBUF, (NB == 2), float>(a, &tmC, stg, mrow, nsub, MODE == DX ? (int)a.R : (int)a.V,
+                                                  MODE == DX ? (split >> 1) * (int)a.R : 0, taddr, q, lane,
+                                                  cb, rsc, MODE == DW && ovw, epi_it);
       }
       tc_fence_before();
       __syncwarp();
@@ -1114,14 +1102,15 @@ cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 64)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 64)) return cudaErrorInvalidValue;
-  CUtensorMap C;  // fp32 dW for TMA reduce-add; unused (a copy of A) for same-dtype dW
+  CUtensorMap C;  // dW for the TMA reduce-add (or store) of the epilogue
   const bool wide = a.R >= tc::DW_WIDE_MIN_ROWS;
   if (a.dW_dt == FLCE_F32) {
     if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, wide ? 16 : 32, 32,
                       wide ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-  } else {
-    C = A;
+  } else {  // same-dtype dW: 32-column boxes of 16-bit values, added (or stored) by the TMA unit
+    if (!tc::make_map(&C, a.dW, a.dW_dt, a.H, a.V, a.H * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
   }
   const int64_t vt = (a.V + 255) / 256, ht = (a.H + 255) / 256;
   if (wide) return tc::launch_mode<tc::DW, 2>(a, chunk, s, A, B, C, vt * ((ht + 1) / 2));

@@ -22,12 +22,13 @@ REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 FLAG_FORCE_SIMT = 0x1
 FLAG_NO_ROW_REF = 0x2
+FLAG_DW_OVERWRITE = 0x4
 FLAG_DEBUG_STALL = 0x100
 EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_fwd_bwd_noalloc",
             "flce_get_status",
             "flce_profile_create", "flce_profile_reset", "flce_profile_destroy",
             "flce_profile_read", "flce_last_cuda_error", "flce_status_string", "flce_abi_version",
-            "flce_jsd_workspace_size", "flce_fused_linear_jsd")
+            "flce_jsd_workspace_size", "flce_fused_linear_jsd", "flce_scale_by")
 STAGES = ("prologue", "gather", "fwd", "finalize", "gpass", "dx", "dw", "reduce")
 
 
@@ -94,6 +95,9 @@ def load(path: str | None = None):
     lib.flce_abi_version.restype = ctypes.c_int32
     lib.flce_last_cuda_error.restype = ctypes.c_char_p
     lib.flce_last_cuda_error.argtypes = []
+    lib.flce_scale_by.restype = ctypes.c_int32
+    lib.flce_scale_by.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
+                                  ctypes.c_void_p]
     lib.flce_jsd_workspace_size.restype = ctypes.c_size_t
     lib.flce_jsd_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int32, ctypes.c_size_t]
     lib.flce_fused_linear_jsd.restype = ctypes.c_int32
@@ -316,6 +320,17 @@ def fused_linear_jsd(Xs, Ws, Xt, Wt, labels=None, *, beta=0.5, temperature=1.0, 
         o["status_code"] = int(lib.flce_get_status(ctypes.c_void_p(_ptr(o["status"])), None,
                                                    ctypes.c_void_p(s.cuda_stream)))
     return o
+
+
+def scale_by(x, g, stream=None):
+    """x *= g in place (x: contiguous CUDA tensor, fp32/bf16/fp16; g: one-element fp32 CUDA
+    tensor), skipped on the device when g == 1."""
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    rc = load().flce_scale_by(ctypes.c_void_p(x.data_ptr()), x.numel(), DTYPES[x.dtype],
+                              ctypes.c_void_p(g.data_ptr()), ctypes.c_void_p(s.cuda_stream))
+    if rc != FLCE_OK:
+        raise FlceError(rc, "flce_scale_by")
+    return x
 
 
 def raw_call(args: FlceArgs, stream_handle: int) -> int:

@@ -38,12 +38,14 @@ def fused_linear_cross_entropy_op(X: torch.Tensor, W: torch.Tensor, targets: tor
     """(loss, z_loss, acc, lse, pred, dX, dW, dbias); dX/dW/dbias are empty when not wanted."""
     V, H = W.shape
     dW_dtype = torch.float32 if dW_fp32 else W.dtype
-    dW = torch.zeros(V, H, dtype=dW_dtype, device=X.device) if want_dW else None
-    db = torch.zeros(V, dtype=dW_dtype, device=X.device) if (want_dW and bias is not None) else None
+    # fresh gradient buffers, written (not accumulated) by the op: no zero fill
+    dW = torch.empty(V, H, dtype=dW_dtype, device=X.device) if want_dW else None
+    db = torch.empty(V, dtype=dW_dtype, device=X.device) if (want_dW and bias is not None) else None
     out = flce.fwd_bwd(X.contiguous(), W.contiguous(), targets.contiguous(),
                        None if bias is None else bias.contiguous(), ignore_index=ignore_index,
                        reduction=reduction, z_loss_scale=z_loss_scale, grad_out=grad_out,
-                       want_dX=want_dX, want_dW=want_dW, dW=dW, dbias=db, check=False)
+                       want_dX=want_dX, want_dW=want_dW, dW=dW, dbias=db, check=False,
+                       flags=flce.FLAG_DW_OVERWRITE)
     empty = X.new_empty(0)
     return (out["loss"], out["z_loss"], out["acc"], out["lse"], out["pred"],
             out["dX"] if want_dX else empty, dW if want_dW else empty.float(),
@@ -104,11 +106,22 @@ class FusedLinearCrossEntropy(torch.autograd.Function):
             dX, dW, db = ctx.saved_tensors
             if ctx.reduction == "none":
                 dX = dX * g_loss.to(dX.dtype)[:, None] if need_x else dX
-            else:
+            elif torch.compiler.is_compiling():
+                # traced backward (torch.compile): plain tensor ops
                 g = g_loss.reshape(())
                 dX = dX * g.to(dX.dtype) if need_x else dX
                 dW = dW * g.to(dW.dtype) if need_w else dW
                 db = db * g.to(db.dtype) if (need_w and ctx.has_bias) else db
+            else:
+                # eager: scale the op's own gradient buffers in place on the device; nothing
+                # is done (no pass over dW) when the upstream gradient is exactly 1
+                g = g_loss.reshape(1).float().contiguous()
+                if need_x:
+                    flce.scale_by(dX, g)
+                if need_w:
+                    flce.scale_by(dW, g)
+                    if ctx.has_bias:
+                        flce.scale_by(db, g)
         return (dX if need_x else None, dW if need_w else None, None,
                 db if (need_w and ctx.has_bias) else None, None, None, None, None)
 

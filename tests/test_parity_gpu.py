@@ -177,7 +177,8 @@ def test_dW_accumulates_into_destination():
 def test_same_dtype_dW_accumulation(dt, path):
     """dW and dbias accumulated in the input dtype ("Reduce FLCE weight-gradient allocation
     overhead across FP16, BF16, and FP32", support matrix: same-dtype FP16/BF16 direct
-    accumulation). Each call rounds dW_init + G^T X to the input dtype once."""
+    accumulation). The tensor-core path adds G^T X, rounded to the input dtype, into dW in
+    the L2 (a second rounding); the SIMT path rounds dW_init + G^T X once."""
     sp = I.spec("frozen_head", BT=300, H=136, V=2100, dtype=dt, w_std=0.15, bias_std=0.3,
                 n_ignored=60, reduction="sum", grad_out=None, want_dW=True, z=1e-3)
     inp = I.generate(sp, seed=12)
@@ -254,3 +255,57 @@ def test_wide_dw_tile_ragged(H):
     assert flce.chunk_rows(sp["BT"], H, sp["V"], torch.bfloat16,
                            flce.workspace_size(sp["BT"], H, sp["V"], torch.bfloat16, 0)) >= 4096
     compare_full(run_gpu(inp, sp), run_oracle(inp, sp), inp, sp)
+
+
+@pytest.mark.parametrize("path", ["tc", "simt"])
+@pytest.mark.parametrize("dw_dt", ["f32", "same"])
+@pytest.mark.parametrize("labelled", ["some", "none"])
+def test_dw_overwrite(path, dw_dt, labelled):
+    """FLCE_FLAG_DW_OVERWRITE: dW and dbias (pre-filled with NaN) receive exactly this call's
+    gradient over several chunks (the first chunk stores, later ones add); with no labelled
+    row they come back zero."""
+    sp = I.spec("frozen_head", BT=700, H=136, V=1500, w_std=0.15, bias_std=0.3, n_ignored=70,
+                reduction="sum", grad_out=None, want_dW=True, z=1e-3,
+                ignore="random" if labelled == "some" else "all")
+    inp = I.generate(sp, seed=23)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    adt = torch.float32 if dw_dt == "f32" else torch.bfloat16
+    dW = torch.full((sp["V"], sp["H"]), float("nan"), dtype=adt, device="cuda")
+    db = torch.full((sp["V"],), float("nan"), dtype=adt, device="cuda")
+    budget = flce.workspace_size(128, sp["H"], sp["V"], torch.bfloat16, 0) + 16 * sp["BT"] + 4096
+    flags = flce.FLAG_DW_OVERWRITE | (flce.FLAG_FORCE_SIMT if path == "simt" else 0)
+    out = flce.fwd_bwd(d["X"], d["W"], d["targets"], d["bias"], reduction="sum", z_loss_scale=sp["z"],
+                       dW=dW, dbias=db, budget_bytes=budget, flags=flags)
+    assert out["status_code"] == flce.FLCE_OK
+    o = run_oracle(inp, sp)
+    gw = dW.float().cpu().numpy()
+    gb = db.float().cpu().numpy()
+    if labelled == "none":
+        assert np.all(gw == 0) and np.all(gb == 0)
+    else:
+        assert np.all(np.isfinite(gw)) and np.all(np.isfinite(gb))
+        assert rel_fro(gw, o["dW"]) <= TOL["bf16"]["grad"]
+        assert rel_fro(gb, o["dbias"]) <= TOL["bf16"]["grad"]
+
+
+def test_overwrite_row_reference_wide_tile():
+    """The same flag on the row-reference, 256x512-tile dW path (no bias, >= 4096 rows)."""
+    sp = I.spec("llama1b", BT=4300, H=136, V=1300, w_std=0.2, ignore="random", n_ignored=100)
+    inp = I.generate(sp, seed=24)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    for adt in (torch.float32, torch.bfloat16):
+        dW = torch.full((sp["V"], sp["H"]), float("nan"), dtype=adt, device="cuda")
+        out = flce.fwd_bwd(d["X"], d["W"], d["targets"], None, dW=dW, flags=flce.FLAG_DW_OVERWRITE)
+        assert out["status_code"] == flce.FLCE_OK
+        assert rel_fro(dW.float().cpu().numpy(), run_oracle(inp, sp)["dW"]) <= TOL["bf16"]["grad"]
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16, torch.float16])
+def test_scale_by(dt):
+    """flce_scale_by: x *= g on the device; bit-identical no-op when g == 1."""
+    x = (torch.randn(100003, generator=torch.Generator().manual_seed(3)) * 3).to(dt).cuda()
+    ref = x.clone()
+    flce.scale_by(x, torch.ones(1, device="cuda"))
+    assert torch.equal(x, ref)
+    flce.scale_by(x, torch.full((1,), 0.375, device="cuda"))
+    assert torch.equal(x, (ref.float() * 0.375).to(dt))

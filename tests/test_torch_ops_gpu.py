@@ -77,3 +77,20 @@ def test_compile_matches_eager():
         res.append((loss.detach().float().cpu(), a.grad.float().cpu(), w.grad.float().cpu()))
     for e, c in zip(res[0], res[1]):
         assert torch.equal(e, c)
+
+
+def test_autograd_upstream_gradient_scales():
+    """(2.5 * loss).backward(): the gradients computed in the forward are scaled on the
+    device by the upstream gradient (and left untouched when it is 1)."""
+    from linear_cross_entropy_logits_gb300.torch_ops import fused_linear_cross_entropy
+    sp = I.spec("llama1b", BT=300, H=192, V=3000, w_std=0.2, ignore="random", n_ignored=40)
+    inp = I.generate(sp, seed=31)
+    o = run_oracle(inp, sp)
+    for scale in (1.0, 2.5):
+        X = inp["X"].cuda().requires_grad_(True)
+        W = inp["W"].cuda().requires_grad_(True)
+        loss = fused_linear_cross_entropy(X, W, inp["targets"].cuda(), accum_dtype=torch.float32)
+        (scale * loss).backward()
+        assert rel_fro(X.grad.float().cpu().numpy(), scale * o["dX"]) <= TOL["bf16"]["grad"]
+        assert rel_fro(W.grad.float().cpu().numpy(), scale * o["dW"]) <= TOL["bf16"]["grad"]
+
