@@ -386,11 +386,26 @@ __device__ __forceinline__ TileSpace tile_space(const CallArgs& a, int rows) {
 }
 // FWD walks m fastest (the pairs in flight share W tiles); DX and DW walk n fastest (the
 // pairs in flight share the slab rows / columns).
+#ifndef FLCE_FWD_MGROUP
+#define FLCE_FWD_MGROUP 16
+#endif
+// The forward walks its row tiles in groups of FWD_MGROUP (4096 rows): within a group m
+// fastest, then n; so the gathered rows a wave needs (a group's Xc, 33 MB) stay in L2
+// while W streams, at the price of reading W once per group.
+constexpr int FWD_MGROUP = FLCE_FWD_MGROUP;
 template <int MODE>
 __device__ __forceinline__ void tile_coords(const TileSpace& ts, int tile, int& m, int& n) {
   if (MODE == FWD) {
-    m = tile % ts.mt;
-    n = tile / ts.mt;
+    if (FWD_MGROUP > 0 && ts.mt > FWD_MGROUP) {
+      const int per_group = FWD_MGROUP * ts.nt;
+      const int g = tile / per_group, t = tile - g * per_group;
+      const int gm = min(FWD_MGROUP, ts.mt - g * FWD_MGROUP);  // rows tiles in this group
+      m = g * FWD_MGROUP + t % gm;
+      n = t / gm;
+    } else {
+      m = tile % ts.mt;
+      n = tile / ts.mt;
+    }
   } else {
     n = tile % ts.nt;
     m = tile / ts.nt;
