@@ -70,9 +70,12 @@ __host__ __device__ constexpr int stage_bytes() {
 }
 // Pipeline depth: 192 KB of stages (6 x 32 KB or 4 x 48 KB) next to 32 KB of epilogue
 // staging.
+#ifndef FLCE_WIDE_STAGES
+#define FLCE_WIDE_STAGES 4
+#endif
 template <int NB>
 __host__ __device__ constexpr int stages_of() {
-  return NB == 1 ? 6 : 4;
+  return NB == 1 ? 6 : FLCE_WIDE_STAGES;
 }
 template <int NB>
 __host__ __device__ constexpr int nacc_of() {      // TMEM accumulators (512 columns in all)
@@ -92,15 +95,32 @@ constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tfull[2], tem
 // (FWD: the exp slab) or reduce-adds (DX/DW: the L2 performs dst += tile; no register
 // read-modify-write).
 constexpr int EPI_BUF_BYTES = 32 * 128;
-constexpr int EPI_BYTES = 8 * EPI_BUF_BYTES;       // 32 KB
+constexpr int EPI_BYTES_MIN = 8 * EPI_BUF_BYTES;   // 32 KB
+// Epilogue staging of a tile shape: 32 KB, or for the wide tile whatever the stages leave
+// (in 2 KB buffers per warp, a multiple of 16 KB).
+template <int NB>
+__host__ __device__ constexpr int epi_bytes_of() {
+  return NB == 1 ? EPI_BYTES_MIN
+                 : ((232448 - 1536 - stages_of<NB>() * stage_bytes<NB>()) / 16384) * 16384;
+}
+template <int NB>
+__host__ __device__ constexpr int epi_warp_bytes_of() {  // staging per epilogue warp
+  return epi_bytes_of<NB>() / (4 * NB);
+}
+template <int NB>
+__host__ __device__ constexpr int half_bufs_of() {  // 2 KB staging buffers per epilogue warp
+  return epi_warp_bytes_of<NB>() / 2048;
+}
 template <int NB>
 __host__ __device__ constexpr int epi_nbuf_of() {
   return 8 / epi_warps_of<NB>();
 }
 template <int NB>
 constexpr int smem_bytes() {
-  return stages_of<NB>() * stage_bytes<NB>() + EPI_BYTES + 1024 + 512;
+  return stages_of<NB>() * stage_bytes<NB>() + epi_bytes_of<NB>() + 1024 + 512;
 }
+static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448, "shared memory per CTA");
+static_assert(half_bufs_of<1>() >= 2 && half_bufs_of<2>() >= 2, "epilogue staging buffers");
 
 __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -655,7 +675,7 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
 // 16-bit destination D (same-dtype dW: the L2 adds in D), the map's box accordingly
 // {16, 32} or {32, 32}. STORE: the box overwrites dst instead of adding to it (the first
 // chunk of a call with FLCE_FLAG_DW_OVERWRITE).
-template <int NBUF, bool HALF, typename D>
+template <int NBUF, bool HALF, typename D, int HB>
 __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtensorMap* tmC, uint8_t* stg,
                                                 int mrow, int n, int ylimit, int yoff, uint32_t taddr,
                                                 int q, int lane, float cb, const float* rsc, bool store,
@@ -676,8 +696,8 @@ __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtenso
 #pragma unroll
       for (int h = 0; h < 32 / BOX; ++h) {
         if (x + BOX * h >= H) break;  // warp-uniform
-        uint8_t* buf = stg + (epi_it & 1u) * (EPI_BUF_BYTES / 2);
-        if (lane == 0) bulk_wait_read<1>();  // the op that last read this buffer is done
+        uint8_t* buf = stg + (epi_it % HB) * (EPI_BUF_BYTES / 2);
+        if (lane == 0) bulk_wait_read<HB - 1>();  // the op that last read this buffer is done
         __syncwarp();
         uint8_t* row = buf + lane * 64;
 #pragma unroll
@@ -762,7 +782,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* epi_stage = smem + STAGES * SBYTES;
-  uint64_t* bars = (uint64_t*)(smem + STAGES * SBYTES + EPI_BYTES);
+  uint64_t* bars = (uint64_t*)(smem + STAGES * SBYTES + epi_bytes_of<NB>());
   uint32_t* tmem_slot = (uint32_t*)(bars + NUM_BARS);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   int* copies = (int*)(tmem_slot + 2);  // per stage: phases this CTA's producer filled / armed
@@ -919,7 +939,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float* rsc = (MODE == DX && a.ref_mode && a.w.ctrl->fb == 0) ? a.w.rsc : nullptr;
     // dW overwrite: the first chunk of the call stores its tiles, later chunks add
     const bool ovw = MODE == DW && (a.flags & FLCE_FLAG_DW_OVERWRITE) && chunk == 0;
-    uint8_t* stg = epi_stage + (warp - 2) * NBUF * EPI_BUF_BYTES;
+    uint8_t* stg = epi_stage + (warp - 2) * epi_warp_bytes_of<NB>();
     uint32_t epi_it = 0;
     int it = 0;
     Items<MODE> items(pair, npairs, ntiles, ts.nkb);
@@ -942,10 +962,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         else if (MODE == FWD)
           epilogue_fwd<T, NBUF>(a, &tmC, stg, row0, rows, mrow, nsub, taddr, q, lane, epi_it);
         else if (MODE == DW && a.dW_dt != FLCE_F32)
-          epilogue_reduce<NBUF, (NB == 2), T>(a, &tmC, stg, mrow, nsub, (int)a.V, 0, taddr, q, lane, cb,
+          epilogue_reduce<NBUF, (NB == 2), T, half_bufs_of<NB>()>(a, &tmC, stg, mrow, nsub, (int)a.V, 0, taddr, q, lane, cb,
                                               nullptr, ovw, epi_it);
         else
-          epilogue_reduce<NBUF, (NB == 2), float>(a, &tmC, stg, mrow, nsub, MODE == DX ? (int)a.R : (int)a.V,
+          epilogue_reduce<NBUF, (NB == 2), float, half_bufs_of<NB>()>(a, &tmC, stg, mrow, nsub, MODE == DX ? (int)a.R : (int)a.V,
                                                   MODE == DX ? (split >> 1) * (int)a.R : 0, taddr, q, lane,
                                                   cb, rsc, MODE == DW && ovw, epi_it);
       }
