@@ -165,3 +165,36 @@ def test_jsd_distill_full_size_sampled():
     vs = np.sort(rng.choice(V, size=256, replace=False))
     got = g2["dW"][torch.from_numpy(vs).cuda()].cpu().numpy()
     assert rel_fro(got, o2["dW"][vs]) <= TOL["bf16"]["grad"]
+
+
+@pytest.mark.parametrize("beta,T", [(1e-4, 1.0), (0.9999, 1.0), (0.5, 0.25), (0.5, 8.0)])
+def test_jsd_extreme_beta_and_temperature(beta, T):
+    """beta next to its KL end points (the general branch with near-degenerate mixtures) and
+    a sharp / flat temperature."""
+    _check("bf16", beta, T, "mean", "tc", BT=260, Hs=136, Ht=200, V=1300, seed=66)
+
+
+def test_jsd_fp16_inputs():
+    _check("f16", 0.5, 1.0, "sum", "tc", BT=260, Hs=136, Ht=200, V=1300, seed=67)
+
+
+@pytest.mark.parametrize("dw", ["same", "overwrite"])
+def test_jsd_dw_modes(dw):
+    """Student dW accumulated in bf16 (same dtype), or overwritten (FLCE_FLAG_DW_OVERWRITE,
+    destination pre-filled with NaN) over several chunks."""
+    Xs, Ws, Xt, Wt, labels, _ = _problem(700, 128, 96, 2000, "bf16", 68, 50)
+    adt = torch.bfloat16 if dw == "same" else torch.float32
+    init = torch.zeros(2000, 128, dtype=adt, device="cuda") if dw == "same" else \
+        torch.full((2000, 128), float("nan"), dtype=adt, device="cuda")
+    budget = flce.jsd_workspace_size(128, 128, 96, 2000, torch.bfloat16, 0) + 16 * 700 + 4096
+    out = flce.fused_linear_jsd(Xs.cuda(), Ws.cuda(), Xt.cuda(), Wt.cuda(), labels.cuda(), beta=0.5,
+                                reduction="sum", dW=init, budget_bytes=budget,
+                                flags=flce.FLAG_DW_OVERWRITE if dw == "overwrite" else 0)
+    assert out["status_code"] == flce.FLCE_OK
+    f = I.to_numpy_exact
+    o = jo.jsd_oracle(f(Xs), f(Ws), f(Xt), f(Wt), labels.numpy(), beta=0.5, reduction="sum")
+    assert rel_fro(init.float().cpu().numpy(), o["dW"]) <= 1e-2
+
+
+def test_jsd_reverse_kl_sum_tc():
+    _check("bf16", 1.0, 1.3, "sum", "tc", BT=333, Hs=200, Ht=136, V=2600, seed=69)
