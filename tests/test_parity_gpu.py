@@ -309,3 +309,16 @@ def test_scale_by(dt):
     assert torch.equal(x, ref)
     flce.scale_by(x, torch.full((1,), 0.375, device="cuda"))
     assert torch.equal(x, (ref.float() * 0.375).to(dt))
+
+
+@pytest.mark.parametrize("BT,n_ignored", [(4864, 0), (6400, 0)])
+def test_dx_three_and_four_way_k_splits(BT, n_ignored):
+    """On 76 pairs, 19 dX pair tiles (4864 rows, H <= 512) take four K splits and 25 tiles
+    (6400 rows) three: splits 0-1 add into one zeroed fp32 buffer, 2-3 into a second, so
+    the result is bit-identical run to run, and it matches the oracle."""
+    sp = I.spec("llama1b", BT=BT, H=256, V=2000, w_std=0.2, ignore="none")
+    inp = I.generate(sp, seed=25)
+    a = run_gpu(inp, sp)
+    b = run_gpu(inp, sp)
+    assert np.array_equal(a["dX"], b["dX"]) and np.array_equal(a["dW"], b["dW"])
+    compare_full(a, run_oracle(inp, sp), inp, sp)
