@@ -35,7 +35,7 @@ c_i is the upstream gradient of the returned loss with respect to loss_i: ``g / 
 ``mean`` (N = number of labelled rows), ``g`` for ``sum``, ``g_i`` for ``none``, where g
 is the scalar upstream gradient (1 when not given) and g_i the per-token one.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * z-loss is ``z * lse^2``, added to the loss and also reported on its own.
   * ``mean`` divides by the number of labelled rows; with none labelled the loss is 0
     and every gradient is 0.
