@@ -1081,10 +1081,9 @@ cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtenso
     if (n <= 0) return cudaErrorInvalidConfiguration;
     if (dev >= 0 && dev < 64) max_pairs[dev] = n;
     else return cudaErrorInvalidDevice;
-  } else {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
   }
+  // (the shared-memory attribute, set once per device above, persists: later launches,
+  // including ones captured into a CUDA graph, enqueue the kernel only)
   const int64_t pairs = pair_tiles_max < max_pairs[dev] ? pair_tiles_max : max_pairs[dev];
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * (unsigned)pairs, 1, 1);
