@@ -228,7 +228,8 @@ typedef struct flce_jsd_args {
  * plumbing for the autograd binding. */
 FLCE_API int32_t flce_scale_by(void* x, int64_t n, int32_t dtype, const float* g, void* stream);
 
-/* Workspace bytes for the distillation op within budget_bytes (0 means 3 GiB); 0 when
+/* Workspace bytes for the distillation op within budget_bytes (0 means 6 GiB: its workspace
+ * holds two logit-sized slabs, one per head); 0 when
  * not even one 128-row chunk fits or on invalid arguments. */
 FLCE_API size_t flce_jsd_workspace_size(int64_t BT, int64_t Hs, int64_t Ht, int64_t V,
                                         int32_t in_dtype, size_t budget_bytes);

@@ -455,7 +455,7 @@ extern "C" size_t flce_jsd_workspace_size(int64_t BT, int64_t Hs, int64_t Ht, in
                                           size_t budget_bytes) {
   if (BT <= 0 || Hs <= 0 || Ht <= 0 || V <= 0) return 0;
   if (in_dtype != FLCE_F32 && in_dtype != FLCE_BF16 && in_dtype != FLCE_F16) return 0;
-  const int64_t R = jsd_rows_for_bytes(BT, Hs, Ht, V, in_dtype, budget_bytes ? budget_bytes : DEFAULT_BUDGET);
+  const int64_t R = jsd_rows_for_bytes(BT, Hs, Ht, V, in_dtype, budget_bytes ? budget_bytes : 2 * DEFAULT_BUDGET);
   if (R <= 0) return 0;
   JsdPlan p;
   if (!jsd_layout(BT, Hs, Ht, V, in_dtype, R, &p)) return 0;
