@@ -1,12 +1,15 @@
-"""Forward outputs of every row at the workloads' full sizes, against the float64 oracle.
+"""Every output at the workloads' full sizes, against the float64 oracle.
 
-The oracle's row-blocked forward (logits in float64 over the whole vocabulary, then the
-per-row lse, loss and argmax) runs on every labelled row of the Llama-3.2-1B,
+The oracle's row-blocked evaluation (logits in float64 over the whole vocabulary, the
+per-row lse, loss and argmax, the gradient of the logits, dX = dS W and dW = dS^T X
+accumulated over the row blocks) runs on every labelled row of the Llama-3.2-1B,
 Llama-3.1-8B and frozen-head workloads, in the launch configuration the benchmark times
-(default workspace, gradients on; reduction "none" so that every per-token loss is
-returned). Every row is compared: lse and per-token loss within the bf16 tolerance (2e-3
-relative), the prediction bit exact outside the fp32 tie band, and the ignored-row outputs
-bit exact. The large-vocab workload (92 TFLOP of float64 forward) stays on sampled rows.
+(default workspace, gradients on; reduction "none" with the workload's per-token upstream
+gradient, or ones, so that every per-token loss is returned). Compared: lse and per-token
+loss of every row within the bf16 tolerance (2e-3 relative), the prediction bit exact
+outside the fp32 tie band, the ignored-row outputs bit exact, and the whole dX and dW
+within the 1e-2 relative-Frobenius tolerance. The large-vocab workload (3 x 92 TFLOP of
+float64) stays on sampled rows and vocabulary entries.
 """
 
 import numpy as np
@@ -17,7 +20,7 @@ from linear_cross_entropy_logits_gb300 import build as B
 from linear_cross_entropy_logits_gb300 import flce
 from linear_cross_entropy_logits_gb300 import inputs as I
 from oracle import flce_oracle as orc
-from parity_util import TOL, pred_ok
+from parity_util import TOL, pred_ok, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +36,7 @@ def _lib():
 
 
 @pytest.mark.parametrize("base,ov", CONFIGS, ids=[c[0] for c in CONFIGS])
-def test_every_row_forward(base, ov):
+def test_every_output_full_size(base, ov):
     sp = I.spec(base, **ov)
     inp = I.generate(sp, seed=0)
     d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
@@ -47,6 +50,9 @@ def test_every_row_forward(base, ov):
     lse = out["lse"].cpu().numpy()
     loss = out["loss"].cpu().numpy()
     pred = out["pred"].cpu().numpy()
+    dX = out["dX"].float().cpu().numpy()
+    dW_gpu = dW.cpu().numpy() if dW is not None else None
+    g_tok = go.cpu().numpy().astype(np.float64)
     del out, dW
 
     t = inp["targets"].numpy()
@@ -57,15 +63,29 @@ def test_every_row_forward(base, ov):
     b = I.to_numpy_exact(inp["bias"])
     tol = TOL[sp["dtype"]]["loss"]
     rows = np.nonzero(mask)[0]
+    assert np.all(dX[~mask] == 0)
+    c = orc.grad_scales(mask, "none", g_tok)
+    dX_ref = np.zeros((BT, H))
+    dW_ref = np.zeros((V, H)) if dW_gpu is not None else None
     worst_lse = worst_loss = 0.0
     for k0 in range(0, rows.size, 1024):
         r = rows[k0:k0 + 1024]
         s = orc.logits_rows(X[r], W64, b)
-        o_lse, o_loss, _, o_pred, _, _ = orc.rows_forward(s, t[r], z)
+        o_lse, o_loss, _, o_pred, _, p = orc.rows_forward(s, t[r], z)
         del s
+        dS = orc.rows_grad_logits(p, t[r], o_lse, c[r], z)
+        del p
+        dX_ref[r] = dS @ W64
+        if dW_ref is not None:
+            dW_ref += dS.T @ np.asarray(X[r], np.float64)
+        del dS
         worst_lse = max(worst_lse, float(np.max(np.abs(lse[r] - o_lse) / np.abs(o_lse))))
         worst_loss = max(worst_loss, float(np.max(np.abs(loss[r] - o_loss) / np.maximum(np.abs(o_loss), 1e-3))))
         ok, where = pred_ok(pred[r], o_pred, X, W64, b, r, mask[r])
         assert ok, f"argmax mismatch outside the tie band at row {where}"
     assert worst_lse <= tol, f"lse rel err {worst_lse}"
     assert worst_loss <= tol, f"per-token loss rel err {worst_loss}"
+    gtol = TOL[sp["dtype"]]["grad"]
+    assert rel_fro(dX, dX_ref) <= gtol, f"dX rel-Frobenius {rel_fro(dX, dX_ref)}"
+    if dW_ref is not None:
+        assert rel_fro(dW_gpu, dW_ref) <= gtol, f"dW rel-Frobenius {rel_fro(dW_gpu, dW_ref)}"
