@@ -99,10 +99,13 @@ typedef enum flce_stage {
   FLCE_STAGE_GATHER = 1,   /* gather of the chunk's labelled rows of X                  */
   FLCE_STAGE_FWD = 2,      /* logits GEMM with online max / sum-exp / argmax epilogue   */
   FLCE_STAGE_FINALIZE = 3, /* per-row merge: lse, loss, prediction, gradient multipliers */
-  FLCE_STAGE_GPASS = 4,    /* gradient of the logits formed in place (and dbias)        */
+  FLCE_STAGE_GPASS = 4,    /* gradient of the logits: formed in place (and dbias), or in
+                              the row-reference form the Xc row scale plus the per-tile
+                              redo launches gated on the chunk's window flag             */
   FLCE_STAGE_DX = 5,       /* dX GEMM                                                   */
   FLCE_STAGE_DW = 6,       /* dW GEMM (accumulating)                                    */
-  FLCE_STAGE_REDUCE = 7,   /* mean/sum reductions                                       */
+  FLCE_STAGE_REDUCE = 7,   /* mean/sum reductions (and, with FLCE_FLAG_DW_OVERWRITE,
+                              the zeroing of dW / dbias when no row is labelled)         */
   FLCE_STAGE_COUNT = 8
 } flce_stage;
 
@@ -129,8 +132,9 @@ typedef struct flce_args {
   int32_t want_dX;          /* 1: write dX                                               */
   int32_t want_dW;          /* 1: accumulate dW (and dbias when bias != NULL)            */
   int32_t dW_dtype;         /* flce_dtype of dW/dbias: FLCE_F32, or in_dtype itself
-                               (same-dtype accumulation: each call rounds dW + G^T X to
-                               in_dtype once); others give FLCE_ERR_UNSUPPORTED          */
+                               (same-dtype accumulation: the call's G^T X is rounded to
+                               in_dtype and added in in_dtype); others give
+                               FLCE_ERR_UNSUPPORTED                                      */
   uint32_t flags;           /* FLCE_FLAG_*                                               */
   /* outputs (NULL = not wanted, except loss) */
   float* loss;              /* [1] for mean/sum (reduced), [BT] for none (per token)     */
@@ -140,8 +144,10 @@ typedef struct flce_args {
   int64_t* pred;            /* [BT] per token argmax; -1 on ignored rows                 */
   int32_t* n_labelled;      /* [1] number of rows that entered the loss                  */
   void* dX;                 /* [BT,H] in_dtype, overwritten (zero on ignored rows)       */
-  void* dW;                 /* [V,H] dW_dtype, ACCUMULATED (+=); zero it for a fresh grad */
-  void* dbias;              /* [V] dW_dtype, ACCUMULATED; used when bias and want_dW     */
+  void* dW;                 /* [V,H] dW_dtype, ACCUMULATED (+=); zero it for a fresh grad,
+                               or pass FLCE_FLAG_DW_OVERWRITE                            */
+  void* dbias;              /* [V] dW_dtype, ACCUMULATED (or overwritten, as dW); used
+                               when bias and want_dW                                     */
   /* scratch and status */
   void* workspace;          /* device scratch of workspace_bytes, caller-owned           */
   size_t workspace_bytes;   /* >= flce_workspace_size(BT,H,V,in_dtype,0) or any size
@@ -205,11 +211,11 @@ typedef struct flce_jsd_args {
   int32_t want_dX;          /* 1: write dX_s                                             */
   int32_t want_dW;          /* 1: accumulate dW_s                                        */
   int32_t dW_dtype;         /* FLCE_F32 or in_dtype                                      */
-  uint32_t flags;           /* FLCE_FLAG_FORCE_SIMT                                      */
+  uint32_t flags;           /* FLCE_FLAG_FORCE_SIMT, FLCE_FLAG_DW_OVERWRITE              */
   float* loss;              /* [1] for mean/sum, [BT] for none                           */
   int32_t* n_labelled;      /* [1] or NULL                                               */
   void* dX;                 /* [BT,Hs] in_dtype, overwritten (zero on ignored rows)      */
-  void* dW;                 /* [V,Hs] dW_dtype, ACCUMULATED                              */
+  void* dW;                 /* [V,Hs] dW_dtype, ACCUMULATED (or overwritten, as above)   */
   void* workspace;          /* device scratch, 256-byte aligned                          */
   size_t workspace_bytes;   /* >= flce_jsd_workspace_size(...) for a chosen budget       */
   int32_t* status;          /* device int or NULL, as in flce_args                       */
