@@ -8,6 +8,7 @@
 // The number of chunks the host enqueues is cdiv(BT, R); chunks past the labelled count
 // (known only on the device) exit at once, so the transient memory is the workspace the
 // caller sized, whatever the labelled share.
+#include <atomic>
 #include <mutex>
 #include <string.h>
 #include <vector>
@@ -102,13 +103,17 @@ Work make_work(const Plan& p, void* ws, int32_t* user_status) {
 }
 
 int num_sms() {
-  static int cache[64] = {0};
+  // per-device cache; concurrent first calls may both query and store the same value
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 132;
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 132;
-  if (dev < 64) cache[dev] = n;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -38,6 +38,7 @@
 // pair reconciles the copies each CTA issued against the leader's barriers and waits
 // (bounded) for them and for the MMAs in flight.
 #include <cuda.h>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -1056,7 +1057,9 @@ cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtenso
                      const CUtensorMap& B, const CUtensorMap& C, int64_t pair_tiles_max) {
   auto kern = k_gemm_tc<MODE, T, NB>;
   constexpr int smem = smem_bytes<NB>();
-  static int max_pairs[64] = {0};
+  // per-device cache of the pairs that fit at once (the shared-memory attribute is set on
+  // the first launch of each device); concurrent first launches may both set and store it
+  static std::atomic<int> max_pairs[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1071,7 +1074,7 @@ cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtenso
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (dev < 0 || dev >= 64 || max_pairs[dev] == 0) {
+  if (dev < 0 || dev >= 64 || max_pairs[dev].load(std::memory_order_relaxed) == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(2 * (unsigned)(num_sms() / 2), 1, 1);
@@ -1079,12 +1082,13 @@ cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtenso
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaErrorInvalidConfiguration;
-    if (dev >= 0 && dev < 64) max_pairs[dev] = n;
+    if (dev >= 0 && dev < 64) max_pairs[dev].store(n, std::memory_order_relaxed);
     else return cudaErrorInvalidDevice;
   }
   // (the shared-memory attribute, set once per device above, persists: later launches,
   // including ones captured into a CUDA graph, enqueue the kernel only)
-  const int64_t pairs = pair_tiles_max < max_pairs[dev] ? pair_tiles_max : max_pairs[dev];
+  const int mp = max_pairs[dev].load(std::memory_order_relaxed);
+  const int64_t pairs = pair_tiles_max < mp ? pair_tiles_max : mp;
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * (unsigned)pairs, 1, 1);
   e = cudaLaunchKernelEx(&cfg, kern, A, B, C, a, chunk);
