@@ -322,3 +322,25 @@ def test_dx_three_and_four_way_k_splits(BT, n_ignored):
     b = run_gpu(inp, sp)
     assert np.array_equal(a["dX"], b["dX"]) and np.array_equal(a["dW"], b["dW"])
     compare_full(a, run_oracle(inp, sp), inp, sp)
+
+
+@pytest.mark.parametrize("BT,H,V", [(1, 64, 1000), (50, 8, 7), (37, 16, 300), (130, 24, 5),
+                                    (257, 72, 257)])
+@pytest.mark.parametrize("path", ["tc", "simt"])
+def test_tiny_shapes(BT, H, V, path):
+    """Shapes far below one tile in every dimension (one row; V = 5 or 7 columns of a
+    256-column tile; H = 8 or 24, under one 64-deep k-block) and just past tile edges
+    (257): every output against the oracle, on both GEMM back-ends."""
+    sp = I.spec("llama1b", BT=BT, H=H, V=V, w_std=0.5, ignore="none" if BT < 10 else "random",
+                n_ignored=BT // 7)
+    inp = I.generate(sp, seed=27 + BT)
+    g = run_gpu(inp, sp, flags=flce.FLAG_FORCE_SIMT if path == "simt" else 0)
+    assert g["status_code"] == flce.FLCE_OK
+    compare_full(g, run_oracle(inp, sp), inp, sp)
+
+
+@pytest.mark.parametrize("BT,H,V", [(1, 24, 9), (45, 40, 300)])
+def test_tiny_shapes_fp32(BT, H, V):
+    sp = I.spec("tiny_fp32", BT=BT, H=H, V=V, ignore="none" if BT < 10 else "random", n_ignored=5)
+    inp = I.generate(sp, seed=28 + BT)
+    compare_full(run_gpu(inp, sp), run_oracle(inp, sp), inp, sp)
