@@ -20,9 +20,9 @@
 
 #include "flce_internal.cuh"
 
-namespace {
+static __device__ __align__(256) unsigned char g_flce_scratch[FLCE_NOALLOC_SCRATCH_BYTES];
 
-__device__ __align__(256) unsigned char g_flce_scratch[FLCE_NOALLOC_SCRATCH_BYTES];
+namespace {
 
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[64] = {nullptr};
