@@ -11,6 +11,9 @@ any size:
   * with z = 0, every column of dW sums to zero over the vocabulary (sum_v dS_iv = 0);
   * dW exactly, on 256 sampled vocabulary rows, from a run at the same full shapes in
     which only 64 seeded rows keep their label (so the oracle needs only those rows).
+The Llama-3.1-8B head is also run with fp16 inputs and with dW accumulated in bf16, the
+FP16/BF16 rows of the support matrix in "Reduce FLCE weight-gradient allocation overhead
+across FP16, BF16, and FP32" (Proposed direction).
 """
 
 import numpy as np
@@ -34,6 +37,9 @@ CONFIGS = [
     ("llama8b", dict(labelled_fraction=0.1)),
     ("large_vocab", {}),
     ("frozen_head", {}),
+    # the support-matrix rows at full size: fp16 inputs, and dW accumulated in the input dtype
+    ("llama8b", dict(dtype="f16")),
+    ("llama8b", dict(dW_dtype="same")),
 ]
 
 
@@ -48,7 +54,8 @@ def _lib():
 def _gpu(d, sp, reduction=None, targets=None, want_dW=None):
     red = reduction or sp["reduction"]
     wdw = sp["want_dW"] if want_dW is None else want_dW
-    dW = torch.zeros(sp["V"], sp["H"], dtype=torch.float32, device="cuda") if wdw else None
+    dW_dt = d["X"].dtype if sp.get("dW_dtype") == "same" else torch.float32
+    dW = torch.zeros(sp["V"], sp["H"], dtype=dW_dt, device="cuda") if wdw else None
     go = d["grad_out"] if red == "none" else None
     out = flce.fwd_bwd(d["X"], d["W"], d["targets"] if targets is None else targets, d["bias"],
                        reduction=red, z_loss_scale=sp.get("z", 0.0), grad_out=go,
@@ -119,5 +126,5 @@ def test_config_sampled(base, ov):
         lse2, _, _, _, _, p = orc.rows_forward(s, t2[keep], sp.get("z", 0.0))
         dS = orc.rows_grad_logits(p, t2[keep], lse2, c, sp.get("z", 0.0))
         ref = dS[:, vs].T @ np.asarray(X[keep], np.float64)
-        got = g2["dW"][torch.from_numpy(vs).cuda()].cpu().numpy()
+        got = g2["dW"][torch.from_numpy(vs).cuda()].float().cpu().numpy()
         assert rel_fro(got, ref) <= tol["grad"]
