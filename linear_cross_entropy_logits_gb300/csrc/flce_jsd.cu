@@ -8,10 +8,10 @@
 //
 // Per row chunk: gather student and teacher rows; the forward GEMM twice (student and
 // teacher, logits scaled by 1/T in the epilogue, each writing per-tile statistics and its
-// exp slab); k_jsd_finalize (both lse, per-tile log offsets); k_jsd_terms (per element
-// divergence terms and sum_v Q g, reduced per (row, tile) in a fixed order); k_jsd_rowsum
-// (per row, fixed order); k_jsd_grad (dloss/dz into the student slab in place); then the
-// same dX / dW GEMMs as the cross-entropy op. Nothing of [BT, V] reaches HBM.
+// exp slab); k_jsd_finalize (both lse, per-tile log offsets); k_jsd_rows (per row: the
+// divergence terms and sum_v Q g in a fixed order, then dloss/dz into the student slab in
+// place, both passes over a row while it is still in L2); then the same dX / dW GEMMs as
+// the cross-entropy op. Nothing of [BT, V] reaches HBM.
 #include <math.h>
 #include <string.h>
 
@@ -30,7 +30,7 @@ struct JsdPlan {
   int esz;
   size_t off_ctrl, off_idx, off_rloss, off_rz, off_racc;
   size_t off_xcs, off_xct, off_stm_s, off_sts_s, off_sti_s, off_stm_t, off_sts_t, off_sti_t;
-  size_t off_tgt_s, off_tgt_t, off_lse_s, off_lse_t, off_arow, off_srow;
+  size_t off_tgt_s, off_tgt_t, off_lse_s, off_lse_t, off_arow;
   size_t off_slab_s, off_slab_t, off_dxacc;
   size_t total;
 };
@@ -74,7 +74,6 @@ bool jsd_layout(int64_t BT, int64_t Hs, int64_t Ht, int64_t V, int dt, int64_t R
   q.off_lse_s = take(4 * (size_t)R);
   q.off_lse_t = take(4 * (size_t)R);
   q.off_arow = take(4 * (size_t)R);
-  q.off_srow = take(4 * (size_t)R);
   q.off_slab_s = take((size_t)R * q.Vp * q.esz);
   q.off_slab_t = take((size_t)R * q.Vp * q.esz);
   q.off_dxacc = take(q.esz == 2 ? 2 * (size_t)R * Hs * 4 : 0);  // two fp32 buffers
@@ -103,7 +102,6 @@ int64_t jsd_rows_for_bytes(int64_t BT, int64_t Hs, int64_t Ht, int64_t V, int dt
 struct JsdArgs {
   CallArgs s, t;
   float beta, inv_T;
-  float* srow;  // [R] sum_v Q_v g_v per row
 };
 
 __device__ __forceinline__ void lse_merge(float& M, float& S, float M2, float S2) {
@@ -219,205 +217,182 @@ template <> struct Load8<float> {
   }
 };
 
-// Per (row, tile): sum_v of the divergence terms and of Q_v g_v (g = dloss/dQ up to a
-// constant), each thread 8 columns, a warp one row of the tile, xor-butterfly reduction.
-// Each warp takes RU rows per iteration (loads for all of them issued first) so that
-// enough bytes are in flight to cover DRAM latency. The slab's pad columns (v >= V) hold
-// exact zeros, whose terms vanish, so no column test is needed. The partial sums
-// overwrite the student / teacher tile sums (no longer needed).
+// Eight slab columns per lane; a warp covers one 256-column tile, and each warp keeps
+// RU tiles' loads in flight so that enough bytes are outstanding to cover DRAM latency.
 constexpr int RU = 4;
 
-template <typename T>
-__global__ void __launch_bounds__(256) k_jsd_terms(const __grid_constant__ JsdArgs j, int chunk,
-                                                   int rows_per_block) {
-  int row0, rows;
-  if (!chunk_bounds(j.s.w.ctrl, chunk, row0, rows)) return;
-  const int t = blockIdx.x;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int rb0 = blockIdx.y * rows_per_block;
-  const int rb1 = min(rb0 + rows_per_block, rows);
-  const int64_t c0 = (int64_t)t * VT + tx * 8;
-  const int64_t nvt = j.s.nvt;
-  const float beta = j.beta, omb = 1.0f - beta;
-  for (int r = rb0 + ty; r < rb1; r += 8 * RU) {
-    typename Load8<T>::Raw rs[RU], rt[RU];
-    float lqo[RU], lpo[RU];
-#pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      // rows past the block's end re-read the block's first row (always valid); their
-      // sums are discarded
-      const int rr = r + 8 * u < rb1 ? r + 8 * u : r;
-      lqo[u] = j.s.w.stm[(int64_t)rr * nvt + t];
-      lpo[u] = j.t.w.stm[(int64_t)rr * nvt + t];
-      rs[u] = Load8<T>::load((const T*)j.s.w.slab + (int64_t)rr * j.s.Vp + c0);
-      rt[u] = Load8<T>::load((const T*)j.t.w.slab + (int64_t)rr * j.t.Vp + c0);
-    }
-    float term[RU], qg[RU];
-#pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      float es[8], et[8];
-      Load8<T>::cvt(rs[u], es);
-      Load8<T>::cvt(rt[u], et);
-      const float qm = expf(lqo[u]), pm = expf(lpo[u]);
-      const float lq2 = lqo[u] * LOG2E, lp2 = lpo[u] * LOG2E;
-      float tm = 0.0f, g = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float Q = es[k] * qm, P = et[k] * pm;
-        const float lQ = lg2_clamped(es[k]) + lq2, lP = lg2_clamped(et[k]) + lp2;
-        if (beta == 0.0f) {
-          tm = fmaf(P, lP - lQ, tm);
-        } else if (beta == 1.0f) {
-          const float x = Q * (lQ - lP);
-          tm += x;
-          g += x;
-        } else {
-          const float lM = lg2_clamped(fmaf(beta, P, omb * Q));
-          const float qpart = omb * Q * (lQ - lM);
-          tm = fmaf(beta * P, lP - lM, tm + qpart);
-          g += qpart;
-        }
-      }
-      term[u] = tm * LN2;
-      qg[u] = g * LN2;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-      for (int u = 0; u < RU; ++u) {
-        term[u] += __shfl_xor_sync(0xffffffffu, term[u], o);
-        qg[u] += __shfl_xor_sync(0xffffffffu, qg[u], o);
-      }
-    }
-    if (tx == 0) {
-#pragma unroll
-      for (int u = 0; u < RU; ++u) {
-        const int rr = r + 8 * u;
-        if (rr < rb1) {
-          j.s.w.sts[(int64_t)rr * nvt + t] = term[u];
-          j.t.w.sts[(int64_t)rr * nvt + t] = qg[u];
-        }
-      }
-    }
-  }
-}
+// Both elementwise passes in one kernel, one row at a time per CTA (persistent, one CTA
+// per SM): pass 1 reads the row of both slabs and sums the divergence terms and Q g (g =
+// dloss/dQ up to a constant) with a fixed-order block reduction, giving loss_i and
+// S_i = sum_v Q_v g_v; pass 2 reads the row again, while it is still in L2 (one row per SM
+// in flight, about 0.5 MB each at V = 128256), and writes dS over the student slab. DRAM
+// moves each slab row once plus the dS write. The slab's pad columns (v >= V) hold exact
+// zeros, whose terms vanish and whose dS is zero, so no column test is needed.
+constexpr int JR_THREADS = 512;
+constexpr int JR_WARPS = JR_THREADS / 32;
 
-// Per row: loss_i = sum over tiles of the term partials, S_i = sum of the Q g partials
-// (fixed order); per-token and per-labelled-row loss outputs.
-__global__ void __launch_bounds__(256) k_jsd_rowsum(const __grid_constant__ JsdArgs j, int chunk) {
-  int row0, rows;
-  if (!chunk_bounds(j.s.w.ctrl, chunk, row0, rows)) return;
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  const int64_t nvt = j.s.nvt;
-  const float* lp = j.s.w.sts + (int64_t)r * nvt;
-  const float* sp = j.t.w.sts + (int64_t)r * nvt;
-  float L = 0.0f, S = 0.0f;
-  for (int64_t t = lane; t < nvt; t += 32) {
-    L += lp[t];
-    S += sp[t];
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    L += __shfl_xor_sync(0xffffffffu, L, o);
-    S += __shfl_xor_sync(0xffffffffu, S, o);
-  }
-  if (lane == 0) {
-    const int row = j.s.w.idx[row0 + r];
-    j.srow[r] = S;
-    j.s.w.rloss[row0 + r] = L;
-    j.s.w.rz[row0 + r] = 0.0f;
-    j.s.w.racc[row0 + r] = 0.0f;
-    if (j.s.reduction == FLCE_NONE) j.s.loss[row] = L;
-  }
-}
-
-// dS = a_i / T * dloss_i/dz_s written over the student slab (in place); rows past the chunk
-// end up to the next multiple of 64 are zeroed (the dW GEMM reduces over them). RU rows per
-// warp iteration, as in k_jsd_terms; pad columns stay zero (Q = P = 0 there).
 template <typename T>
-__global__ void __launch_bounds__(256) k_jsd_grad(const __grid_constant__ JsdArgs j, int chunk,
-                                                  int rows_per_block) {
+__global__ void __launch_bounds__(JR_THREADS, 1) k_jsd_rows(const __grid_constant__ JsdArgs j, int chunk,
+                                                           int grads) {
   int row0, rows;
   if (!chunk_bounds(j.s.w.ctrl, chunk, row0, rows)) return;
-  const int t = blockIdx.x;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int rlim = (int)rup64(rows, 64);
-  const int rb0 = blockIdx.y * rows_per_block;
-  const int rb1 = min(rb0 + rows_per_block, rlim);
-  const int64_t c0 = (int64_t)t * VT + tx * 8;
-  const int64_t nvt = j.s.nvt;
+  __shared__ float red_t[JR_WARPS], red_g[JR_WARPS];
+  __shared__ float row_S;
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int rlim = grads ? (int)rup64(rows, 64) : rows;
+  const int nvt = (int)j.s.nvt;
   const float beta = j.beta, omb = 1.0f - beta;
-  // dz in base-2 logs: (1 - beta) (lQ - lM) = (1 - beta) ln2 (lQ2 - lM2)
   const float cg = (beta == 1.0f ? 1.0f : omb) * LN2;
-  for (int r = rb0 + ty; r < rb1; r += 8 * RU) {
-    typename Load8<T>::Raw rs[RU], rt[RU];
-    float lqo[RU], lpo[RU], f[RU], S[RU];
+  constexpr int RUJ = sizeof(T) == 4 ? 2 : RU;  // tiles in flight per warp (fp32 rows are twice the bytes)
+  for (int r = blockIdx.x; r < rlim; r += gridDim.x) {
+    const bool live = r < rows;
+    const T* s_row = (const T*)j.s.w.slab + (int64_t)r * j.s.Vp;
+    const T* t_row = (const T*)j.t.w.slab + (int64_t)r * j.t.Vp;
+    const float* soff = j.s.w.stm + (int64_t)r * nvt;
+    const float* toff = j.t.w.stm + (int64_t)r * nvt;
+    float S = 0.0f;
+    if (live) {
+      // ---- pass 1: warp wp takes tiles wp, wp + JR_WARPS, ... RUJ at a time
+      float tm = 0.0f, g = 0.0f;
+      for (int t0 = wp; t0 < nvt; t0 += JR_WARPS * RUJ) {
+        typename Load8<T>::Raw rs[RUJ], rt[RUJ];
+        float lqo[RUJ], lpo[RUJ];
 #pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      // rows in [rows, rlim) are written as exact zeros (below) and read the chunk's first
-      // row instead; rows at or past rb1 are skipped
-      const int rr = r + 8 * u < rows ? r + 8 * u : 0;
-      lqo[u] = j.s.w.stm[(int64_t)rr * nvt + t];
-      lpo[u] = j.t.w.stm[(int64_t)rr * nvt + t];
-      f[u] = r + 8 * u < rows ? j.s.w.arow[rr] * j.inv_T : 0.0f;
-      S[u] = j.srow[rr];
-      rs[u] = Load8<T>::load((const T*)j.s.w.slab + (int64_t)rr * j.s.Vp + c0);
-      rt[u] = Load8<T>::load((const T*)j.t.w.slab + (int64_t)rr * j.t.Vp + c0);
-    }
-#pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      const int rr = r + 8 * u;
-      if (rr >= rb1) continue;
-      const bool live = rr < rows;
-      float es[8], et[8];
-      Load8<T>::cvt(rs[u], es);
-      Load8<T>::cvt(rt[u], et);
-      const float qm = expf(lqo[u]), pm = expf(lpo[u]);
-      const float lq2 = lqo[u] * LOG2E, lp2 = lpo[u] * LOG2E;
-      float out[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float Q = es[k] * qm, P = et[k] * pm;
-        float dz;
-        if (beta == 0.0f) {
-          dz = Q - P;
-        } else {
-          const float lQ = lg2_clamped(es[k]) + lq2;
-          const float lR = beta == 1.0f ? lg2_clamped(et[k]) + lp2
-                                        : lg2_clamped(fmaf(beta, P, omb * Q));
-          dz = Q * fmaf(cg, lQ - lR, -S[u]);
+        for (int u = 0; u < RUJ; ++u) {
+          const int t = t0 + u * JR_WARPS < nvt ? t0 + u * JR_WARPS : t0;  // re-read t0 past the end
+          lqo[u] = soff[t];
+          lpo[u] = toff[t];
+          rs[u] = Load8<T>::load(s_row + (int64_t)t * VT + lane * 8);
+          rt[u] = Load8<T>::load(t_row + (int64_t)t * VT + lane * 8);
         }
-        out[k] = live ? f[u] * dz : 0.0f;
+#pragma unroll
+        for (int u = 0; u < RUJ; ++u) {
+          if (t0 + u * JR_WARPS >= nvt) continue;
+          float es[8], et[8];
+          Load8<T>::cvt(rs[u], es);
+          Load8<T>::cvt(rt[u], et);
+          const float qm = expf(lqo[u]), pm = expf(lpo[u]);
+          const float lq2 = lqo[u] * LOG2E, lp2 = lpo[u] * LOG2E;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float Q = es[k] * qm, P = et[k] * pm;
+            const float lQ = lg2_clamped(es[k]) + lq2, lP = lg2_clamped(et[k]) + lp2;
+            if (beta == 0.0f) {
+              tm = fmaf(P, lP - lQ, tm);
+            } else if (beta == 1.0f) {
+              const float x = Q * (lQ - lP);
+              tm += x;
+              g += x;
+            } else {
+              const float lM = lg2_clamped(fmaf(beta, P, omb * Q));
+              const float qpart = omb * Q * (lQ - lM);
+              tm = fmaf(beta * P, lP - lM, tm + qpart);
+              g += qpart;
+            }
+          }
+        }
       }
-      Load8<T>::store((T*)j.s.w.slab + (int64_t)rr * j.s.Vp + c0, out);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        tm += __shfl_xor_sync(0xffffffffu, tm, o);
+        g += __shfl_xor_sync(0xffffffffu, g, o);
+      }
+      if (lane == 0) {
+        red_t[wp] = tm;
+        red_g[wp] = g;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float L = 0.0f, G = 0.0f;
+        for (int w = 0; w < JR_WARPS; ++w) {  // fixed order
+          L += red_t[w];
+          G += red_g[w];
+        }
+        L *= LN2;
+        G *= LN2;
+        row_S = G;
+        const int row = j.s.w.idx[row0 + r];
+        j.s.w.rloss[row0 + r] = L;
+        j.s.w.rz[row0 + r] = 0.0f;
+        j.s.w.racc[row0 + r] = 0.0f;
+        if (j.s.reduction == FLCE_NONE) j.s.loss[row] = L;
+      }
+      __syncthreads();
+      S = row_S;
     }
+    if (grads) {
+      // ---- pass 2: dS = a_i / T * dloss_i/dz_s over the student row, with dloss/dz_s =
+      // Q ((1 - beta) ln2 (lQ2 - lM2) - S) in base-2 logs (M = P when beta = 1, and Q - P when
+      // beta = 0); rows past the chunk up to the next multiple of 64 are written as zeros
+      // (the dW GEMM reduces over them)
+      T* d_row = (T*)j.s.w.slab + (int64_t)r * j.s.Vp;
+      const float f = live ? j.s.w.arow[r] * j.inv_T : 0.0f;
+      for (int t0 = wp; t0 < nvt; t0 += JR_WARPS * RUJ) {
+        typename Load8<T>::Raw rs[RUJ], rt[RUJ];
+        float lqo[RUJ], lpo[RUJ];
+        if (live) {
+#pragma unroll
+          for (int u = 0; u < RUJ; ++u) {
+            const int t = t0 + u * JR_WARPS < nvt ? t0 + u * JR_WARPS : t0;
+            lqo[u] = soff[t];
+            lpo[u] = toff[t];
+            rs[u] = Load8<T>::load(s_row + (int64_t)t * VT + lane * 8);
+            rt[u] = Load8<T>::load(t_row + (int64_t)t * VT + lane * 8);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < RUJ; ++u) {
+          const int t = t0 + u * JR_WARPS;
+          if (t >= nvt) continue;
+          float out[8];
+          if (live) {
+            float es[8], et[8];
+            Load8<T>::cvt(rs[u], es);
+            Load8<T>::cvt(rt[u], et);
+            const float qm = expf(lqo[u]), pm = expf(lpo[u]);
+            const float lq2 = lqo[u] * LOG2E, lp2 = lpo[u] * LOG2E;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float Q = es[k] * qm, P = et[k] * pm;
+              float dz;
+              if (beta == 0.0f) {
+                dz = Q - P;
+              } else {
+                const float lQ = lg2_clamped(es[k]) + lq2;
+                const float lR = beta == 1.0f ? lg2_clamped(et[k]) + lp2
+                                              : lg2_clamped(fmaf(beta, P, omb * Q));
+                dz = Q * fmaf(cg, lQ - lR, -S);
+              }
+              out[k] = f * dz;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) out[k] = 0.0f;
+          }
+          Load8<T>::store(d_row + (int64_t)t * VT + lane * 8, out);
+        }
+      }
+    }
+    __syncthreads();  // red_t / red_g / row_S are reused by the next row
   }
 }
 
 template <typename T>
-cudaError_t launch_jsd_elementwise(const JsdArgs& j, int chunk, cudaStream_t s, bool grad) {
-  const int rpb = 256;
-  dim3 grid((unsigned)j.s.nvt, (unsigned)cdiv(j.s.R, rpb));
-  if (!grad) {
-    k_jsd_terms<T><<<grid, 256, 0, s>>>(j, chunk, rpb);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    k_jsd_rowsum<<<(unsigned)cdiv(j.s.R, 8), 256, 0, s>>>(j, chunk);
-  } else {
-    k_jsd_grad<T><<<grid, 256, 0, s>>>(j, chunk, rpb);
-  }
+cudaError_t launch_jsd_rows(const JsdArgs& j, int chunk, cudaStream_t s, bool grads) {
+  int g = num_sms();
+  if (g > j.s.R) g = (int)j.s.R;
+  k_jsd_rows<T><<<(unsigned)g, JR_THREADS, 0, s>>>(j, chunk, grads ? 1 : 0);
   return cudaGetLastError();
 }
 
-cudaError_t jsd_elementwise(const JsdArgs& j, int chunk, cudaStream_t s, bool grad) {
+cudaError_t jsd_rows(const JsdArgs& j, int chunk, cudaStream_t s, bool grads) {
   switch (j.s.dt) {
-    case FLCE_BF16: return launch_jsd_elementwise<__nv_bfloat16>(j, chunk, s, grad);
-    case FLCE_F16: return launch_jsd_elementwise<__half>(j, chunk, s, grad);
-    default: return launch_jsd_elementwise<float>(j, chunk, s, grad);
+    case FLCE_BF16: return launch_jsd_rows<__nv_bfloat16>(j, chunk, s, grads);
+    case FLCE_F16: return launch_jsd_rows<__half>(j, chunk, s, grads);
+    default: return launch_jsd_rows<float>(j, chunk, s, grads);
   }
 }
+
 
 inline bool aligned(const void* p, size_t n) { return ((uintptr_t)p % n) == 0; }
 
@@ -540,7 +515,6 @@ extern "C" int32_t flce_fused_linear_jsd(const flce_jsd_args* x, void* stream) {
   j.t = t;
   j.beta = x->beta;
   j.inv_T = 1.0f / x->temperature;
-  j.srow = (float*)(b + p.off_srow);
 
   cudaStream_t st = (cudaStream_t)stream;
   const bool tc = !(x->flags & FLCE_FLAG_FORCE_SIMT) && tc_supported(s) && tc_supported(t);
@@ -565,10 +539,7 @@ extern "C" int32_t flce_fused_linear_jsd(const flce_jsd_args* x, void* stream) {
       k_jsd_finalize<<<(unsigned)cdiv(p.R, 8), 256, 0, st>>>(j, k);
       return cudaGetLastError();
     }));
-    JSD_TRY(staged(prof, FLCE_STAGE_GPASS, grads ? 3 : 2, st, [&] {
-      cudaError_t e = jsd_elementwise(j, k, st, false);
-      return (e != cudaSuccess || !grads) ? e : jsd_elementwise(j, k, st, true);
-    }));
+    JSD_TRY(staged(prof, FLCE_STAGE_GPASS, 1, st, [&] { return jsd_rows(j, k, st, grads); }));
     if (s.want_dX) {
       if (tc) {
         JSD_TRY(staged(prof, FLCE_STAGE_DX, 2, st, [&] {
