@@ -460,7 +460,16 @@ def run_ours(args):
                 "peak_kind": f"bf16 sustained ({peak_src})",
                 "per_launch": f"2*H*V FLOPs per labelled row x {n_lab * args.steps / max(dom_launches, 1):.0f} rows per launch",
                 "traffic": (rec["per_launch_bytes"].get(dom) if rec else None),
-                "traffic_source": "profiles/traffic.json (ncu, full size)" if rec else None}
+                "traffic_source": "profiles/traffic.json (ncu, full size)" if rec else None,
+                # the same kernel against the burst figure, and every GEMM of the step
+                "peak_burst": peaks["bf16_tflops"], "frac_burst": achieved / peaks["bf16_tflops"],
+                "gemms": {k: {"ms_per_step": stages[k][0] / args.steps,
+                              "tflops": gemm_flops / (stages[k][0] / args.steps / 1000.0) / 1e12,
+                              "frac_sustained": gemm_flops / (stages[k][0] / args.steps / 1000.0) / 1e12 / peak,
+                              "frac_burst": gemm_flops / (stages[k][0] / args.steps / 1000.0) / 1e12
+                              / peaks["bf16_tflops"],
+                              "traffic": (rec["per_launch_bytes"].get(k) if rec else None)}
+                          for k in ("fwd", "dx", "dw") if k in stages and stages[k][1] > 0}}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks.get("hbm_gbs"),
                 "unit": "GB/s", "frac": None, "traffic": None}
@@ -643,7 +652,8 @@ def run_jsd(args):
                                                      "sustained": tflops / peak, "source": src},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_kind": f"bf16 sustained ({src})", "traffic": None},
+                         "peak_kind": f"bf16 sustained ({src})", "traffic": None,
+                         "peak_burst": peaks["bf16_tflops"], "frac_burst": achieved / peaks["bf16_tflops"]},
             "stages": {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                        for k, v in stages.items() if v[1] > 0},
             "gpu_launches": int(sum(v[1] for v in stages.values())) if args.api == "abi" else None, "clocks": clocks, "e2e": e2e}
