@@ -171,6 +171,17 @@ FLCE_API size_t flce_workspace_size(int64_t BT, int64_t H, int64_t V, int32_t in
 FLCE_API int64_t flce_chunk_rows(int64_t BT, int64_t H, int64_t V, int32_t in_dtype,
                         size_t workspace_bytes);
 
+/* Human-readable plan of a call with this workspace size, for logs and debugging: chunk
+ * rows, host chunk launches, vocabulary tiles, the workspace regions with their offsets and
+ * sizes, and the GEMM tile shapes and tile counts when every row is labelled (the device
+ * balances the rows it actually finds over cdiv(N, R) chunks). Writes at most `out_len`
+ * bytes including the terminating NUL into `out` (which may be NULL when out_len is 0) and
+ * returns the length of the full text, like snprintf, or -1 for invalid sizes or dtype or
+ * a workspace too small for one 128-row chunk. Host-only; touches no GPU. This is the tile
+ * plan trace of the design, offered as a call rather than an environment switch. */
+FLCE_API int64_t flce_plan_describe(int64_t BT, int64_t H, int64_t V, int32_t in_dtype,
+                                    size_t workspace_bytes, char* out, size_t out_len);
+
 /* Enqueue the fused forward+backward on `stream` (a cudaStream_t; NULL = legacy default
  * stream). Returns FLCE_OK once every kernel is enqueued, or an error code with nothing
  * enqueued (FLCE_ERR_CUDA may follow a partial enqueue if a launch fails). */

@@ -10,7 +10,9 @@
 // caller sized, whatever the labelled share.
 #include <atomic>
 #include <mutex>
+#include <stdio.h>
 #include <string.h>
+#include <string>
 #include <vector>
 
 #include "flce_internal.cuh"
@@ -201,6 +203,59 @@ extern "C" int64_t flce_chunk_rows(int64_t BT, int64_t H, int64_t V, int32_t in_
   if (BT <= 0 || H <= 0 || V <= 0) return 0;
   if (in_dtype != FLCE_F32 && in_dtype != FLCE_BF16 && in_dtype != FLCE_F16) return 0;
   return plan_rows_for_bytes(BT, H, V, in_dtype, workspace_bytes);
+}
+
+extern "C" int64_t flce_plan_describe(int64_t BT, int64_t H, int64_t V, int32_t in_dtype,
+                                      size_t workspace_bytes, char* out, size_t out_len) {
+  if (BT <= 0 || H <= 0 || V <= 0) return -1;
+  if (in_dtype != FLCE_F32 && in_dtype != FLCE_BF16 && in_dtype != FLCE_F16) return -1;
+  if (out == nullptr && out_len != 0) return -1;
+  const int64_t R = plan_rows_for_bytes(BT, H, V, in_dtype, workspace_bytes);
+  Plan p;
+  if (R <= 0 || !plan_layout(BT, H, V, in_dtype, R, &p)) return -1;
+  static const char* const names[3] = {"f32", "bf16", "f16"};
+  std::string t;
+  char line[256];
+  auto add = [&](const char* fmt, auto... v) {
+    snprintf(line, sizeof(line), fmt, v...);
+    t += line;
+  };
+  add("flce plan: BT=%lld H=%lld V=%lld dtype=%s workspace=%zu B (%zu B used)\n", (long long)BT,
+      (long long)H, (long long)V, names[in_dtype], workspace_bytes, p.total);
+  add("  chunk rows R=%lld, host chunk launches cdiv(BT,R)=%lld (the device runs cdiv(N,R) of them "
+      "for N labelled rows)\n", (long long)R, (long long)p.kmax);
+  add("  vocabulary tiles: %lld x %d columns (slab pitch %lld), H padded to %lld\n", (long long)p.nvt,
+      VT, (long long)p.Vp, (long long)p.Hp);
+  const struct {
+    const char* name;
+    size_t off, next;
+  } reg[] = {{"ctrl", p.off_ctrl, p.off_idx},        {"idx", p.off_idx, p.off_rloss},
+             {"rloss", p.off_rloss, p.off_rz},       {"rz", p.off_rz, p.off_racc},
+             {"racc", p.off_racc, p.off_xc},         {"xc", p.off_xc, p.off_stm},
+             {"stm", p.off_stm, p.off_sts},          {"sts", p.off_sts, p.off_sti},
+             {"sti", p.off_sti, p.off_tgt},          {"tgt", p.off_tgt, p.off_lse},
+             {"lse", p.off_lse, p.off_arow},         {"arow", p.off_arow, p.off_rsc},
+             {"rsc", p.off_rsc, p.off_slab},         {"slab", p.off_slab, p.off_dxacc},
+             {"dxacc", p.off_dxacc, p.total}};
+  for (const auto& r : reg)
+    if (r.next > r.off) add("  workspace %-6s at %12zu, %12zu B\n", r.name, r.off, r.next - r.off);
+  if (in_dtype == FLCE_F32 || H % 8 != 0) {
+    add("  GEMMs: SIMT fp32-FMA kernels (%s)\n", in_dtype == FLCE_F32 ? "fp32 inputs" : "H not a multiple of 8");
+  } else {
+    const int64_t mt = (R + 255) / 256, ht = (H + 255) / 256, vt = (V + 255) / 256;
+    const bool wide_dw = R >= 4096;
+    add("  GEMMs (tcgen05, CTA pairs) per full chunk: forward %lld tiles of 256x256; dX %lld tiles of "
+        "256x512 (K = V, up to 4 K splits); dW %lld tiles of %s\n",
+        (long long)(mt * p.nvt), (long long)(mt * ((ht + 1) / 2)),
+        (long long)(wide_dw ? vt * ((ht + 1) / 2) : vt * ht), wide_dw ? "256x512" : "256x256");
+  }
+  const int64_t n = (int64_t)t.size();
+  if (out_len > 0) {
+    const size_t c = (size_t)n < out_len - 1 ? (size_t)n : out_len - 1;
+    memcpy(out, t.data(), c);
+    out[c] = '\0';
+  }
+  return n;
 }
 
 extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {

@@ -28,7 +28,8 @@ EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_fwd_
             "flce_get_status",
             "flce_profile_create", "flce_profile_reset", "flce_profile_destroy",
             "flce_profile_read", "flce_last_cuda_error", "flce_status_string", "flce_abi_version",
-            "flce_jsd_workspace_size", "flce_fused_linear_jsd", "flce_scale_by")
+            "flce_jsd_workspace_size", "flce_fused_linear_jsd", "flce_scale_by",
+            "flce_plan_describe")
 STAGES = ("prologue", "gather", "fwd", "finalize", "gpass", "dx", "dw", "reduce")
 
 
@@ -84,6 +85,9 @@ def load(path: str | None = None):
     lib.flce_workspace_size.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int32, ctypes.c_size_t]
     lib.flce_chunk_rows.restype = ctypes.c_int64
     lib.flce_chunk_rows.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int32, ctypes.c_size_t]
+    lib.flce_plan_describe.restype = ctypes.c_int64
+    lib.flce_plan_describe.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_int32, ctypes.c_size_t,
+                                                              ctypes.c_char_p, ctypes.c_size_t]
     lib.flce_fwd_bwd.restype = ctypes.c_int32
     lib.flce_fwd_bwd.argtypes = [ctypes.POINTER(FlceArgs), ctypes.c_void_p]
     lib.flce_fwd_bwd_noalloc.restype = ctypes.c_int32
@@ -134,6 +138,19 @@ def workspace_size(BT, H, V, dtype=torch.bfloat16, budget_bytes=0) -> int:
 
 def chunk_rows(BT, H, V, dtype, workspace_bytes) -> int:
     return int(load().flce_chunk_rows(BT, H, V, DTYPES[dtype], workspace_bytes))
+
+
+def describe_plan(BT, H, V, dtype=torch.bfloat16, workspace_bytes=None, budget_bytes=0) -> str:
+    """The library's text plan of a call (chunk rows, workspace regions, GEMM tiles) for a
+    workspace of ``workspace_bytes`` (default: the planner's size for ``budget_bytes``)."""
+    lib = load()
+    wb = workspace_size(BT, H, V, dtype, budget_bytes) if workspace_bytes is None else workspace_bytes
+    n = int(lib.flce_plan_describe(BT, H, V, DTYPES[dtype], wb, None, 0))
+    if n < 0:
+        raise FlceError(FLCE_ERR_INVALID_ARG, "flce_plan_describe")
+    buf = ctypes.create_string_buffer(n + 1)
+    lib.flce_plan_describe(BT, H, V, DTYPES[dtype], wb, buf, n + 1)
+    return buf.value.decode()
 
 
 class Profiler:

@@ -171,3 +171,30 @@ def test_jsd_workspace_flat_in_BT(lib):
          for BT in (8192, 16384)}
     assert 0 < s[8192] <= int(1.5 * 2 ** 30)
     assert abs((s[16384] - s[8192]) - 16 * 8192) <= 4 * 256
+
+
+def test_plan_describe(lib):
+    """The host-side plan text: chunk rows and tiles as the planner computes them, snprintf
+    length semantics (the NULL / 0 query gives the full length, a short buffer truncates),
+    and -1 for an invalid call."""
+    BT, H, V = 8192, 4096, 128256
+    wb = flce.workspace_size(BT, H, V, torch.bfloat16, 0)
+    R = flce.chunk_rows(BT, H, V, torch.bfloat16, wb)
+    txt = flce.describe_plan(BT, H, V, torch.bfloat16, wb)
+    assert f"chunk rows R={R}," in txt and "cdiv(BT,R)=1 " in txt
+    assert "vocabulary tiles: 501 x 256 columns" in txt
+    assert f"forward {((R + 255) // 256) * 501} tiles of 256x256" in txt
+    assert "dW 4008 tiles of 256x512" in txt
+    assert "workspace slab   at" in txt and str(R * 128256 * 2) in txt
+    n = lib.flce_plan_describe(BT, H, V, 1, wb, None, 0)
+    assert n == len(txt.encode())
+    buf = ctypes.create_string_buffer(16)
+    assert lib.flce_plan_describe(BT, H, V, 1, wb, buf, 16) == n
+    assert buf.value.decode() == txt[:15]
+    # fp32 and a workspace that forces 128-row chunks
+    small = flce.workspace_size(128, 64, 1000, torch.float32, 0) + 16 * 1000 + 4096
+    t32 = flce.describe_plan(1000, 64, 1000, torch.float32, small)
+    assert "chunk rows R=128," in t32 and "cdiv(BT,R)=8 " in t32 and "SIMT fp32-FMA" in t32
+    assert lib.flce_plan_describe(0, H, V, 1, wb, None, 0) == -1
+    assert lib.flce_plan_describe(BT, H, V, 7, wb, None, 0) == -1
+    assert lib.flce_plan_describe(BT, H, V, 1, 1024, None, 0) == -1
