@@ -91,10 +91,10 @@ constexpr int BOX_BYTES = 64 * 64 * 2;             // one 64x64 MN-major TMA box
 constexpr int NUM_THREADS = 320;                   // producer, MMA, 8 epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tfull[2], tempty[2], drain
-// Epilogue staging: 32 KB, split over the active epilogue warps: 32-row x 128-byte
-// buffers (two per warp with four warps, one with eight) that feed TMA bulk tensor stores
-// (FWD: the exp slab) or reduce-adds (DX/DW: the L2 performs dst += tile; no register
-// read-modify-write).
+// Epilogue staging of DX / DW: 32 KB, split over the active epilogue warps: 32-row x
+// 128-byte buffers (two per warp with four warps, one with eight) that feed TMA
+// reduce-adds (the L2 performs dst += tile; no register read-modify-write). The forward
+// writes its exp slab straight from registers and stages nothing.
 constexpr int EPI_BUF_BYTES = 32 * 128;
 constexpr int EPI_BYTES_MIN = 8 * EPI_BUF_BYTES;   // 32 KB
 // Epilogue staging of a tile shape: 32 KB, or for the wide tile whatever the stages leave
@@ -116,11 +116,16 @@ template <int NB>
 __host__ __device__ constexpr int epi_nbuf_of() {
   return 8 / epi_warps_of<NB>();
 }
-template <int NB>
-constexpr int smem_bytes() {
-  return stages_of<NB>() * stage_bytes<NB>() + epi_bytes_of<NB>() + 1024 + 512;
+// Staging bytes a launch reserves: none for the forward.
+template <int MODE, int NB>
+__host__ __device__ constexpr int epi_bytes_m() {
+  return MODE == FWD ? 0 : epi_bytes_of<NB>();
 }
-static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448, "shared memory per CTA");
+template <int MODE, int NB>
+constexpr int smem_bytes() {
+  return stages_of<NB>() * stage_bytes<NB>() + epi_bytes_m<MODE, NB>() + 1024 + 512;
+}
+static_assert(smem_bytes<DX, 1>() <= 232448 && smem_bytes<DX, 2>() <= 232448, "shared memory per CTA");
 static_assert(half_bufs_of<1>() >= 2 && half_bufs_of<2>() >= 2, "epilogue staging buffers");
 
 __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -478,118 +483,158 @@ struct Items {
 };
 
 // ------------------------------------------------------------------ epilogues
-// Row-reference forward epilogue: exp(s) needs no tile max, so one pass over TMEM gives
-// the max / lowest-index argmax / target logit and the staged exp values (64 columns per
-// TMEM wait), written to the slab by TMA bulk tensor stores as in the per-tile form.
-template <typename T, int NBUF>
-__device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, const CUtensorMap* tmS, uint8_t* stg,
-                                                 int row0, int rows, int mrow, int n, uint32_t taddr,
-                                                 int q, int lane, uint32_t& epi_it) {
+// The forward epilogues write the exp slab straight from registers: each thread holds 64
+// consecutive columns of its row as 16-bit values (128 bytes, one whole line) and stores
+// them with four 32-byte stores. Slab rows past R are skipped (the slab has R rows; rows
+// between the chunk's end and R hold values nothing reads, and the zero Xc rows there make
+// them finite).
+template <typename T>
+__device__ __forceinline__ void store_slab64(const CallArgs& a, int rr, int col, const uint32_t (&pk)[32]) {
+  if (rr >= (int)a.R) return;
+  uint32_t* dst = (uint32_t*)((T*)a.w.slab + (int64_t)rr * a.Vp + col);  // 32-byte aligned
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 8 * j), "r"(pk[8 * j]),
+                 "r"(pk[8 * j + 1]), "r"(pk[8 * j + 2]), "r"(pk[8 * j + 3]), "r"(pk[8 * j + 4]),
+                 "r"(pk[8 * j + 5]), "r"(pk[8 * j + 6]), "r"(pk[8 * j + 7])
+                 : "memory");
+}
+
+// r[idx] for a per-thread index 0 <= idx < 64 by a six-level select tree (indexing the
+// register array at run time would move it to local memory).
+__device__ __forceinline__ float select64(const uint32_t (&r)[64], int idx) {
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = __uint_as_float((idx & 1) ? r[2 * i + 1] : r[2 * i]);
+#pragma unroll
+  for (int w = 16, b = 2; w >= 1; w >>= 1, b <<= 1) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) x[i] = (idx & b) ? x[2 * i + 1] : x[2 * i];
+  }
+  return x[0];
+}
+
+// The target logit of a row whose target column lies in the 64 columns just loaded
+// (loc in [0, 64)). The warp picks it out only when one of its 32 rows has its target
+// there (about one 64-column block in 60 at V = 128256), so no per-column comparison runs.
+template <typename T>
+__device__ __forceinline__ void pick_target(const uint32_t (&r)[64], int loc, int v, float ls, const T* bias,
+                                            float& tl) {
+  const bool mine = (unsigned)loc < 64u;
+  if (__any_sync(0xffffffffu, mine)) {
+    const float tv = select64(r, loc & 63) * ls;
+    if (mine) tl = bias != nullptr ? tv + to_f<T>(bias[v]) : tv;
+  }
+}
+
+// 64 columns of the row-reference forward: max / lowest-index argmax (four independent
+// chains, merged with lowest-index ties, so that the compare-select latency of one chain
+// does not serialise the columns), the sum of exp(s) and the packed exp(s) values. FULL:
+// every column lies inside the vocabulary (all but the last tile), no column test.
+template <typename T, bool FULL>
+__device__ __forceinline__ void fwd_ref_cols(const CallArgs& a, const uint32_t (&r)[64], int vbase, float ls,
+                                             const T* bias, float& mx, int& ai, float& sum, uint32_t (&pk)[32]) {
+  const int V = (int)a.V;
+  float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
+  int a4[4] = {ai, 0x7fffffff, 0x7fffffff, 0x7fffffff};
+#pragma unroll
+  for (int jj = 0; jj < 64; jj += 2) {
+    const int v = vbase + jj;
+    float s0 = __uint_as_float(r[jj]) * ls, s1 = __uint_as_float(r[jj + 1]) * ls;
+    const bool ok0 = FULL || v < V, ok1 = FULL || v + 1 < V;
+    if (bias != nullptr) {
+      if (ok0) s0 += to_f<T>(bias[v]);
+      if (ok1) s1 += to_f<T>(bias[v + 1]);
+    }
+    const int u = 2 * ((jj >> 1) & 1);
+    if (ok0 && s0 > m4[u]) {
+      m4[u] = s0;
+      a4[u] = v;
+    }
+    if (ok1 && s1 > m4[u + 1]) {
+      m4[u + 1] = s1;
+      a4[u + 1] = v + 1;
+    }
+    const float e0 = ok0 ? ex2_fast(s0 * LOG2E) : 0.0f;
+    const float e1 = ok1 ? ex2_fast(s1 * LOG2E) : 0.0f;
+    sum += e0 + e1;
+    pk[jj / 2] = pack2<T>(e0, e1);
+  }
+#pragma unroll
+  for (int k = 1; k < 4; ++k)
+    if (m4[k] > m4[0] || (m4[k] == m4[0] && a4[k] < a4[0])) {
+      m4[0] = m4[k];
+      a4[0] = a4[k];
+    }
+  mx = m4[0];
+  ai = a4[0];
+}
+
+// Row-reference forward epilogue: exp(s) needs no tile max, so one pass over TMEM (64
+// columns per wait) gives the max / lowest-index argmax, the target logit and the exp
+// values, written to the slab.
+template <typename T>
+__device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, int row0, int rows, int mrow, int n,
+                                                 uint32_t taddr, int q, int lane) {
   const int rr = mrow + q * 32 + lane;  // row within the chunk
   const bool valid = rr < rows;
-  const int V = (int)a.V;
-  int64_t tg = -1;
-  if (valid && a.targets != nullptr) tg = a.targets[a.w.idx[row0 + rr]];
   const int v0 = n * VT;
+  int toff = -1;  // the target's column within this tile, or -1
+  if (valid && a.targets != nullptr) {
+    const int64_t tg = a.targets[a.w.idx[row0 + rr]];
+    if (tg >= v0 && tg < v0 + BN) toff = (int)(tg - v0);
+  }
   const float ls = a.logit_scale;
   const T* bias = (const T*)a.bias;
+  const bool full = v0 + BN <= (int)a.V;
   float mx = -INFINITY, tl = 0.0f, sum = 0.0f;
   int ai = v0;
-  bool ht = false;
 #pragma unroll 1
   for (int c2 = 0; c2 < BN / 64; ++c2) {
     uint32_t r[64];
     tmem_ld64(taddr + c2 * 64, r);
-    uint8_t* buf = stg + (epi_it % NBUF) * EPI_BUF_BYTES;
-    uint8_t* row = buf + lane * 128;
-    if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last read this buffer is done
-    __syncwarp();
+    pick_target<T>(r, toff - c2 * 64, v0 + toff, ls, bias, tl);
     uint32_t pk[32];
-    // four independent max / argmax chains (merged below with lowest-index ties), so the
-    // compare-select latency of one chain does not serialise the 64 columns
-    float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
-    int a4[4] = {ai, 0x7fffffff, 0x7fffffff, 0x7fffffff};
-#pragma unroll
-    for (int jj = 0; jj < 64; jj += 2) {
-      const int v = v0 + c2 * 64 + jj;
-      float s0 = __uint_as_float(r[jj]) * ls, s1 = __uint_as_float(r[jj + 1]) * ls;
-      const bool ok0 = v < V, ok1 = v + 1 < V;
-      if (bias != nullptr) {
-        if (ok0) s0 += to_f<T>(bias[v]);
-        if (ok1) s1 += to_f<T>(bias[v + 1]);
-      }
-      const int u = 2 * ((jj >> 1) & 1);
-      if (ok0 && s0 > m4[u]) {
-        m4[u] = s0;
-        a4[u] = v;
-      }
-      if (ok1 && s1 > m4[u + 1]) {
-        m4[u + 1] = s1;
-        a4[u + 1] = v + 1;
-      }
-      if (v == tg) {
-        tl = s0;
-        ht = true;
-      }
-      if (v + 1 == tg) {
-        tl = s1;
-        ht = true;
-      }
-      const float e0 = ok0 ? ex2_fast(s0 * LOG2E) : 0.0f;
-      const float e1 = ok1 ? ex2_fast(s1 * LOG2E) : 0.0f;
-      sum += e0 + e1;
-      pk[jj / 2] = pack2<T>(e0, e1);
-    }
-#pragma unroll
-    for (int k = 1; k < 4; ++k)
-      if (m4[k] > m4[0] || (m4[k] == m4[0] && a4[k] < a4[0])) {
-        m4[0] = m4[k];
-        a4[0] = a4[k];
-      }
-    mx = m4[0];
-    ai = a4[0];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      *(uint4*)(row + ((j ^ (lane & 7)) << 4)) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(tmS, smem_u32(buf), v0 + c2 * 64, mrow + q * 32);
-      bulk_commit();
-    }
-    ++epi_it;
+    if (full) fwd_ref_cols<T, true>(a, r, v0 + c2 * 64, ls, bias, mx, ai, sum, pk);
+    else fwd_ref_cols<T, false>(a, r, v0 + c2 * 64, ls, bias, mx, ai, sum, pk);
+    store_slab64<T>(a, rr, v0 + c2 * 64, pk);
   }
   if (valid) {
     const int64_t o = (int64_t)rr * a.nvt + n;
     a.w.stm[o] = mx;
     a.w.sts[o] = sum;
     a.w.sti[o] = ai;
-    if (ht) a.w.tgt[rr] = tl;
+    if (toff >= 0) a.w.tgt[rr] = tl;
   }
 }
 
-template <typename T, int NBUF>
-__device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMap* tmS, uint8_t* stg,
-                                             int row0, int rows, int mrow, int n, uint32_t taddr, int q,
-                                             int lane, uint32_t& epi_it) {
+// Per-tile forward epilogue (fp16 inputs, dbias, the distillation op, a chunk outside the
+// row-reference window): a first pass over TMEM for the max / argmax / target logit, a
+// second for exp(s - max) into the slab.
+template <typename T>
+__device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int rows, int mrow, int n,
+                                             uint32_t taddr, int q, int lane) {
   const int rr = mrow + q * 32 + lane;  // row within the chunk
   const bool valid = rr < rows;
   const int V = (int)a.V;
-  int64_t tg = -1;
-  if (valid && a.targets != nullptr) tg = a.targets[a.w.idx[row0 + rr]];
+  int toff = -1;
   const int v0 = n * VT;
+  if (valid && a.targets != nullptr) {
+    const int64_t tg = a.targets[a.w.idx[row0 + rr]];
+    if (tg >= v0 && tg < v0 + BN) toff = (int)(tg - v0);
+  }
   const float ls = a.logit_scale;
   const T* bias = (const T*)a.bias;
   float mx = -INFINITY, tl = 0.0f;
   int ai = v0;
-  bool ht = false;
 #pragma unroll 1
-  for (int cc = 0; cc < BN / 32; ++cc) {
-    uint32_t r[32];
-    tmem_ld32(taddr + cc * 32, r);
+  for (int c2 = 0; c2 < BN / 64; ++c2) {
+    uint32_t r[64];
+    tmem_ld64(taddr + c2 * 64, r);
+    pick_target<T>(r, toff - c2 * 64, v0 + toff, ls, bias, tl);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int v = v0 + cc * 32 + j;
+    for (int j = 0; j < 64; ++j) {
+      const int v = v0 + c2 * 64 + j;
       float s = __uint_as_float(r[j]) * ls;
       if (v < V) {
         if (bias != nullptr) s += to_f<T>(bias[v]);
@@ -597,66 +642,41 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const CUtensorMa
           mx = s;
           ai = v;
         }
-        if (v == tg) {
-          tl = s;
-          ht = true;
-        }
       }
     }
   }
-  // exp(s - max) to the slab: 64 columns at a time, staged per warp in a 32-row x 128-byte
-  // buffer (128-byte swizzle: 16-byte chunk j of row r at chunk j ^ (r % 8)) and written
-  // by one TMA bulk tensor store (whole lines; rows past the chunk hold values nothing
-  // reads, rows past R are clipped by the TMA unit)
+  // exp(s - max) to the slab, 64 columns at a time
   float sum = 0.0f;
   const float mxl = a.ref_mode ? 0.0f : mx * LOG2E;  // row-reference mode stores exp(s)
-  uint8_t* row = nullptr;
 #pragma unroll 1
   for (int c2 = 0; c2 < BN / 64; ++c2) {
-    uint8_t* buf = stg + (epi_it % NBUF) * EPI_BUF_BYTES;
-    row = buf + lane * 128;
-    if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last read this buffer is done
-    __syncwarp();
-#pragma unroll 1
-    for (int hh = 0; hh < 2; ++hh) {
-      uint32_t r[32];
-      tmem_ld32(taddr + c2 * 64 + hh * 32, r);
-      uint32_t pk[16];
+    uint32_t r[64];
+    tmem_ld64(taddr + c2 * 64, r);
+    uint32_t pk[32];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const int v = v0 + c2 * 64 + hh * 32 + j;
-        float s0 = __uint_as_float(r[j]) * ls, s1 = __uint_as_float(r[j + 1]) * ls;
-        float e0 = 0.0f, e1 = 0.0f;
-        if (v < V) {
-          if (bias != nullptr) s0 += to_f<T>(bias[v]);
-          e0 = ex2_fast(fmaf(s0, LOG2E, -mxl));
-        }
-        if (v + 1 < V) {
-          if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
-          e1 = ex2_fast(fmaf(s1, LOG2E, -mxl));
-        }
-        sum += e0 + e1;
-        pk[j / 2] = pack2<T>(e0, e1);
+    for (int j = 0; j < 64; j += 2) {
+      const int v = v0 + c2 * 64 + j;
+      float s0 = __uint_as_float(r[j]) * ls, s1 = __uint_as_float(r[j + 1]) * ls;
+      float e0 = 0.0f, e1 = 0.0f;
+      if (v < V) {
+        if (bias != nullptr) s0 += to_f<T>(bias[v]);
+        e0 = ex2_fast(fmaf(s0, LOG2E, -mxl));
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *(uint4*)(row + (((hh * 4 + j) ^ (lane & 7)) << 4)) =
-            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      if (v + 1 < V) {
+        if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
+        e1 = ex2_fast(fmaf(s1, LOG2E, -mxl));
+      }
+      sum += e0 + e1;
+      pk[j / 2] = pack2<T>(e0, e1);
     }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(tmS, smem_u32(buf), v0 + c2 * 64, mrow + q * 32);
-      bulk_commit();
-    }
-    ++epi_it;
+    store_slab64<T>(a, rr, v0 + c2 * 64, pk);
   }
   if (valid) {
     const int64_t o = (int64_t)rr * a.nvt + n;
     a.w.stm[o] = mx;
     a.w.sts[o] = sum;
     a.w.sti[o] = ai;
-    if (ht) a.w.tgt[rr] = tl;
+    if (toff >= 0) a.w.tgt[rr] = tl;
   }
 }
 
@@ -783,7 +803,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* epi_stage = smem + STAGES * SBYTES;
-  uint64_t* bars = (uint64_t*)(smem + STAGES * SBYTES + epi_bytes_of<NB>());
+  uint64_t* bars = (uint64_t*)(smem + STAGES * SBYTES + epi_bytes_m<MODE, NB>());
   uint32_t* tmem_slot = (uint32_t*)(bars + NUM_BARS);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   int* copies = (int*)(tmem_slot + 2);  // per stage: phases this CTA's producer filled / armed
@@ -959,9 +979,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((as * NB + j) * BN);
       if (nsub < ts.nsub) {
         if (MODE == FWD && a.ref_mode)
-          epilogue_fwd_ref<T, NBUF>(a, &tmC, stg, row0, rows, mrow, nsub, taddr, q, lane, epi_it);
+          epilogue_fwd_ref<T>(a, row0, rows, mrow, nsub, taddr, q, lane);
         else if (MODE == FWD)
-          epilogue_fwd<T, NBUF>(a, &tmC, stg, row0, rows, mrow, nsub, taddr, q, lane, epi_it);
+          epilogue_fwd<T>(a, row0, rows, mrow, nsub, taddr, q, lane);
         else if (MODE == DW && a.dW_dt != FLCE_F32)
           epilogue_reduce<NBUF, (NB == 2), T, half_bufs_of<NB>()>(a, &tmC, stg, mrow, nsub, (int)a.V, 0, taddr, q, lane, cb,
                                               nullptr, ovw, epi_it);
@@ -1056,7 +1076,7 @@ template <int MODE, typename T, int NB>
 cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
                      const CUtensorMap& B, const CUtensorMap& C, int64_t pair_tiles_max) {
   auto kern = k_gemm_tc<MODE, T, NB>;
-  constexpr int smem = smem_bytes<NB>();
+  constexpr int smem = smem_bytes<MODE, NB>();
   // per-device cache of the pairs that fit at once (the shared-memory attribute is set on
   // the first launch of each device); concurrent first launches may both set and store it
   static std::atomic<int> max_pairs[64];
@@ -1117,10 +1137,9 @@ cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 128)) return cudaErrorInvalidValue;
-  CUtensorMap C;  // the exp slab, written by the epilogue
-  if (!tc::make_map(&C, a.w.slab, a.dt, a.Vp, a.R, a.Vp * esz, 64, 32)) return cudaErrorInvalidValue;
   const int64_t tiles = ((a.R + 255) / 256) * a.nvt;
-  return tc::launch_mode<tc::FWD, 1>(a, chunk, s, A, B, C, tiles);
+  // the forward epilogue writes the slab with plain stores: the third map is not read
+  return tc::launch_mode<tc::FWD, 1>(a, chunk, s, A, B, B, tiles);
 }
 
 cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
