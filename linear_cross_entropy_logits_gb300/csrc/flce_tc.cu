@@ -608,6 +608,58 @@ __device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, int row0, in
   }
 }
 
+// Per-tile forward epilogue, first pass over 64 columns: max and lowest-index argmax (four
+// independent chains merged with lowest-index ties, as in the row-reference pass).
+template <typename T, bool FULL>
+__device__ __forceinline__ void fwd_tile_max(const CallArgs& a, const uint32_t (&r)[64], int vbase, float ls,
+                                             const T* bias, float& mx, int& ai) {
+  float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
+  int a4[4] = {ai, 0x7fffffff, 0x7fffffff, 0x7fffffff};
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    const int v = vbase + j;
+    float s = __uint_as_float(r[j]) * ls;
+    if (FULL || v < (int)a.V) {
+      if (bias != nullptr) s += to_f<T>(bias[v]);
+      if (s > m4[j & 3]) {
+        m4[j & 3] = s;
+        a4[j & 3] = v;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 1; k < 4; ++k)
+    if (m4[k] > m4[0] || (m4[k] == m4[0] && a4[k] < a4[0])) {
+      m4[0] = m4[k];
+      a4[0] = a4[k];
+    }
+  mx = m4[0];
+  ai = a4[0];
+}
+
+// Per-tile forward epilogue, second pass over 64 columns: exp(s - max) (base 2, mxl =
+// max * log2 e) packed for the slab, and their sum.
+template <typename T, bool FULL>
+__device__ __forceinline__ void fwd_tile_exp(const CallArgs& a, const uint32_t (&r)[64], int vbase, float ls,
+                                             const T* bias, float mxl, float& sum, uint32_t (&pk)[32]) {
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    const int v = vbase + j;
+    float s0 = __uint_as_float(r[j]) * ls, s1 = __uint_as_float(r[j + 1]) * ls;
+    float e0 = 0.0f, e1 = 0.0f;
+    if (FULL || v < (int)a.V) {
+      if (bias != nullptr) s0 += to_f<T>(bias[v]);
+      e0 = ex2_fast(fmaf(s0, LOG2E, -mxl));
+    }
+    if (FULL || v + 1 < (int)a.V) {
+      if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
+      e1 = ex2_fast(fmaf(s1, LOG2E, -mxl));
+    }
+    sum += e0 + e1;
+    pk[j / 2] = pack2<T>(e0, e1);
+  }
+}
+
 // Per-tile forward epilogue (fp16 inputs, dbias, the distillation op, a chunk outside the
 // row-reference window): a first pass over TMEM for the max / argmax / target logit, a
 // second for exp(s - max) into the slab.
@@ -616,7 +668,6 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
                                              uint32_t taddr, int q, int lane) {
   const int rr = mrow + q * 32 + lane;  // row within the chunk
   const bool valid = rr < rows;
-  const int V = (int)a.V;
   int toff = -1;
   const int v0 = n * VT;
   if (valid && a.targets != nullptr) {
@@ -625,6 +676,7 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
   }
   const float ls = a.logit_scale;
   const T* bias = (const T*)a.bias;
+  const bool full = v0 + BN <= (int)a.V;
   float mx = -INFINITY, tl = 0.0f;
   int ai = v0;
 #pragma unroll 1
@@ -632,18 +684,8 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
     uint32_t r[64];
     tmem_ld64(taddr + c2 * 64, r);
     pick_target<T>(r, toff - c2 * 64, v0 + toff, ls, bias, tl);
-#pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      const int v = v0 + c2 * 64 + j;
-      float s = __uint_as_float(r[j]) * ls;
-      if (v < V) {
-        if (bias != nullptr) s += to_f<T>(bias[v]);
-        if (s > mx) {
-          mx = s;
-          ai = v;
-        }
-      }
-    }
+    if (full) fwd_tile_max<T, true>(a, r, v0 + c2 * 64, ls, bias, mx, ai);
+    else fwd_tile_max<T, false>(a, r, v0 + c2 * 64, ls, bias, mx, ai);
   }
   // exp(s - max) to the slab, 64 columns at a time
   float sum = 0.0f;
@@ -653,22 +695,8 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
     uint32_t r[64];
     tmem_ld64(taddr + c2 * 64, r);
     uint32_t pk[32];
-#pragma unroll
-    for (int j = 0; j < 64; j += 2) {
-      const int v = v0 + c2 * 64 + j;
-      float s0 = __uint_as_float(r[j]) * ls, s1 = __uint_as_float(r[j + 1]) * ls;
-      float e0 = 0.0f, e1 = 0.0f;
-      if (v < V) {
-        if (bias != nullptr) s0 += to_f<T>(bias[v]);
-        e0 = ex2_fast(fmaf(s0, LOG2E, -mxl));
-      }
-      if (v + 1 < V) {
-        if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
-        e1 = ex2_fast(fmaf(s1, LOG2E, -mxl));
-      }
-      sum += e0 + e1;
-      pk[j / 2] = pack2<T>(e0, e1);
-    }
+    if (full) fwd_tile_exp<T, true>(a, r, v0 + c2 * 64, ls, bias, mxl, sum, pk);
+    else fwd_tile_exp<T, false>(a, r, v0 + c2 * 64, ls, bias, mxl, sum, pk);
     store_slab64<T>(a, rr, v0 + c2 * 64, pk);
   }
   if (valid) {
