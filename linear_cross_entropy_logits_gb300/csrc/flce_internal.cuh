@@ -17,6 +17,11 @@ namespace flce {
 // produces one (max, sum-exp, argmax) triple per row and per VT columns.
 constexpr int VT = 256;
 constexpr int CHUNK_ALIGN = 128;   // row-chunk granularity (one tensor-core M tile)
+// Tile-shape thresholds of the tensor-core GEMMs (the reasons are at their use in
+// flce_tc.cu): the dW GEMM takes 256 x 512 pair tiles from chunks of this many rows on, the
+// forward from this hidden size on.
+constexpr int DW_WIDE_MIN_ROWS = 4096;
+constexpr int FWD_WIDE_MIN_H = 4096;
 constexpr uint32_t DEFAULT_TIMEOUT_MS = 4000;
 // Default workspace budget: 3 GiB, about 1% of a GB300's 288 GB of HBM. It holds the
 // whole 8192-row chunk of a Llama-3.1-8B head (one pass of W per GEMM, one dW

@@ -58,11 +58,14 @@ enum Mode { FWD = 0, DX = 1, DW = 2 };
 // are bound by the operand feed), with one 512-column TMEM accumulator and eight epilogue
 // warps (one per TMEM lane quadrant and sub-tile). NB = 1: 256 x 256 tiles with two
 // 256-column accumulators, so that a tile's epilogue overlaps the next tile's mainloop.
-// The forward takes NB = 1 (its epilogue must overlap: the wide forward tile measured
-// slower); dX takes NB = 2 (K = V, the epilogue is negligible); dW takes NB = 2 when a
-// chunk holds at least DW_WIDE_MIN_ROWS rows (K long enough to amortise the exposed
-// reduce-add epilogue) and NB = 1 below that.
-constexpr int DW_WIDE_MIN_ROWS = 4096;
+// The forward takes NB = 2 when H >= FWD_WIDE_MIN_H and NB = 1 below (a short K cannot
+// hide the exposed epilogue of the single accumulator); dX takes NB = 2 (K = V, the
+// epilogue is negligible); dW takes NB = 2 when a chunk holds at least DW_WIDE_MIN_ROWS
+// rows (K long enough to amortise the exposed reduce-add epilogue) and NB = 1 below that.
+// DW_WIDE_MIN_ROWS, FWD_WIDE_MIN_H (flce_internal.cuh): the forward takes the wide tile
+// from H = 4096 on, where its K loop is long enough that the wide tile's smaller operand
+// traffic per FLOP outweighs its exposed epilogue (measured 1% faster at H = 4096, in short
+// and in power-capped runs; 10% slower at H = 2048).
 constexpr int A_BYTES = BM * BK * 2;               // 16 KB
 constexpr int B_BYTES = (BN / 2) * BK * 2;         // 16 KB per 256-column sub-tile
 template <int NB>
@@ -1165,9 +1168,10 @@ cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const uint64_t esz = 2;
   if (!tc::make_map(&A, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 128)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.W, a.dt, a.H, a.V, a.H * esz, 64, 128)) return cudaErrorInvalidValue;
-  const int64_t tiles = ((a.R + 255) / 256) * a.nvt;
+  const int64_t mt = (a.R + 255) / 256;
   // the forward epilogue writes the slab with plain stores: the third map is not read
-  return tc::launch_mode<tc::FWD, 1>(a, chunk, s, A, B, B, tiles);
+  if (a.H >= FWD_WIDE_MIN_H) return tc::launch_mode<tc::FWD, 2>(a, chunk, s, A, B, B, mt * ((a.nvt + 1) / 2));
+  return tc::launch_mode<tc::FWD, 1>(a, chunk, s, A, B, B, mt * a.nvt);
 }
 
 cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s) {
@@ -1188,7 +1192,7 @@ cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   if (!tc::make_map(&A, a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 64)) return cudaErrorInvalidValue;
   if (!tc::make_map(&B, a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 64)) return cudaErrorInvalidValue;
   CUtensorMap C;  // dW for the TMA reduce-add (or store) of the epilogue
-  const bool wide = a.R >= tc::DW_WIDE_MIN_ROWS;
+  const bool wide = a.R >= DW_WIDE_MIN_ROWS;
   if (a.dW_dt == FLCE_F32) {
     if (!tc::make_map(&C, a.dW, FLCE_F32, a.H, a.V, a.H * 4, wide ? 16 : 32, 32,
                       wide ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))

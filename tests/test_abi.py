@@ -183,7 +183,9 @@ def test_plan_describe(lib):
     txt = flce.describe_plan(BT, H, V, torch.bfloat16, wb)
     assert f"chunk rows R={R}," in txt and "cdiv(BT,R)=1 " in txt
     assert "vocabulary tiles: 501 x 256 columns" in txt
-    assert f"forward {((R + 255) // 256) * 501} tiles of 256x256" in txt
+    assert f"forward {((R + 255) // 256) * 251} tiles of 256x512" in txt  # H >= 4096: wide tile
+    t2 = flce.describe_plan(BT, 2048, V, torch.bfloat16)
+    assert "forward " in t2 and "tiles of 256x256;" in t2
     assert "dW 4008 tiles of 256x512" in txt
     assert "workspace slab   at" in txt and str(R * 128256 * 2) in txt
     n = lib.flce_plan_describe(BT, H, V, 1, wb, None, 0)

@@ -38,6 +38,11 @@ SMALL = [
                                  ignore="random", n_ignored=5)),
     ("bf16_tiny_H64", "llama1b", dict(BT=130, H=64, V=1000, w_std=0.3, ignore="random",
                                       n_ignored=3)),
+    # H >= 4096: the forward runs on 256 x 512 tiles (ragged last tile: 12 of 13 sub-tiles)
+    ("bf16_wide_fwd_H4096", "llama1b", dict(BT=300, H=4096, V=3100, w_std=0.03, ignore="random",
+                                            n_ignored=40)),
+    ("f16_wide_fwd_H4096_bias", "frozen_head", dict(BT=260, H=4096, V=2000, dtype="f16", w_std=0.03,
+                                                    bias_std=0.3, n_ignored=30)),
 ]
 
 

@@ -72,10 +72,13 @@ def test_row_reference_matches_oracle_and_tile_form(name, base, ov):
     assert rel_fro(g_ref["dX"], g_tile["dX"]) < 1e-2
 
 
-def test_large_logits_fall_back_per_tile():
+@pytest.mark.parametrize("H", [256, 4096])
+def test_large_logits_fall_back_per_tile(H):
     """Row maxima far above the window (X scaled so that |s| reaches ~100): the chunk is
-    redone with per-tile maxima and still matches the oracle."""
-    sp = I.spec("llama1b", BT=300, H=256, V=3000, x_std=4.0, w_std=0.4, ignore="random", n_ignored=20)
+    redone with per-tile maxima and still matches the oracle (H = 4096: on the wide forward
+    tile)."""
+    sp = I.spec("llama1b", BT=300, H=H, V=3000, x_std=4.0, w_std=6.4 / H ** 0.5, ignore="random",
+                n_ignored=20)
     inp = I.generate(sp, seed=12)
     o = run_oracle(inp, sp)
     assert np.max(o["lse_tok"]) > 80.0

@@ -22,8 +22,9 @@ def _lib():
     flce.load()
 
 
-def test_stalled_pipeline_reports_timeout_and_context_survives():
-    sp = I.spec("llama1b", BT=512, H=256, V=4000, w_std=0.2, ignore="random", n_ignored=64)
+@pytest.mark.parametrize("H", [256, 4096])  # 256 x 256 and 256 x 512 forward tiles
+def test_stalled_pipeline_reports_timeout_and_context_survives(H):
+    sp = I.spec("llama1b", BT=512, H=H, V=4000, w_std=3.2 / H ** 0.5, ignore="random", n_ignored=64)
     inp = I.generate(sp, seed=30)
     d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
 
