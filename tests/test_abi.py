@@ -200,3 +200,18 @@ def test_plan_describe(lib):
     assert lib.flce_plan_describe(0, H, V, 1, wb, None, 0) == -1
     assert lib.flce_plan_describe(BT, H, V, 7, wb, None, 0) == -1
     assert lib.flce_plan_describe(BT, H, V, 1, 1024, None, 0) == -1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), flce.FLCE_ERR_INVALID_ARG),                    # a caller workspace is given
+    (dict(workspace=None), flce.FLCE_ERR_INVALID_ARG),      # ... or its size
+    (dict(workspace=None, workspace_bytes=0, BT=0), flce.FLCE_ERR_INVALID_ARG),
+    (dict(workspace=None, workspace_bytes=0, in_dtype=7), flce.FLCE_ERR_INVALID_ARG),
+    (dict(workspace=None, workspace_bytes=0, H=4096, V=10_000_000), flce.FLCE_ERR_SCRATCH_LIMIT),
+])
+def test_noalloc_host_rejections(lib, kw, code):
+    """The scratch-only entry point refuses a caller workspace and problems whose 128-row
+    chunk exceeds its fixed scratch, on the host, before any CUDA call."""
+    a = _args(**kw)
+    assert lib.flce_fwd_bwd_noalloc(ctypes.byref(a), None) == code
+    assert lib.flce_fwd_bwd_noalloc(None, None) == flce.FLCE_ERR_INVALID_ARG
