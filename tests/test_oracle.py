@@ -343,3 +343,47 @@ def test_planted_mistakes_are_caught(monkeypatch):
 
     monkeypatch.setattr(orc, "grad_scales", bt_divisor)
     assert _fd_errors("mean", 0.0) > 1e-3
+
+
+# --------------------------------------------------------------------------- argmax tie band
+
+def _fp32_dot(x, w, order):
+    """x . w in fp32: each product rounded to fp32, summed one term at a time in `order`."""
+    acc = np.float32(0.0)
+    for h in order:
+        acc = np.float32(acc + np.float32(np.float32(x[h]) * np.float32(w[h])))
+    return acc
+
+
+def test_argmax_tie_band_bounds_fp32_logit_error():
+    """The band accepts an argmax mismatch only where fp32 evaluation could produce one.
+    (1) Logits of bf16-exact values evaluated in fp32 (sequential, reversed and numpy's own
+    order, then an fp32 bias add) stay within one logit's share of the band (half of it) of
+    the float64 value on 240 random row / vocabulary pairs. (2) The worst case the bound is
+    written for, reached: x = w = (2^12, 1, ..., 1) summed left to right in fp32 keeps
+    rounding 2^24 + 1 back to 2^24, an error of H - 1, which the band covers and a bound
+    without its factor H (u times the absolute dot product) would not."""
+    rng = np.random.default_rng(5)
+    H = 512
+    X = torch.from_numpy(rng.standard_normal((8, H))).to(torch.bfloat16).double().numpy()
+    W = torch.from_numpy(rng.standard_normal((30, H)) * 0.05).to(torch.bfloat16).double().numpy()
+    b = torch.from_numpy(rng.standard_normal(30) * 0.3).to(torch.bfloat16).double().numpy()
+    bmax = float(np.max(np.abs(b)))
+    for i in range(X.shape[0]):
+        absdot = orc._absdot_max(np.abs(X[i:i + 1]), W)[0]
+        half_band = orc.argmax_tie_band(absdot, bmax, H) / 2.0
+        for v in range(W.shape[0]):
+            exact = float(X[i] @ W[v]) + b[v]
+            for order in (range(H), range(H - 1, -1, -1), None):
+                d = (X[i].astype(np.float32) @ W[v].astype(np.float32) if order is None
+                     else _fp32_dot(X[i], W[v], order))
+                got = float(np.float32(d + np.float32(b[v])))
+                assert abs(got - exact) <= half_band, (i, v, order)
+    x = np.ones(H)
+    x[0] = 4096.0
+    exact = float(x @ x)
+    err = abs(float(_fp32_dot(x, x, range(H))) - exact)
+    assert err == H - 1
+    absdot = float(np.abs(x) @ np.abs(x))
+    assert err <= orc.argmax_tie_band(absdot, 0.0, H) / 2.0
+    assert err > 2.0 ** -23 * absdot  # what a bound without the factor H would allow
