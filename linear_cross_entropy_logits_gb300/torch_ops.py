@@ -114,14 +114,20 @@ class FusedLinearCrossEntropy(torch.autograd.Function):
                 db = db * g.to(db.dtype) if (need_w and ctx.has_bias) else db
             else:
                 # eager: scale the op's own gradient buffers in place on the device; nothing
-                # is done (no pass over dW) when the upstream gradient is exactly 1
+                # is done (no pass over dW) when the upstream gradient is exactly 1. A second
+                # backward through the same graph (retain_graph) finds the buffers already
+                # scaled by the previous upstream gradient and applies only the ratio (so it
+                # cannot follow a first backward whose upstream gradient was exactly 0).
                 g = g_loss.reshape(1).float().contiguous()
+                prev = getattr(ctx, "applied_scale", None)
+                r = g if prev is None else (g / prev).contiguous()
+                ctx.applied_scale = g.clone()
                 if need_x:
-                    flce.scale_by(dX, g)
+                    flce.scale_by(dX, r)
                 if need_w:
-                    flce.scale_by(dW, g)
+                    flce.scale_by(dW, r)
                     if ctx.has_bias:
-                        flce.scale_by(db, g)
+                        flce.scale_by(db, r)
         return (dX if need_x else None, dW if need_w else None, None,
                 db if (need_w and ctx.has_bias) else None, None, None, None, None)
 

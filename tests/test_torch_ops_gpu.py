@@ -94,3 +94,20 @@ def test_autograd_upstream_gradient_scales():
         assert rel_fro(X.grad.float().cpu().numpy(), scale * o["dX"]) <= TOL["bf16"]["grad"]
         assert rel_fro(W.grad.float().cpu().numpy(), scale * o["dW"]) <= TOL["bf16"]["grad"]
 
+
+
+def test_second_backward_through_a_retained_graph():
+    """loss.backward(retain_graph=True) with an upstream gradient of 2.5, then again with 1:
+    the in-place scaling of the op's gradient buffers must not compound (each backward
+    adds its own scale times the gradient)."""
+    from linear_cross_entropy_logits_gb300.torch_ops import fused_linear_cross_entropy
+    sp = I.spec("llama1b", BT=300, H=192, V=3000, w_std=0.2, ignore="random", n_ignored=40)
+    inp = I.generate(sp, seed=32)
+    o = run_oracle(inp, sp)
+    X = inp["X"].cuda().requires_grad_(True)
+    W = inp["W"].cuda().requires_grad_(True)
+    loss = fused_linear_cross_entropy(X, W, inp["targets"].cuda(), accum_dtype=torch.float32)
+    loss.backward(torch.tensor(2.5, device="cuda"), retain_graph=True)
+    loss.backward()
+    assert rel_fro(X.grad.float().cpu().numpy(), 3.5 * o["dX"]) <= TOL["bf16"]["grad"]
+    assert rel_fro(W.grad.float().cpu().numpy(), 3.5 * o["dW"]) <= TOL["bf16"]["grad"]
