@@ -4,14 +4,16 @@
 //
 // One kernel template serves the three products of the method:
 //   FWD: S = Xc W^T (K = H). The epilogue never writes S: per row and per 256-column
-//        vocabulary tile it keeps the max, the sum of exp(s - max), the lowest-index
-//        argmax and the target logit, and stores exp(s - max) (in the input dtype) into
-//        the chunk slab, from which the gradient is formed once the row's lse is known.
-//   DX:  dX[idx] = cbar * G W (K = V): tiles (optionally split in two K halves) added by
-//        TMA reduce-add into a zeroed fp32 chunk buffer, then scattered to the dX rows
-//        through the compaction index by k_dx_store.
-//   DW:  dW += cbar * G^T Xc (K = chunk rows), added into the fp32 destination by TMA
-//        reduce-add from the single CTA that owns each tile (one add per element per
+//        vocabulary tile it keeps the max, the sum of the exponentials, the lowest-index
+//        argmax and the target logit, and writes exp(s) (row-reference form) or
+//        exp(s - tile max) (per-tile form), in the input dtype, from registers into the
+//        chunk slab, from which the gradient is formed once the row's lse is known.
+//   DX:  dX[idx] = cbar * G W (K = V): tiles, optionally split in up to four K ranges,
+//        added by TMA reduce-add into two zeroed fp32 chunk buffers (at most two adds per
+//        element, onto zero), then summed and scattered to the dX rows through the
+//        compaction index by k_dx_store.
+//   DW:  dW += cbar * G^T Xc (K = chunk rows), added into the destination by TMA
+//        reduce-add from the single CTA pair that owns each tile (one add per element per
 //        launch: deterministic).
 // The three products are the logits, grad_input and grad_weight GEMMs that the pages'
 // op runs in its forward ("Liger-Kernel PR #1554: skip ignore_index rows", Summary); dW is
@@ -19,21 +21,23 @@
 // weight-gradient allocation overhead across FP16, BF16, and FP32", Proposed direction).
 //
 // Launch shape: clusters of 2 CTAs (one CTA pair = two SMs of a TPC), one CTA per SM,
-// persistent over pair tiles of 256 (M) x 256 (N). The pair runs
-// tcgen05.mma.cta_group::2 with M = 256: each CTA stages its own 128 rows of A and one
-// half (128 rows) of B, and holds its 128 x 256 fp32 accumulator in its own TMEM. Per CTA
-// and k-block of 64 this is 32 KB of shared memory for 512 tensor cycles, two thirds of
-// the traffic of a 128 x 256 single-CTA tile, which leaves room for 6 stages (192 KB).
+// persistent over pair tiles of 256 (M) x 256 or 256 x 512 (N). The pair runs
+// tcgen05.mma.cta_group::2 with M = 256 and N = 256: each CTA stages its own 128 rows of A
+// and one half (128 rows) of each B sub-tile, and holds its 128-row fp32 accumulator in its
+// own TMEM. 256 x 256 tiles (6 stages of 32 KB) keep two accumulators, so a tile's
+// epilogue overlaps the next tile's mainloop; 256 x 512 tiles (4 stages of 48 KB) issue two
+// MMAs per staged A block, a quarter less operand traffic per FLOP, with one 512-column
+// accumulator whose epilogue is exposed.
 //
-// Warp roles (192 threads per CTA):
+// Warp roles (320 threads per CTA):
 //   warp 0        TMA producer (one thread) in both CTAs; the peer's copies complete on
 //                 the leader's "full" barrier, which the leader arms for both halves
 //   warp 1        TMEM allocator (both CTAs) and, in the leader CTA, the MMA issuer (one
 //                 thread); its commits arrive on both CTAs' "empty" / "tmem full" barriers
-//   warps 2..5    epilogue in both CTAs; warp w reads TMEM lanes 32*(w%4) .. +31 and both
-//                 CTAs' epilogues arrive on the leader's "tmem empty" barrier
-// Two 256-column TMEM accumulators let the epilogue of one tile overlap the mainloop of
-// the next. Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+//   warps 2..9    epilogue in both CTAs (2..5 only on 256 x 256 tiles); warp w reads TMEM
+//                 lanes 32*(w%4) .. +31 of sub-tile (w-2)/4, and both CTAs' epilogues
+//                 arrive on the leader's "tmem empty" barrier
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // FLCE_ERR_TIMEOUT, tells its peer, and both leave their loops; before TMEM is freed the
 // pair reconciles the copies each CTA issued against the leader's barriers and waits
 // (bounded) for them and for the MMAs in flight.
