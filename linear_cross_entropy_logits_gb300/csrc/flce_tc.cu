@@ -76,8 +76,8 @@ template <int NB>
 __host__ __device__ constexpr int stage_bytes() {
   return A_BYTES + NB * B_BYTES;                   // 32 or 48 KB per CTA
 }
-// Pipeline depth: 192 KB of stages (6 x 32 KB or 4 x 48 KB) next to 32 KB of epilogue
-// staging.
+// Pipeline depth: 192 KB of stages (6 x 32 KB or 4 x 48 KB), next to the dX / dW epilogue
+// staging (the forward stages nothing).
 #ifndef FLCE_WIDE_STAGES
 #define FLCE_WIDE_STAGES 4
 #endif
