@@ -147,7 +147,8 @@ typedef struct flce_args {
   void* dW;                 /* [V,H] dW_dtype, ACCUMULATED (+=); zero it for a fresh grad,
                                or pass FLCE_FLAG_DW_OVERWRITE                            */
   void* dbias;              /* [V] dW_dtype, ACCUMULATED (or overwritten, as dW); used
-                               when bias and want_dW                                     */
+                               when bias and want_dW; NULL: the bias gradient is not
+                               wanted                                                    */
   /* scratch and status */
   void* workspace;          /* device scratch of workspace_bytes, caller-owned           */
   size_t workspace_bytes;   /* >= flce_workspace_size(BT,H,V,in_dtype,0) or any size
