@@ -5,9 +5,10 @@ Tolerances (fixed by the method's contract, not tuned to results):
   * bf16/fp16 inputs: loss and per-token loss/lse relative error <= 2e-3; dX and dW
     relative Frobenius error <= 1e-2.
   * fp32 inputs: all of the above <= 1e-5.
-  * Prediction and ignored-row mask: bit exact, except on rows whose two largest oracle
-    logits are closer than the fp32 evaluation bound (oracle.argmax_tie_band), where
-    either of the tied indices is accepted.
+  * Prediction and ignored-row mask: bit exact, except on rows whose two competing oracle
+    logits are closer than fp32 evaluation can resolve (four times their spread over
+    several fp32 accumulation orders, pred_ok), where either index is accepted; the number
+    of such rows is capped (max_argmax_mismatches) and reported.
 """
 
 import numpy as np
@@ -71,23 +72,75 @@ def run_oracle(inp, sp):
                            want_dX=sp.get("want_dX", True), want_dW=sp.get("want_dW", True))
 
 
-def pred_ok(gpu_pred, orc_pred, X, W, b, rows, targets_mask):
-    """Bit-exact predictions except within the fp32 tie band of a row."""
+def _round_f32(v, toward_zero):
+    """float64 -> float32, to nearest or toward zero."""
+    r = np.float32(v)
+    if toward_zero and abs(float(r)) > abs(float(v)):
+        r = np.nextafter(r, np.float32(0.0))
+    return r
+
+
+def fp32_logit_spread(x, w, b=0.0):
+    """How far fp32 evaluations of one logit x.w + b stray from its float64 value, over the
+    accumulation orders a tensor-core GEMM or a CPU may use: one term at a time, numpy's
+    pairwise float32 sum, and blocks of 16 exact products (one MMA's K step) added to an
+    fp32 accumulator rounded to nearest or toward zero; each followed by an fp32 bias add.
+    The inputs are bf16/fp16/fp32 values, whose products are exact in fp32."""
+    x = np.asarray(x, np.float64)
+    w = np.asarray(w, np.float64)
+    exact = float(x @ w) + float(b)
+    p = x * w                                  # exact products
+    outs = []
+    acc = np.float32(0.0)
+    for v in p:                                # sequential
+        acc = np.float32(acc + np.float32(v))
+    outs.append(acc)
+    outs.append(np.sum(p.astype(np.float32)))  # pairwise
+    for rz in (False, True):                   # K blocks of 16, fp32 accumulator
+        acc = np.float32(0.0)
+        for k0 in range(0, p.size, 16):
+            acc = _round_f32(float(acc) + float(np.sum(p[k0:k0 + 16])), rz)
+        outs.append(acc)
+    return max(abs(float(np.float32(o + np.float32(b))) - exact) for o in outs)
+
+
+def pred_ok(gpu_pred, orc_pred, X, W, b, rows, targets_mask, report=None):
+    """Predictions bit exact, except on rows where the two competing logits lie closer in
+    float64 than fp32 evaluation can resolve: the gap between the oracle's maximum and the
+    logit the GPU picked must be within four times the sum of the two logits' fp32 spreads
+    (fp32_logit_spread), with a floor of four fp32 ulps of the larger logit. Returns
+    (ok, n_mismatches) or (False, row) at the first mismatch outside that; appends
+    (row, gap, bound) per accepted mismatch to ``report`` when given."""
     bad = np.nonzero(gpu_pred != orc_pred)[0]
     if bad.size == 0:
         return True, 0
-    H = X.shape[1]
-    bmax = 0.0 if b is None else float(np.max(np.abs(b)))
     for j in bad:
         r = rows[j]
         if not targets_mask[j]:
             return False, int(r)
-        s = orc.logits_rows(np.asarray(X[r:r + 1], np.float64), W, b)[0]
-        absdot = orc._absdot_max(np.abs(np.asarray(X[r:r + 1], np.float64)), W)[0]
-        band = orc.argmax_tie_band(absdot, bmax, H)
-        if s[gpu_pred[j]] < s.max() - band:
+        x = np.asarray(X[r], np.float64)
+        s = orc.logits_rows(x[None, :], W, b)[0]
+        a, g = int(orc_pred[j]), int(gpu_pred[j])
+        if not (0 <= g < s.shape[0]):
             return False, int(r)
+        ba = 0.0 if b is None else float(b[a])
+        bg = 0.0 if b is None else float(b[g])
+        spread = fp32_logit_spread(x, W[a], ba) + fp32_logit_spread(x, W[g], bg)
+        ulp = float(np.spacing(np.float32(max(abs(s[a]), abs(s[g])))))
+        bound = max(4.0 * spread, 4.0 * ulp)
+        gap = float(s[a] - s[g])
+        if gap > bound:
+            return False, int(r)
+        if report is not None:
+            report.append((int(r), gap, bound))
     return True, int(bad.size)
+
+
+def max_argmax_mismatches(n_rows):
+    """Cap on accepted near-tie mismatches among n_rows: at these workloads' logit spreads
+    (top-1/top-2 gaps of order 0.1, fp32 errors of order 1e-5) well under one row in a
+    thousand can be a near tie."""
+    return 2 + n_rows // 4096
 
 
 def compare_full(g, o, inp, sp):
@@ -124,7 +177,8 @@ def compare_full(g, o, inp, sp):
     b = I.to_numpy_exact(inp["bias"])
     rows = np.arange(BT)
     ok, nties = pred_ok(g["pred"], o["pred_tok"], X, W, b, rows, mask)
-    assert ok, f"argmax mismatch outside the tie band at row {nties}"
+    assert ok, f"argmax mismatch outside the fp32 spread at row {nties}"
+    assert nties <= max_argmax_mismatches(int(mask.sum())), f"{nties} near-tie argmax mismatches"
     # accuracy follows the prediction
     exp_acc = (g["pred"] == inp["targets"].numpy()).astype(np.float64) * mask
     if sp["reduction"] == "none":

@@ -387,3 +387,33 @@ def test_argmax_tie_band_bounds_fp32_logit_error():
     absdot = float(np.abs(x) @ np.abs(x))
     assert err <= orc.argmax_tie_band(absdot, 0.0, H) / 2.0
     assert err > 2.0 ** -23 * absdot  # what a bound without the factor H would allow
+
+
+def test_vocabulary_blocks_match_torch_float64():
+    """The oracle converts and multiplies W in vocabulary blocks of 32768 rows
+    (logits_rows, dX_rows, _absdot_max). At V = 70000 (three blocks, a ragged last one) the
+    blocked evaluation must equal torch's float64 cross entropy + autograd over the whole
+    vocabulary, and the blocked max |x|.|w| the unblocked one; the target and argmax of some
+    rows are placed in the second and third blocks."""
+    rng = np.random.default_rng(21)
+    BT, H, V = 6, 8, 70000
+    X = rng.standard_normal((BT, H))
+    W = rng.standard_normal((V, H)) * 0.3
+    b = rng.standard_normal(V) * 0.1
+    t = np.array([5, 32767, 32768, 65535, 69999, -100])
+    W[40000] = 3.0 * X[1] / np.linalg.norm(X[1])   # row 1's argmax in the second block
+    W[69000] = 3.0 * X[2] / np.linalg.norm(X[2])   # row 2's argmax in the last block
+    for red in ("mean", "none"):
+        g = np.linspace(0.5, 1.5, BT) if red == "none" else np.array([1.3])
+        r = orc.flce_oracle(X, W, t, bias=b, reduction=red, z_loss_scale=1e-3, grad_out=g)
+        loss, dX, dW, db, am = _torch_reference(X, W, b, t, red, 1e-3, g)
+        assert np.allclose(r["loss"], loss, rtol=1e-12, atol=1e-12)
+        assert np.allclose(r["dX"], dX, rtol=1e-10, atol=1e-13)
+        assert np.allclose(r["dW"], dW, rtol=1e-10, atol=1e-15)
+        assert np.allclose(r["dbias"], db, rtol=1e-10, atol=1e-15)
+        lab = t != -100
+        assert np.array_equal(r["pred_tok"][lab], am[lab])
+    assert r["pred_tok"][1] == 40000 and r["pred_tok"][2] == 69000
+    xa = np.abs(X)
+    assert np.allclose(orc._absdot_max(xa, W), (xa @ np.abs(W).T).max(axis=1), rtol=1e-14)
+    assert np.allclose(orc._absdot_max(xa, W, v_block=1000), orc._absdot_max(xa, W), rtol=1e-14)
