@@ -65,11 +65,18 @@ def parse():
     p.add_argument("--labelled-fraction", type=float, default=None)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-seconds", type=float, default=20.0,
+                   help="timed oracle seconds of the cpu_baseline leg")
     p.add_argument("--ref-seconds", type=float, default=100.0,
                    help="total oracle time budget of the --impl reference arm")
     p.add_argument("--bt", type=int, default=None,
                    help="override BT (smaller cases for profiler captures)")
+    p.add_argument("--bounded-budget-gib", type=float, default=1.5,
+                   help="also time the step at this workspace budget when the default one "
+                        "holds the slab of every row (0: skip)")
+    p.add_argument("--budget-gib", type=float, default=None,
+                   help="workspace budget in GiB (default: the workload's cap, else the "
+                        "library's default); sets the chunk rows R")
     return p.parse_args()
 
 
@@ -81,6 +88,8 @@ def workload_spec(args):
         ov["BT"] = args.bt
     if getattr(args, "dtype", None) is not None:
         ov["dtype"] = args.dtype
+    if getattr(args, "budget_gib", None) is not None:
+        ov["workspace_cap"] = int(args.budget_gib * 2 ** 30)
     return I.spec(args.workload, **ov)
 
 
@@ -110,19 +119,71 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def peak_for_region(peaks, src, region_ms):
+    """The bf16 denominator for a timed region: the burst figure (cuBLAS timed alone) for a
+    region under two seconds, which runs mostly before the power cap pulls the clocks
+    down; the sustained figure (cuBLAS back to back for seconds) for a longer one."""
+    if region_ms < 2000.0 or "bf16_tflops_sustained" not in peaks:
+        return peaks["bf16_tflops"], f"bf16 burst ({src}; timed region {region_ms / 1000.0:.2f} s < 2 s)"
+    return peaks["bf16_tflops_sustained"], f"bf16 sustained ({src}; timed region {region_ms / 1000.0:.1f} s)"
+
+
+def fp32_fma_peak(peaks, dev):
+    """FP32 FMA peak of the GPU from its unit counts and clock: 128 FP32 lanes per SM, two
+    FLOPs per FMA, at the maximum SM clock."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = peaks.get("sm_max_mhz", 2070.0)
+    return 2.0 * 128 * sms * mhz * 1e6 / 1e12, f"fp32 FMA: 2 x 128 lanes x {sms} SMs x {mhz:.0f} MHz"
+
+
+def cpu_baseline_subprocess(args):
+    """The oracle timed in a fresh process (this process's CUDA and threading state slowed
+    the oracle's BLAS calls by 2x): the --impl reference arm of this script on the same
+    workload, 2 steps of cpu_seconds/2 after a short warm-up. Returns its cpu_baseline."""
+    argv = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--op", args.op,
+            "--workload", args.workload, "--steps", "2", "--warmup", "1",
+            "--ref-seconds", str(1.5 * args.cpu_seconds)]
+    for flag, v in (("--labelled-fraction", args.labelled_fraction), ("--bt", args.bt),
+                    ("--dtype", args.dtype), ("--budget-gib", args.budget_gib)):
+        if v is not None:
+            argv += [flag, str(v)]
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE")}
+    r = subprocess.run(argv, capture_output=True, text=True, env=env, timeout=600)
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    if r.returncode != 0 or not lines:
+        return {"value": None, "error": (r.stderr or r.stdout)[-300:]}
+    ref = json.loads(lines[-1])
+    cb = dict(ref["cpu_baseline"])
+    cb["process"] = "fresh subprocess (bench.py --impl reference, 2 steps)"
+    return cb
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi samples every 50 ms, time-stamped on arrival by a reader thread; the
+    summary keeps only the samples taken inside the timed region (mark_start / mark_end),
+    so that idle clocks before or after it do not enter the median."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, dev):
         self.proc = None
         self.dev = dev
+        self.rows = []
+        self.t0 = self.t1 = None
+        self.thread = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            if line.count(",") >= 8:
+                self.rows.append((time.perf_counter(), line.strip().split(",")))
 
     def start(self):
+        import threading
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "200"]
+               "-lms", str(self.PERIOD_MS)]
         try:
             uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
             cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
@@ -130,56 +191,94 @@ class ClockSampler:
             pass
         try:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
-                                         text=True)
+                                         text=True, bufsize=1)
         except Exception:
             self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
         time.sleep(0.3)
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(2 * self.PERIOD_MS / 1000.0)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        # a sample reports the state of the preceding period: keep those that arrive
+        # inside the region, plus the first one after it
+        lo = self.t0 if self.t0 is not None else -float("inf")
+        hi = (self.t1 if self.t1 is not None else float("inf")) + self.PERIOD_MS / 1000.0
+        inside = [r for t, r in self.rows if lo <= t <= hi]
+        rows = inside if inside else [r for _, r in self.rows]
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        pw = [v for v in (num(r[3]) for r in rows) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "in_timed_region": bool(inside),
+                "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(pw) if pw else None,
+                "period_ms": self.PERIOD_MS}
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def oracle_sample_rate(sp, inp, seconds, rows_per_call=32, rng_seed=99):
-    """Time the float64 oracle (as it stands) on seeded samples of labelled rows of this
-    workload until about `seconds` of CPU work; returns (BT-tokens per second, rows,
-    seconds). Ignored rows cost the oracle nothing, so labelled rows per second are scaled
-    by BT / n_labelled to the metric's BT-token convention."""
-    from oracle import flce_oracle as orc
+def oracle_prepare(sp, inp):
+    """Untimed set-up of the oracle timing: the head weight (and bias) converted to float64
+    once, the labelled rows listed. The timed calls then run the oracle on float64 arrays,
+    on which its own per-block conversions are no-ops."""
     t = inp["targets"].numpy()
-    lab = np.nonzero(t != I.IGNORE_INDEX)[0]
-    W = I.to_numpy_exact(inp["W"])
-    b = I.to_numpy_exact(inp["bias"])
-    X = inp["X"]
-    go = inp["grad_out"].numpy() if inp["grad_out"] is not None else None
+    return {"sp": sp, "t": t, "lab": np.nonzero(t != I.IGNORE_INDEX)[0],
+            "W": I.to_numpy_exact(inp["W"]).astype(np.float64),
+            "b": None if inp["bias"] is None else I.to_numpy_exact(inp["bias"]).astype(np.float64),
+            "X": inp["X"],
+            "go": inp["grad_out"].numpy() if inp["grad_out"] is not None else None}
+
+
+def oracle_sample_rate(prep, seconds, rows_per_call=32, rng_seed=99, warmup_calls=1):
+    """Time the float64 oracle (as it stands) on seeded samples of labelled rows of this
+    workload until about `seconds` of CPU work, after `warmup_calls` untimed calls; returns
+    (BT-tokens per second, rows, seconds). Ignored rows cost the oracle nothing, so labelled
+    rows per second are scaled by BT / n_labelled to the metric's BT-token convention."""
+    from oracle import flce_oracle as orc
+    sp, t, lab, W, b, X, go = (prep[k] for k in ("sp", "t", "lab", "W", "b", "X", "go"))
     rng = np.random.default_rng(rng_seed)
-    done, spent = 0, 0.0
-    while spent < seconds and done < lab.size:
-        rows = np.sort(rng.choice(lab, size=min(rows_per_call, lab.size), replace=False))
-        Xs = I.to_numpy_exact(X[torch.from_numpy(rows)])
+
+    def call(rows):
+        Xs = I.to_numpy_exact(X[torch.from_numpy(rows)]).astype(np.float64)
         gs = go[rows] if (go is not None and sp["reduction"] == "none") else None
         t0 = time.perf_counter()
         orc.flce_oracle(Xs, W, t[rows], bias=b, reduction=sp["reduction"],
                         z_loss_scale=sp.get("z", 0.0), grad_out=gs, want_dX=True,
                         want_dW=sp["want_dW"])
-        spent += time.perf_counter() - t0
+        return time.perf_counter() - t0
+
+    for _ in range(warmup_calls):
+        call(np.sort(rng.choice(lab, size=min(rows_per_call, lab.size), replace=False)))
+    done, spent = 0, 0.0
+    while spent < seconds:
+        rows = np.sort(rng.choice(lab, size=min(rows_per_call, lab.size), replace=False))
+        spent += call(rows)
         done += rows.size
     rate_lab = done / spent
     return rate_lab * sp["BT"] / max(lab.size, 1), done, spent
@@ -192,13 +291,16 @@ def jsd_oracle_sample_rate(sp, inp, seconds, rows_per_call=16, rng_seed=7):
     from oracle import jsd_oracle as jo
     lab_all = inp["labels"].numpy()
     lab = np.nonzero(lab_all != I.IGNORE_INDEX)[0]
-    Ws, Wt = I.to_numpy_exact(inp["Ws"]), I.to_numpy_exact(inp["Wt"])
+    # the heads converted to float64 once, outside the timed calls
+    Ws = I.to_numpy_exact(inp["Ws"]).astype(np.float64)
+    Wt = I.to_numpy_exact(inp["Wt"]).astype(np.float64)
     rng = np.random.default_rng(rng_seed)
     done, spent = 0, 0.0
-    while spent < seconds and done < lab.size:
+    while spent < seconds:
         rows = np.sort(rng.choice(lab, size=min(rows_per_call, lab.size), replace=False))
         idx = torch.from_numpy(rows)
-        xs, xt = I.to_numpy_exact(inp["Xs"][idx]), I.to_numpy_exact(inp["Xt"][idx])
+        xs = I.to_numpy_exact(inp["Xs"][idx]).astype(np.float64)
+        xt = I.to_numpy_exact(inp["Xt"][idx]).astype(np.float64)
         t0 = time.perf_counter()
         jo.jsd_oracle(xs, Ws, xt, Wt, lab_all[rows], beta=sp["beta"], temperature=sp["temperature"],
                       reduction=sp["reduction"], want_dX=True, want_dW=sp["want_dW"])
@@ -270,13 +372,13 @@ def run_reference(args):
     sp = workload_spec(args)
     inp = I.generate(sp, seed=0)
     n_lab = int((inp["targets"] != I.IGNORE_INDEX).sum())
+    prep = oracle_prepare(sp, inp)
     per_step_seconds = max(min(2.0, args.ref_seconds), args.ref_seconds / max(args.steps + args.warmup, 1))
     for _ in range(args.warmup):
-        oracle_sample_rate(sp, inp, per_step_seconds / 4, rng_seed=1)
-    rates, rows_total, secs_total = [], 0, 0.0
+        oracle_sample_rate(prep, per_step_seconds / 4, rng_seed=1)
+    rows_total, secs_total = 0, 0.0
     for k in range(args.steps):
-        r, rows, secs = oracle_sample_rate(sp, inp, per_step_seconds, rng_seed=100 + k)
-        rates.append(r)
+        _, rows, secs = oracle_sample_rate(prep, per_step_seconds, rng_seed=100 + k, warmup_calls=0)
         rows_total += rows
         secs_total += secs
     value = rows_total * sp["BT"] / max(n_lab, 1) / secs_total
@@ -288,10 +390,15 @@ def run_reference(args):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.Generator)",
         "config": config_of(sp, n_lab, {"sample": "seeded samples of labelled rows"}),
+        # the oracle never runs a whole step: ms_per_step is the time one step of all BT
+        # rows would take at the measured rate
+        "extrapolated": True, "timed_seconds": secs_total, "timed_rows": rows_total,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{rows_total} labelled rows in {args.steps} steps of "
-                                   f"~{per_step_seconds:.0f} s (float64 oracle: logits, lse, "
-                                   f"loss, dX and dW per row), scaled by BT/n_labelled"},
+                                   f"~{per_step_seconds:.0f} s, 32 rows per call (float64 oracle: "
+                                   f"logits, lse, loss, dX and dW per row; W converted to float64 "
+                                   f"once, untimed), scaled by BT/n_labelled; ms_per_step "
+                                   f"extrapolated from {secs_total:.1f} s timed"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -383,11 +490,13 @@ def run_ours(args):
     torch.cuda.reset_peak_memory_stats(dev)
     mem0 = torch.cuda.memory_allocated(dev)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    clk.mark_start()
     evs[0].record(stream)
     for i in range(args.steps):
         step(profiler=prof)
         evs[i + 1].record(stream)
     torch.cuda.synchronize(dev)
+    clk.mark_end()
     if dist:
         dist.barrier()
     clocks = clk.stop()
@@ -399,6 +508,36 @@ def run_ours(args):
     ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / args.steps
     value = BT * world / (ms_step / 1000.0)
+
+    # ---- the same step with the workspace capped so that the exp slab holds fewer rows
+    # than BT (R < BT): the memory / time trade of the budget argument
+    bounded = None
+    if (args.api == "abi" and world == 1 and args.budget_gib is None and R >= BT
+            and args.bounded_budget_gib > 0):
+        ws2_bytes = flce.workspace_size(BT, H, V, dt, int(args.bounded_budget_gib * 2 ** 30))
+        R2 = flce.chunk_rows(BT, H, V, dt, ws2_bytes)
+        if 0 < R2 < BT:
+            ws2 = torch.empty(ws2_bytes, dtype=torch.uint8, device=dev)
+
+            def step2():
+                flce.fwd_bwd(X, W, tg, bias, reduction=sp["reduction"], z_loss_scale=sp.get("z", 0.0),
+                             grad_out=go, want_dX=True, want_dW=sp["want_dW"], dW=dW, dbias=dbias,
+                             workspace=ws2, outputs=outs, check=False)
+            for _ in range(3):
+                step2()
+            torch.cuda.synchronize(dev)
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(args.steps):
+                step2()
+            b1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms2 = b0.elapsed_time(b1) / args.steps
+            bounded = {"budget_bytes": int(args.bounded_budget_gib * 2 ** 30), "workspace_bytes": ws2_bytes,
+                       "chunk_rows": R2, "chunks": -(-n_lab // R2), "ms_per_step": ms2,
+                       "value": BT / (ms2 / 1000.0), "unit": UNIT,
+                       "slab_bytes": R2 * -(-V // 256) * 256 * X.element_size()}
+            del ws2
 
     # ---- end to end through the public API with pinned host inputs / outputs: every step
     # copies its token rows, targets (and per-token gradient) in from pinned host memory and
@@ -454,22 +593,25 @@ def run_ours(args):
         roof = None
     elif dom in ("fwd", "dx", "dw"):
         achieved = gemm_flops / (per_step_dom_ms / 1000.0) / 1e12
-        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_kind": f"bf16 sustained ({peak_src})",
+        if sp["dtype"] == "f32":
+            # fp32 inputs run the SIMT FMA kernels: the bound is the FP32 FMA pipes
+            peak, peak_kind = fp32_fma_peak(peaks, dev)
+            bound = "alu"
+        else:
+            peak, peak_kind = peak_for_region(peaks, peak_src, evs[0].elapsed_time(evs[-1]))
+            bound = "tensor"
+
+        def gemm_entry(k):
+            tf = gemm_flops / (stages[k][0] / args.steps / 1000.0) / 1e12
+            return {"ms_per_step": stages[k][0] / args.steps, "tflops": tf, "frac": tf / peak,
+                    "traffic": (rec["per_launch_bytes"].get(k) if rec else None)}
+        roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                "sm_mhz_median": (clocks or {}).get("sm_mhz"),
                 "per_launch": f"2*H*V FLOPs per labelled row x {n_lab * args.steps / max(dom_launches, 1):.0f} rows per launch",
                 "traffic": (rec["per_launch_bytes"].get(dom) if rec else None),
                 "traffic_source": "profiles/traffic.json (ncu, full size)" if rec else None,
-                # the same kernel against the burst figure, and every GEMM of the step
-                "peak_burst": peaks["bf16_tflops"], "frac_burst": achieved / peaks["bf16_tflops"],
-                "gemms": {k: {"ms_per_step": stages[k][0] / args.steps,
-                              "tflops": gemm_flops / (stages[k][0] / args.steps / 1000.0) / 1e12,
-                              "frac_sustained": gemm_flops / (stages[k][0] / args.steps / 1000.0) / 1e12 / peak,
-                              "frac_burst": gemm_flops / (stages[k][0] / args.steps / 1000.0) / 1e12
-                              / peaks["bf16_tflops"],
-                              "traffic": (rec["per_launch_bytes"].get(k) if rec else None)}
-                          for k in ("fwd", "dx", "dw") if k in stages and stages[k][1] > 0}}
+                "gemms": {k: gemm_entry(k) for k in ("fwd", "dx", "dw") if k in stages and stages[k][1] > 0}}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks.get("hbm_gbs"),
                 "unit": "GB/s", "frac": None, "traffic": None}
@@ -498,13 +640,11 @@ def run_ours(args):
         "gpu_launches": int(sum(v[1] for v in stages.values())) if args.api == "abi" else None,
         "clocks": clocks,
         "e2e": e2e,
+        "slab_rows_below_bt": bounded,
         "context_vs_h200_public_default_ms": 53.039 if sp["name"] == "llama8b" else None,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, rows, secs = oracle_sample_rate(sp, inp, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                                "sample": f"{rows} seeded labelled rows, {secs:.1f} s of float64 oracle "
-                                          f"work (logits, lse, loss, dX, dW), scaled by BT/n_labelled"}
+        line["cpu_baseline"] = cpu_baseline_subprocess(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -539,7 +679,7 @@ def run_jsd(args):
                           "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                           "ms_per_step": BT / value * 1000.0, "higher_is_better": True, "scaling": "weak",
                           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded torch.Generator)",
-                          "config": cfg,
+                          "config": cfg, "extrapolated": True, "timed_seconds": spent, "timed_rows": done,
                           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(),
                                            "kind": "oracle",
                                            "sample": f"{done} seeded labelled rows, {spent:.1f} s of float64 "
@@ -587,11 +727,13 @@ def run_jsd(args):
     torch.cuda.reset_peak_memory_stats(dev)
     mem0 = torch.cuda.memory_allocated(dev)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    clk.mark_start()
     evs[0].record(stream)
     for i in range(args.steps):
         step(prof)
         evs[i + 1].record(stream)
     torch.cuda.synchronize(dev)
+    clk.mark_end()
     if dist:
         dist.barrier()
     clocks = clk.stop()
@@ -640,7 +782,7 @@ def run_jsd(args):
     dom = max(("fwd", "dx", "dw"), key=lambda k: stages[k][0])
     dom_flops = 2.0 * n_lab * V * ((Hs + Ht) if dom == "fwd" else Hs)
     achieved = dom_flops / (stages[dom][0] / args.steps / 1000.0) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    peak, peak_kind = peak_for_region(peaks, src, evs[0].elapsed_time(evs[-1]))
     line = {"op": "fused_linear_jsd", "metric": metric,
             "value": BT * world / (ms / 1000.0), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -649,19 +791,16 @@ def run_jsd(args):
                            l2="no flush: the heads (0.5 + 1.05 GB) exceed the 129 MB L2"),
             "ms_per_step_percentiles": per_step, "transient": transient,
             "tflops": tflops, "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
-                                                     "sustained": tflops / peak, "source": src},
+                                                     "sustained": tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
+                                                     "source": src},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_kind": f"bf16 sustained ({src})", "traffic": None,
-                         "peak_burst": peaks["bf16_tflops"], "frac_burst": achieved / peaks["bf16_tflops"]},
+                         "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                         "sm_mhz_median": (clocks or {}).get("sm_mhz"), "traffic": None},
             "stages": {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                        for k, v in stages.items() if v[1] > 0},
             "gpu_launches": int(sum(v[1] for v in stages.values())) if args.api == "abi" else None, "clocks": clocks, "e2e": e2e}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, rows_done, secs = jsd_oracle_sample_rate(sp, inp, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                                "sample": f"{rows_done} seeded labelled rows, {secs:.1f} s of float64 oracle "
-                                          f"work (both heads' logits, loss, dX, dW)"}
+        line["cpu_baseline"] = cpu_baseline_subprocess(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
