@@ -113,21 +113,44 @@ class FusedLinearCrossEntropy(torch.autograd.Function):
                 dW = dW * g.to(dW.dtype) if need_w else dW
                 db = db * g.to(db.dtype) if (need_w and ctx.has_bias) else db
             else:
-                # eager: scale the op's own gradient buffers in place on the device; nothing
-                # is done (no pass over dW) when the upstream gradient is exactly 1. A second
-                # backward through the same graph (retain_graph) finds the buffers already
-                # scaled by the previous upstream gradient and applies only the ratio (so it
-                # cannot follow a first backward whose upstream gradient was exactly 0).
                 g = g_loss.reshape(1).float().contiguous()
                 prev = getattr(ctx, "applied_scale", None)
-                r = g if prev is None else (g / prev).contiguous()
-                ctx.applied_scale = g.clone()
-                if need_x:
-                    flce.scale_by(dX, r)
-                if need_w:
-                    flce.scale_by(dW, r)
-                    if ctx.has_bias:
-                        flce.scale_by(db, r)
+                if prev is None:
+                    # eager, first backward: scale the op's own gradient buffers in place on
+                    # the device and hand them out; nothing is done (no pass over dW) when
+                    # the upstream gradient is exactly 1
+                    ctx.applied_scale = g.clone()
+                    if need_x:
+                        flce.scale_by(dX, g)
+                    if need_w:
+                        flce.scale_by(dW, g)
+                        if ctx.has_bias:
+                            flce.scale_by(db, g)
+                    ctx.versions = tuple(t._version for t in (dX, dW, db))
+                else:
+                    # a later backward through a retained graph: the buffers were handed
+                    # out scaled by the first upstream gradient, and whoever holds them
+                    # (torch.autograd.grad's result, a hook) must keep what they got, so
+                    # the new gradients are fresh tensors scaled by the ratio
+                    if tuple(t._version for t in (dX, dW, db)) != ctx.versions:
+                        raise RuntimeError(
+                            "fused_linear_cross_entropy: the gradients returned by the first "
+                            "backward were modified in place, so a second backward through the "
+                            "retained graph cannot be formed from them")
+                    if float(prev) == 0.0:
+                        raise RuntimeError(
+                            "fused_linear_cross_entropy: a second backward through a retained "
+                            "graph cannot follow a first backward whose upstream gradient was 0")
+                    r = (g / prev).contiguous()
+                    dX = dX.clone() if need_x else dX
+                    dW = dW.clone() if need_w else dW
+                    db = db.clone() if (need_w and ctx.has_bias) else db
+                    if need_x:
+                        flce.scale_by(dX, r)
+                    if need_w:
+                        flce.scale_by(dW, r)
+                        if ctx.has_bias:
+                            flce.scale_by(db, r)
         return (dX if need_x else None, dW if need_w else None, None,
                 db if (need_w and ctx.has_bias) else None, None, None, None, None)
 

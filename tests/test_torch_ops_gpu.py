@@ -111,3 +111,47 @@ def test_second_backward_through_a_retained_graph():
     loss.backward()
     assert rel_fro(X.grad.float().cpu().numpy(), 3.5 * o["dX"]) <= TOL["bf16"]["grad"]
     assert rel_fro(W.grad.float().cpu().numpy(), 3.5 * o["dW"]) <= TOL["bf16"]["grad"]
+
+
+def test_autograd_grad_twice_keeps_the_first_result():
+    """torch.autograd.grad(..., retain_graph=True) twice: the tensors the first call
+    returned keep their values (the second call's gradients are fresh tensors), and each
+    call's gradients are its own upstream gradient times the oracle's."""
+    from linear_cross_entropy_logits_gb300.torch_ops import fused_linear_cross_entropy
+    sp = I.spec("llama1b", BT=300, H=192, V=3000, w_std=0.2, ignore="random", n_ignored=40)
+    inp = I.generate(sp, seed=33)
+    o = run_oracle(inp, sp)
+    X = inp["X"].cuda().requires_grad_(True)
+    W = inp["W"].cuda().requires_grad_(True)
+    loss = fused_linear_cross_entropy(X, W, inp["targets"].cuda(), accum_dtype=torch.float32)
+    gx1, gw1 = torch.autograd.grad(loss, (X, W), torch.tensor(2.5, device="cuda"), retain_graph=True)
+    keep_x, keep_w = gx1.clone(), gw1.clone()
+    gx2, gw2 = torch.autograd.grad(loss, (X, W), torch.tensor(-0.5, device="cuda"), retain_graph=True)
+    assert torch.equal(gx1, keep_x) and torch.equal(gw1, keep_w)
+    assert gx2.data_ptr() != gx1.data_ptr() and gw2.data_ptr() != gw1.data_ptr()
+    assert rel_fro(gx1.float().cpu().numpy(), 2.5 * o["dX"]) <= TOL["bf16"]["grad"]
+    assert rel_fro(gw1.float().cpu().numpy(), 2.5 * o["dW"]) <= TOL["bf16"]["grad"]
+    assert rel_fro(gx2.float().cpu().numpy(), -0.5 * o["dX"]) <= TOL["bf16"]["grad"]
+    assert rel_fro(gw2.float().cpu().numpy(), -0.5 * o["dW"]) <= TOL["bf16"]["grad"]
+
+
+def test_second_backward_after_a_zero_upstream_gradient_raises():
+    """A first backward with upstream gradient 0 leaves nothing to rescale from: a second
+    backward through the retained graph raises instead of returning inf/NaN gradients; so
+    does one after the first gradients were modified in place."""
+    from linear_cross_entropy_logits_gb300.torch_ops import fused_linear_cross_entropy
+    sp = I.spec("llama1b", BT=200, H=128, V=2000, w_std=0.2)
+    inp = I.generate(sp, seed=34)
+    X = inp["X"].cuda().requires_grad_(True)
+    W = inp["W"].cuda().requires_grad_(True)
+    loss = fused_linear_cross_entropy(X, W, inp["targets"].cuda(), accum_dtype=torch.float32)
+    torch.autograd.grad(loss, (X, W), torch.tensor(0.0, device="cuda"), retain_graph=True)
+    with pytest.raises(RuntimeError, match="upstream gradient was 0"):
+        torch.autograd.grad(loss, (X, W), torch.tensor(1.0, device="cuda"), retain_graph=True)
+    loss = fused_linear_cross_entropy(X, W, inp["targets"].cuda(), accum_dtype=torch.float32)
+    gx, gw = torch.autograd.grad(loss, (X, W), retain_graph=True)
+    # dX comes back in X's dtype, so autograd hands out the op's own buffer (the fp32 dW
+    # is cast to W's dtype on the way out, a copy)
+    gx.mul_(3.0)
+    with pytest.raises(RuntimeError, match="modified in place"):
+        torch.autograd.grad(loss, (X, W), retain_graph=True)

@@ -7,7 +7,8 @@ compiled into the library instead of a caller workspace.
 The file is named so that pytest collects it last. It passes run alone in a fresh process
 and after the other tests: two calls in a row (different problems, sharing the one
 scratch array) must each match flce_fwd_bwd on the same inputs, within the tolerances of
-the parity tests; a problem too large for the scratch is rejected before any launch.
+the parity tests; once a first call has set the device up, a call leaves the device's
+free memory unchanged; a problem too large for the scratch is rejected before any launch.
 """
 
 import ctypes
@@ -102,6 +103,45 @@ def test_noalloc_matches_fwd_bwd_on_two_calls(lib):
         assert _rel_fro(got["dW"], ref["dW"]) <= 1e-2
         if d["bias"] is not None:
             assert _rel_fro(got["dbias"], ref["dbias"]) <= 1e-2
+
+
+def test_noalloc_call_allocates_no_device_memory(lib):
+    """The point of the entry point: once a first call on the device has looked up the
+    scratch array's address (and loaded the kernels), a call allocates no device memory.
+    The caller's buffers are allocated before the measurement; free device memory is read
+    before and after a second call of the same problem."""
+    sp = PROBLEMS[1]
+    inp = I.generate(sp, seed=30)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    dW = torch.zeros(sp["V"], sp["H"], dtype=torch.float32, device="cuda")
+    first = _noalloc_call(lib, d, sp, dW)
+    torch.cuda.synchronize()
+    a = flce.FlceArgs()
+    # rebuild the same call with the same (already allocated) output buffers
+    BT, H, V = sp["BT"], sp["H"], sp["V"]
+    a.BT, a.H, a.V = BT, H, V
+    a.in_dtype = flce.DTYPES[d["X"].dtype]
+    a.reduction = flce.REDUCTIONS[sp["reduction"]]
+    a.X, a.W, a.bias = d["X"].data_ptr(), d["W"].data_ptr(), None
+    a.targets = d["targets"].data_ptr()
+    a.ignore_index = I.IGNORE_INDEX
+    a.z_loss_scale = sp.get("z", 0.0)
+    a.grad_out = None
+    a.want_dX, a.want_dW, a.dW_dtype = 1, 1, 0
+    for k in ("loss", "z_loss", "acc", "lse", "pred", "n_labelled", "status"):
+        setattr(a, k, first[k].data_ptr())
+    a.dX, a.dW, a.dbias = first["dX"].data_ptr(), dW.data_ptr(), None
+    a.workspace, a.workspace_bytes, a.profile = None, 0, None
+    loss1 = float(first["loss"][0])
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    s = torch.cuda.current_stream()
+    rc = lib.flce_fwd_bwd_noalloc(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream))
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert rc == flce.FLCE_OK, flce.status_string(rc)
+    assert free1 == free0, f"device memory changed by {free0 - free1} bytes"
+    assert float(first["loss"][0]) == loss1  # same inputs, same result
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(lib):
