@@ -7,7 +7,9 @@
  * backward in one call. For token rows X[BT,H], head weight W[V,H], optional bias b[V] and
  * targets t[BT], every row i whose target is not ignore_index gets
  *
- *     s_v    = X_i . W_v + b_v                          (logits, never stored in full)
+ *     s_v    = X_i . W_v + b_v                          (logits: fp32 on chip; exp(s_v)
+ *                                                       of the chunk's rows stored in the
+ *                                                       input dtype, in the workspace)
  *     lse_i  = log sum_v exp(s_v)
  *     loss_i = lse_i - s_{t_i} + z lse_i^2              (z = z_loss_scale)
  *     pred_i = argmax_v s_v (lowest index on ties),     acc_i = [pred_i == t_i]
