@@ -57,6 +57,7 @@ bool plan_layout(int64_t BT, int64_t H, int64_t V, int dt, int64_t R, Plan* p) {
   q.off_lse = take(4 * (size_t)R);
   q.off_arow = take(4 * (size_t)R);
   q.off_rsc = take(4 * (size_t)R);
+  q.off_rmax = take(4 * (size_t)R);
   q.off_slab = take((size_t)R * q.Vp * q.esz);
   // two fp32 dX accumulator buffers of the tensor-core path (16-bit inputs only)
   q.off_dxacc = take(q.esz == 2 ? 2 * (size_t)R * H * 4 : 0);
@@ -98,6 +99,7 @@ Work make_work(const Plan& p, void* ws, int32_t* user_status) {
   w.lse = (float*)(b + p.off_lse);
   w.arow = (float*)(b + p.off_arow);
   w.rsc = (float*)(b + p.off_rsc);
+  w.rmax = (int*)(b + p.off_rmax);
   w.slab = b + p.off_slab;
   w.dxacc = (float*)(b + p.off_dxacc);
   w.status = user_status ? (int*)user_status : &w.ctrl->status;
@@ -235,7 +237,8 @@ extern "C" int64_t flce_plan_describe(int64_t BT, int64_t H, int64_t V, int32_t 
              {"stm", p.off_stm, p.off_sts},          {"sts", p.off_sts, p.off_sti},
              {"sti", p.off_sti, p.off_tgt},          {"tgt", p.off_tgt, p.off_lse},
              {"lse", p.off_lse, p.off_arow},         {"arow", p.off_arow, p.off_rsc},
-             {"rsc", p.off_rsc, p.off_slab},         {"slab", p.off_slab, p.off_dxacc},
+             {"rsc", p.off_rsc, p.off_rmax},         {"rmax", p.off_rmax, p.off_slab},
+             {"slab", p.off_slab, p.off_dxacc},
              {"dxacc", p.off_dxacc, p.total}};
   for (const auto& r : reg)
     if (r.next > r.off) add("  workspace %-6s at %12zu, %12zu B\n", r.name, r.off, r.next - r.off);

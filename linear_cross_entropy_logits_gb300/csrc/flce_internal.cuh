@@ -20,8 +20,14 @@ constexpr int CHUNK_ALIGN = 128;   // row-chunk granularity (one tensor-core M t
 // Tile-shape thresholds of the tensor-core GEMMs (the reasons are at their use in
 // flce_tc.cu): the dW GEMM takes 256 x 512 pair tiles from chunks of this many rows on, the
 // forward from this hidden size on.
-constexpr int DW_WIDE_MIN_ROWS = 4096;
-constexpr int FWD_WIDE_MIN_H = 4096;
+#ifndef FLCE_DW_WIDE_MIN_ROWS
+#define FLCE_DW_WIDE_MIN_ROWS 4096
+#endif
+#ifndef FLCE_FWD_WIDE_MIN_H
+#define FLCE_FWD_WIDE_MIN_H 4096
+#endif
+constexpr int DW_WIDE_MIN_ROWS = FLCE_DW_WIDE_MIN_ROWS;
+constexpr int FWD_WIDE_MIN_H = FLCE_FWD_WIDE_MIN_H;
 constexpr uint32_t DEFAULT_TIMEOUT_MS = 4000;
 // Default workspace budget: 3 GiB, about 1% of a GB300's 288 GB of HBM. It holds the
 // whole 8192-row chunk of a Llama-3.1-8B head (one pass of W per GEMM, one dW
@@ -55,7 +61,8 @@ struct Plan {
   int64_t R;     // max rows per chunk (multiple of 128)
   int64_t kmax;  // chunks the host enqueues = cdiv(BT, R)
   size_t off_ctrl, off_idx, off_rloss, off_rz, off_racc;
-  size_t off_xc, off_stm, off_sts, off_sti, off_tgt, off_lse, off_arow, off_rsc, off_slab, off_dxacc;
+  size_t off_xc, off_stm, off_sts, off_sti, off_tgt, off_lse, off_arow, off_rsc, off_rmax, off_slab,
+      off_dxacc;
   size_t total;
 };
 
@@ -78,6 +85,9 @@ struct Work {
   float* lse;      // [R] row logsumexp
   float* arow;     // [R] per-row factor a_i (g_i for none, 1 otherwise)
   float* rsc;      // [R] row-reference mode: G row scale a_i (1 + 2 z lse_i) exp(-lse_i)
+  int* rmax;       // [R] largest tile maximum of the row written so far by the forward
+                   // (order-preserving integer key, max_key), reset by the gather; lets a
+                   // tile skip its argmax search where it cannot hold the row's maximum
   void* slab;      // [R, Vp] exp(s - tile max) (row-reference mode: exp(s)), then G, in the
                    // input dtype
   float* dxacc;    // [2, R, H] fp32 dX accumulator buffers of the tensor-core path (K
@@ -172,6 +182,17 @@ __device__ __forceinline__ bool chunk_bounds(const Ctrl* c, int k, int& row0, in
 }
 
 constexpr float LOG2E = 1.4426950408889634f;
+
+// Order-preserving integer key of a float (a > b  <=>  key(a) > key(b) for non-NaN a, b),
+// so that a row's running maximum can be kept with integer atomicMax.
+__device__ __forceinline__ int max_key(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : (i ^ 0x7fffffff);
+}
+__device__ __forceinline__ float max_key_value(int k) {
+  return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff));
+}
+constexpr int MAX_KEY_NEG_INF = (int)(0xff800000u ^ 0x7fffffffu);  // max_key(-inf)
 
 }  // namespace flce
 

@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(256) k_gather(const __grid_constant__ CallArgs
   const int esz = a.dt == FLCE_F32 ? 4 : 2;
   const int64_t src_bytes = a.H * esz, dst_bytes = a.Hp * esz;
   for (int r = blockIdx.x; r < lim; r += gridDim.x) {
+    if (threadIdx.x == 0 && a.w.rmax != nullptr) a.w.rmax[r] = MAX_KEY_NEG_INF;
     char* dst = (char*)a.w.xc + (int64_t)r * dst_bytes;
     if (r < rows) {
       const char* src = (const char*)a.X + (int64_t)a.w.idx[row0 + r] * src_bytes;

@@ -521,148 +521,179 @@ __device__ __forceinline__ float select64(const uint32_t (&r)[64], int idx) {
   return x[0];
 }
 
+// The logit of one accumulator element: acc * ls (+ bias[v]). SCALE: ls != 1 (the
+// distillation op's 1/T); BIAS: a bias is added. Rounded multiply and add (no contraction
+// into an FMA), so that every place that evaluates a logit gets the same bits.
+template <typename T, bool SCALE, bool BIAS>
+__device__ __forceinline__ float logit_of(uint32_t acc, int v, float ls, const T* bias) {
+  float s = __uint_as_float(acc);
+  if (SCALE) s = __fmul_rn(s, ls);
+  if (BIAS) s = __fadd_rn(s, to_f<T>(bias[v]));
+  return s;
+}
+
 // The target logit of a row whose target column lies in the 64 columns just loaded
 // (loc in [0, 64)). The warp picks it out only when one of its 32 rows has its target
 // there (about one 64-column block in 60 at V = 128256), so no per-column comparison runs.
-template <typename T>
+template <typename T, bool SCALE, bool BIAS>
 __device__ __forceinline__ void pick_target(const uint32_t (&r)[64], int loc, int v, float ls, const T* bias,
                                             float& tl) {
   const bool mine = (unsigned)loc < 64u;
   if (__any_sync(0xffffffffu, mine)) {
-    const float tv = select64(r, loc & 63) * ls;
-    if (mine) tl = bias != nullptr ? tv + to_f<T>(bias[v]) : tv;
+    const float tv = select64(r, loc & 63);
+    if (mine) tl = logit_of<T, SCALE, BIAS>(__float_as_uint(tv), v, ls, bias);
   }
 }
 
-// 64 columns of the row-reference forward: max / lowest-index argmax (four independent
-// chains, merged with lowest-index ties, so that the compare-select latency of one chain
-// does not serialise the columns), the sum of exp(s) and the packed exp(s) values. FULL:
-// every column lies inside the vocabulary (all but the last tile), no column test.
-template <typename T, bool FULL>
-__device__ __forceinline__ void fwd_ref_cols(const CallArgs& a, const uint32_t (&r)[64], int vbase, float ls,
-                                             const T* bias, float& mx, int& ai, float& sum, uint32_t (&pk)[32]) {
-  const int V = (int)a.V;
-  float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
-  int a4[4] = {ai, 0x7fffffff, 0x7fffffff, 0x7fffffff};
+// The argmax is kept as a value-only maximum per 64 columns (one max instruction per
+// logit); the lowest column holding a block's maximum is searched for only when that block
+// raises the tile's maximum AND can hold the row's maximum, i.e. its maximum is at least
+// the largest tile maximum of the row already written by other tiles of this chunk (thr,
+// read from the workspace's running row maxima at the start of the tile). A tile whose
+// maximum stays below thr cannot hold the row's argmax: its stored index is never chosen,
+// because the merge in finalize takes the index of a tile with the row's largest maximum
+// (lowest index among equal maxima), and every such tile searched its own. Most blocks skip
+// the search: once a few tiles of a row are done, thr is near the row's maximum.
+//
+// Lowest column among the 64 just evaluated whose logit equals m (their maximum); s holds
+// the logits (columns past the vocabulary hold -inf, never equal to a searched maximum).
+__device__ __forceinline__ int find_max_col(const uint32_t (&s)[64], int vbase, float m) {
+  int j0 = 0;
+#pragma unroll
+  for (int j = 63; j >= 0; --j)
+    if (__uint_as_float(s[j]) == m) j0 = j;
+  return vbase + j0;
+}
+
+// Argmax bookkeeping after a 64-column block of logits s with maximum bm (warp-collective).
+__device__ __forceinline__ void argmax_update(const uint32_t (&s)[64], int vbase, float bm, float thr, float& mx,
+                                              int& ai) {
+  const bool need = bm > mx && bm >= thr;
+  if (__any_sync(0xffffffffu, need)) {
+    if (need) ai = find_max_col(s, vbase, bm);
+  }
+  mx = fmaxf(mx, bm);
+}
+
+// 64 columns of the row-reference forward: their maximum (four independent chains), the
+// sums of exp(s) (four partial sums) and the packed exp(s) values; the accumulator values
+// in r are replaced by the logits (for the argmax search). FULL: every column lies inside
+// the vocabulary (all but the last tile), no column test; columns past the vocabulary count
+// as -inf (exp 0).
+template <typename T, bool FULL, bool SCALE, bool BIAS>
+__device__ __forceinline__ void fwd_ref_cols(uint32_t (&r)[64], int vbase, int V, float ls, const T* bias,
+                                             float& bm, float (&sum4)[4], uint32_t (&pk)[32]) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int jj = 0; jj < 64; jj += 2) {
     const int v = vbase + jj;
-    float s0 = __uint_as_float(r[jj]) * ls, s1 = __uint_as_float(r[jj + 1]) * ls;
-    const bool ok0 = FULL || v < V, ok1 = FULL || v + 1 < V;
-    if (bias != nullptr) {
-      if (ok0) s0 += to_f<T>(bias[v]);
-      if (ok1) s1 += to_f<T>(bias[v + 1]);
-    }
-    const int u = 2 * ((jj >> 1) & 1);
-    if (ok0 && s0 > m4[u]) {
-      m4[u] = s0;
-      a4[u] = v;
-    }
-    if (ok1 && s1 > m4[u + 1]) {
-      m4[u + 1] = s1;
-      a4[u + 1] = v + 1;
-    }
-    const float e0 = ok0 ? ex2_fast(s0 * LOG2E) : 0.0f;
-    const float e1 = ok1 ? ex2_fast(s1 * LOG2E) : 0.0f;
-    sum += e0 + e1;
+    const int u = (jj >> 1) & 3;
+    float s0 = -INFINITY, s1 = -INFINITY;
+    if (FULL || v < V) s0 = logit_of<T, SCALE, BIAS>(r[jj], v, ls, bias);
+    if (FULL || v + 1 < V) s1 = logit_of<T, SCALE, BIAS>(r[jj + 1], v + 1, ls, bias);
+    r[jj] = __float_as_uint(s0);
+    r[jj + 1] = __float_as_uint(s1);
+    m4[u] = fmaxf(m4[u], fmaxf(s0, s1));
+    const float e0 = ex2_fast(s0 * LOG2E);
+    const float e1 = ex2_fast(s1 * LOG2E);
+    sum4[u] += e0 + e1;
     pk[jj / 2] = pack2<T>(e0, e1);
   }
-#pragma unroll
-  for (int k = 1; k < 4; ++k)
-    if (m4[k] > m4[0] || (m4[k] == m4[0] && a4[k] < a4[0])) {
-      m4[0] = m4[k];
-      a4[0] = a4[k];
-    }
-  mx = m4[0];
-  ai = a4[0];
+  bm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+
+// The row's running maximum thr (see argmax_update) at the start of a tile.
+__device__ __forceinline__ float row_threshold(const CallArgs& a, int rr) {
+  if (a.w.rmax == nullptr) return -INFINITY;
+  int k;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(k) : "l"(a.w.rmax + rr) : "memory");
+  return max_key_value(k);
+}
+
+// Per-tile statistics of a row, and its contribution to the running row maximum.
+__device__ __forceinline__ void write_tile_stats(const CallArgs& a, int rr, int n, float mx, float sum, int ai,
+                                                 float thr, bool want_arg) {
+  const int64_t o = (int64_t)rr * a.nvt + n;
+  a.w.stm[o] = mx;
+  a.w.sts[o] = sum;
+  a.w.sti[o] = ai;
+  if (want_arg && a.w.rmax != nullptr && mx > thr) atomicMax(a.w.rmax + rr, max_key(mx));
 }
 
 // Row-reference forward epilogue: exp(s) needs no tile max, so one pass over TMEM (64
 // columns per wait) gives the max / lowest-index argmax, the target logit and the exp
 // values, written to the slab.
-template <typename T>
+template <typename T, bool SCALE, bool BIAS>
 __device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, int row0, int rows, int mrow, int n,
                                                  uint32_t taddr, int q, int lane) {
   const int rr = mrow + q * 32 + lane;  // row within the chunk
   const bool valid = rr < rows;
   const int v0 = n * VT;
+  const int V = (int)a.V;
+  const bool want_arg = a.targets != nullptr;  // the distillation op needs no argmax
   int toff = -1;  // the target's column within this tile, or -1
-  if (valid && a.targets != nullptr) {
+  float thr = -INFINITY;
+  if (valid && want_arg) {
     const int64_t tg = a.targets[a.w.idx[row0 + rr]];
     if (tg >= v0 && tg < v0 + BN) toff = (int)(tg - v0);
+    thr = row_threshold(a, rr);
   }
   const float ls = a.logit_scale;
   const T* bias = (const T*)a.bias;
-  const bool full = v0 + BN <= (int)a.V;
-  float mx = -INFINITY, tl = 0.0f, sum = 0.0f;
+  const bool full = v0 + BN <= V;
+  float mx = -INFINITY, tl = 0.0f;
+  float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   int ai = v0;
 #pragma unroll 1
   for (int c2 = 0; c2 < BN / 64; ++c2) {
     uint32_t r[64];
     tmem_ld64(taddr + c2 * 64, r);
-    pick_target<T>(r, toff - c2 * 64, v0 + toff, ls, bias, tl);
+    const int vb = v0 + c2 * 64;
+    pick_target<T, SCALE, BIAS>(r, toff - c2 * 64, v0 + toff, ls, bias, tl);
     uint32_t pk[32];
-    if (full) fwd_ref_cols<T, true>(a, r, v0 + c2 * 64, ls, bias, mx, ai, sum, pk);
-    else fwd_ref_cols<T, false>(a, r, v0 + c2 * 64, ls, bias, mx, ai, sum, pk);
-    store_slab64<T>(a, rr, v0 + c2 * 64, pk);
+    float bm;
+    if (full) {
+      fwd_ref_cols<T, true, SCALE, BIAS>(r, vb, V, ls, bias, bm, sum4, pk);
+    } else {
+      fwd_ref_cols<T, false, SCALE, BIAS>(r, vb, V, ls, bias, bm, sum4, pk);
+    }
+    if (want_arg) argmax_update(r, vb, bm, thr, mx, ai);
+    if (!want_arg) mx = fmaxf(mx, bm);
+    store_slab64<T>(a, rr, vb, pk);
   }
   if (valid) {
-    const int64_t o = (int64_t)rr * a.nvt + n;
-    a.w.stm[o] = mx;
-    a.w.sts[o] = sum;
-    a.w.sti[o] = ai;
+    write_tile_stats(a, rr, n, mx, (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]), ai, thr, want_arg);
     if (toff >= 0) a.w.tgt[rr] = tl;
   }
 }
 
-// Per-tile forward epilogue, first pass over 64 columns: max and lowest-index argmax (four
-// independent chains merged with lowest-index ties, as in the row-reference pass).
-template <typename T, bool FULL>
-__device__ __forceinline__ void fwd_tile_max(const CallArgs& a, const uint32_t (&r)[64], int vbase, float ls,
-                                             const T* bias, float& mx, int& ai) {
-  float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
-  int a4[4] = {ai, 0x7fffffff, 0x7fffffff, 0x7fffffff};
+// Per-tile forward epilogue, first pass over 64 columns: their maximum (four chains); the
+// accumulator values in r are replaced by the logits (-inf past the vocabulary).
+template <typename T, bool FULL, bool SCALE, bool BIAS>
+__device__ __forceinline__ float fwd_tile_max(uint32_t (&r)[64], int vbase, int V, float ls, const T* bias) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
   for (int j = 0; j < 64; ++j) {
     const int v = vbase + j;
-    float s = __uint_as_float(r[j]) * ls;
-    if (FULL || v < (int)a.V) {
-      if (bias != nullptr) s += to_f<T>(bias[v]);
-      if (s > m4[j & 3]) {
-        m4[j & 3] = s;
-        a4[j & 3] = v;
-      }
-    }
+    const float s = (FULL || v < V) ? logit_of<T, SCALE, BIAS>(r[j], v, ls, bias) : -INFINITY;
+    r[j] = __float_as_uint(s);
+    m4[j & 3] = fmaxf(m4[j & 3], s);
   }
-#pragma unroll
-  for (int k = 1; k < 4; ++k)
-    if (m4[k] > m4[0] || (m4[k] == m4[0] && a4[k] < a4[0])) {
-      m4[0] = m4[k];
-      a4[0] = a4[k];
-    }
-  mx = m4[0];
-  ai = a4[0];
+  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
 // Per-tile forward epilogue, second pass over 64 columns: exp(s - max) (base 2, mxl =
-// max * log2 e) packed for the slab, and their sum.
-template <typename T, bool FULL>
-__device__ __forceinline__ void fwd_tile_exp(const CallArgs& a, const uint32_t (&r)[64], int vbase, float ls,
-                                             const T* bias, float mxl, float& sum, uint32_t (&pk)[32]) {
+// max * log2 e) packed for the slab, and their sums (four partial sums).
+template <typename T, bool FULL, bool SCALE, bool BIAS>
+__device__ __forceinline__ void fwd_tile_exp(const uint32_t (&r)[64], int vbase, int V, float ls, const T* bias,
+                                             float mxl, float (&sum4)[4], uint32_t (&pk)[32]) {
 #pragma unroll
   for (int j = 0; j < 64; j += 2) {
     const int v = vbase + j;
-    float s0 = __uint_as_float(r[j]) * ls, s1 = __uint_as_float(r[j + 1]) * ls;
     float e0 = 0.0f, e1 = 0.0f;
-    if (FULL || v < (int)a.V) {
-      if (bias != nullptr) s0 += to_f<T>(bias[v]);
-      e0 = ex2_fast(fmaf(s0, LOG2E, -mxl));
-    }
-    if (FULL || v + 1 < (int)a.V) {
-      if (bias != nullptr) s1 += to_f<T>(bias[v + 1]);
-      e1 = ex2_fast(fmaf(s1, LOG2E, -mxl));
-    }
-    sum += e0 + e1;
+    if (FULL || v < V) e0 = ex2_fast(fmaf(logit_of<T, SCALE, BIAS>(r[j], v, ls, bias), LOG2E, -mxl));
+    if (FULL || v + 1 < V) e1 = ex2_fast(fmaf(logit_of<T, SCALE, BIAS>(r[j + 1], v + 1, ls, bias), LOG2E, -mxl));
+    sum4[(j >> 1) & 3] += e0 + e1;
     pk[j / 2] = pack2<T>(e0, e1);
   }
 }
@@ -670,48 +701,77 @@ __device__ __forceinline__ void fwd_tile_exp(const CallArgs& a, const uint32_t (
 // Per-tile forward epilogue (fp16 inputs, dbias, the distillation op, a chunk outside the
 // row-reference window): a first pass over TMEM for the max / argmax / target logit, a
 // second for exp(s - max) into the slab.
-template <typename T>
+template <typename T, bool SCALE, bool BIAS>
 __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int rows, int mrow, int n,
                                              uint32_t taddr, int q, int lane) {
   const int rr = mrow + q * 32 + lane;  // row within the chunk
   const bool valid = rr < rows;
-  int toff = -1;
   const int v0 = n * VT;
-  if (valid && a.targets != nullptr) {
+  const int V = (int)a.V;
+  const bool want_arg = a.targets != nullptr;
+  int toff = -1;
+  float thr = -INFINITY;
+  if (valid && want_arg) {
     const int64_t tg = a.targets[a.w.idx[row0 + rr]];
     if (tg >= v0 && tg < v0 + BN) toff = (int)(tg - v0);
+    thr = row_threshold(a, rr);
   }
   const float ls = a.logit_scale;
   const T* bias = (const T*)a.bias;
-  const bool full = v0 + BN <= (int)a.V;
+  const bool full = v0 + BN <= V;
   float mx = -INFINITY, tl = 0.0f;
   int ai = v0;
 #pragma unroll 1
   for (int c2 = 0; c2 < BN / 64; ++c2) {
     uint32_t r[64];
     tmem_ld64(taddr + c2 * 64, r);
-    pick_target<T>(r, toff - c2 * 64, v0 + toff, ls, bias, tl);
-    if (full) fwd_tile_max<T, true>(a, r, v0 + c2 * 64, ls, bias, mx, ai);
-    else fwd_tile_max<T, false>(a, r, v0 + c2 * 64, ls, bias, mx, ai);
+    const int vb = v0 + c2 * 64;
+    pick_target<T, SCALE, BIAS>(r, toff - c2 * 64, v0 + toff, ls, bias, tl);
+    const float bm = full ? fwd_tile_max<T, true, SCALE, BIAS>(r, vb, V, ls, bias)
+                          : fwd_tile_max<T, false, SCALE, BIAS>(r, vb, V, ls, bias);
+    if (want_arg) argmax_update(r, vb, bm, thr, mx, ai);
+    else mx = fmaxf(mx, bm);
   }
   // exp(s - max) to the slab, 64 columns at a time
-  float sum = 0.0f;
+  float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   const float mxl = a.ref_mode ? 0.0f : mx * LOG2E;  // row-reference mode stores exp(s)
 #pragma unroll 1
   for (int c2 = 0; c2 < BN / 64; ++c2) {
     uint32_t r[64];
     tmem_ld64(taddr + c2 * 64, r);
     uint32_t pk[32];
-    if (full) fwd_tile_exp<T, true>(a, r, v0 + c2 * 64, ls, bias, mxl, sum, pk);
-    else fwd_tile_exp<T, false>(a, r, v0 + c2 * 64, ls, bias, mxl, sum, pk);
-    store_slab64<T>(a, rr, v0 + c2 * 64, pk);
+    const int vb = v0 + c2 * 64;
+    if (full) fwd_tile_exp<T, true, SCALE, BIAS>(r, vb, V, ls, bias, mxl, sum4, pk);
+    else fwd_tile_exp<T, false, SCALE, BIAS>(r, vb, V, ls, bias, mxl, sum4, pk);
+    store_slab64<T>(a, rr, vb, pk);
   }
   if (valid) {
-    const int64_t o = (int64_t)rr * a.nvt + n;
-    a.w.stm[o] = mx;
-    a.w.sts[o] = sum;
-    a.w.sti[o] = ai;
+    write_tile_stats(a, rr, n, mx, (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]), ai, thr, want_arg);
     if (toff >= 0) a.w.tgt[rr] = tl;
+  }
+}
+
+// Dispatch of the forward epilogues on the logit scale and the bias (warp-uniform).
+template <typename T, bool SCALE, bool BIAS>
+__device__ __forceinline__ void epilogue_fwd_any3(const CallArgs& a, int row0, int rows, int mrow, int n,
+                                                  uint32_t taddr, int q, int lane) {
+  if (a.ref_mode) epilogue_fwd_ref<T, SCALE, BIAS>(a, row0, rows, mrow, n, taddr, q, lane);
+  else epilogue_fwd<T, SCALE, BIAS>(a, row0, rows, mrow, n, taddr, q, lane);
+}
+// GEN: 0 for launches with no bias and a logit scale of 1 (the cross-entropy op without
+// bias), 1 with a bias and a scale of 1, 2 with another scale (the distillation op at
+// T != 1). Each is a kernel build of its own, so that the common ones keep all their values
+// in registers.
+template <typename T, int GEN>
+__device__ __forceinline__ void epilogue_fwd_any(const CallArgs& a, int row0, int rows, int mrow, int n,
+                                                 uint32_t taddr, int q, int lane) {
+  if constexpr (GEN == 0) {
+    epilogue_fwd_any3<T, false, false>(a, row0, rows, mrow, n, taddr, q, lane);
+  } else if constexpr (GEN == 1) {
+    epilogue_fwd_any3<T, false, true>(a, row0, rows, mrow, n, taddr, q, lane);
+  } else {
+    if (a.bias != nullptr) epilogue_fwd_any3<T, true, true>(a, row0, rows, mrow, n, taddr, q, lane);
+    else epilogue_fwd_any3<T, true, false>(a, row0, rows, mrow, n, taddr, q, lane);
   }
 }
 
@@ -814,7 +874,7 @@ __device__ __forceinline__ void epilogue_reduce(const CallArgs& a, const CUtenso
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int MODE, typename T, int NB>
+template <int MODE, typename T, int NB, int GEN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CallArgs a,
@@ -1013,10 +1073,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int mrow = m * 2 * BM + (int)rank * BM;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((as * NB + j) * BN);
       if (nsub < ts.nsub) {
-        if (MODE == FWD && a.ref_mode)
-          epilogue_fwd_ref<T>(a, row0, rows, mrow, nsub, taddr, q, lane);
-        else if (MODE == FWD)
-          epilogue_fwd<T>(a, row0, rows, mrow, nsub, taddr, q, lane);
+        if (MODE == FWD)
+          epilogue_fwd_any<T, GEN>(a, row0, rows, mrow, nsub, taddr, q, lane);
         else if (MODE == DW && a.dW_dt != FLCE_F32)
           epilogue_reduce<NBUF, (NB == 2), T, half_bufs_of<NB>()>(a, &tmC, stg, mrow, nsub, (int)a.V, 0, taddr, q, lane, cb,
                                               nullptr, ovw, epi_it);
@@ -1107,10 +1165,10 @@ bool make_map(CUtensorMap* m, const void* ptr, int dt, uint64_t inner, uint64_t 
 
 // Launch as clusters of 2 CTAs, one pair per pair tile up to the number of pairs that fit
 // the GPU at once (persistent).
-template <int MODE, typename T, int NB>
+template <int MODE, typename T, int NB, int GEN>
 cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
                      const CUtensorMap& B, const CUtensorMap& C, int64_t pair_tiles_max) {
-  auto kern = k_gemm_tc<MODE, T, NB>;
+  auto kern = k_gemm_tc<MODE, T, NB, GEN>;
   constexpr int smem = smem_bytes<MODE, NB>();
   // per-device cache of the pairs that fit at once (the shared-memory attribute is set on
   // the first launch of each device); concurrent first launches may both set and store it
@@ -1154,8 +1212,19 @@ cudaError_t launch_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtenso
 template <int MODE, int NB>
 cudaError_t launch_mode(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap& A,
                         const CUtensorMap& B, const CUtensorMap& C, int64_t tiles_max) {
-  if (a.dt == FLCE_BF16) return launch_t<MODE, __nv_bfloat16, NB>(a, chunk, s, A, B, C, tiles_max);
-  return launch_t<MODE, __half, NB>(a, chunk, s, A, B, C, tiles_max);
+  // the forward has builds of its own for launches with a bias or a logit scale
+  if constexpr (MODE == FWD) {
+    if (a.logit_scale != 1.0f) {
+      if (a.dt == FLCE_BF16) return launch_t<MODE, __nv_bfloat16, NB, 2>(a, chunk, s, A, B, C, tiles_max);
+      return launch_t<MODE, __half, NB, 2>(a, chunk, s, A, B, C, tiles_max);
+    }
+    if (a.bias != nullptr) {
+      if (a.dt == FLCE_BF16) return launch_t<MODE, __nv_bfloat16, NB, 1>(a, chunk, s, A, B, C, tiles_max);
+      return launch_t<MODE, __half, NB, 1>(a, chunk, s, A, B, C, tiles_max);
+    }
+  }
+  if (a.dt == FLCE_BF16) return launch_t<MODE, __nv_bfloat16, NB, 0>(a, chunk, s, A, B, C, tiles_max);
+  return launch_t<MODE, __half, NB, 0>(a, chunk, s, A, B, C, tiles_max);
 }
 
 }  // namespace tc
