@@ -591,8 +591,9 @@ def run_ours(args):
     if args.api == "torch":
         # the autograd op takes no profiler: whole-step numbers only
         roof = None
-    elif dom in ("fwd", "dx", "dw"):
-        achieved = gemm_flops / (per_step_dom_ms / 1000.0) / 1e12
+    elif dom in ("fwd", "dx", "dw", "bwd"):
+        # "bwd": the dX and dW GEMMs in one launch (two GEMMs' FLOPs)
+        achieved = gemm_flops * (2 if dom == "bwd" else 1) / (per_step_dom_ms / 1000.0) / 1e12
         if sp["dtype"] == "f32":
             # fp32 inputs run the SIMT FMA kernels: the bound is the FP32 FMA pipes
             peak, peak_kind = fp32_fma_peak(peaks, dev)
@@ -602,16 +603,18 @@ def run_ours(args):
             bound = "tensor"
 
         def gemm_entry(k):
-            tf = gemm_flops / (stages[k][0] / args.steps / 1000.0) / 1e12
+            tf = gemm_flops * (2 if k == "bwd" else 1) / (stages[k][0] / args.steps / 1000.0) / 1e12
             return {"ms_per_step": stages[k][0] / args.steps, "tflops": tf, "frac": tf / peak,
                     "traffic": (rec["per_launch_bytes"].get(k) if rec else None)}
         roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": peak_kind,
                 "sm_mhz_median": (clocks or {}).get("sm_mhz"),
-                "per_launch": f"2*H*V FLOPs per labelled row x {n_lab * args.steps / max(dom_launches, 1):.0f} rows per launch",
+                "per_launch": (f"{4 if dom == 'bwd' else 2}*H*V FLOPs per labelled row x "
+                               f"{n_lab * args.steps / max(stages[dom][1] / (2 if dom in ('dx', 'bwd') else 1), 1):.0f} "
+                               f"rows per launch"),
                 "traffic": (rec["per_launch_bytes"].get(dom) if rec else None),
                 "traffic_source": "profiles/traffic.json (ncu, full size)" if rec else None,
-                "gemms": {k: gemm_entry(k) for k in ("fwd", "dx", "dw") if k in stages and stages[k][1] > 0}}
+                "gemms": {k: gemm_entry(k) for k in ("fwd", "dx", "dw", "bwd") if k in stages and stages[k][1] > 0}}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": peaks.get("hbm_gbs"),
                 "unit": "GB/s", "frac": None, "traffic": None}

@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define FLCE_ABI_VERSION 1
+#define FLCE_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define FLCE_API __attribute__((visibility("default")))
@@ -91,6 +91,9 @@ typedef enum flce_dtype { FLCE_F32 = 0, FLCE_BF16 = 1, FLCE_F16 = 2 } flce_dtype
 #define FLCE_FLAG_DW_OVERWRITE 0x4u /* dW and dbias receive this call's gradient instead of
                                      accumulating it (no need to zero them first); with no
                                      labelled row they are set to zero                      */
+#define FLCE_FLAG_SEPARATE_BWD 0x8u /* run the dX and dW GEMMs as two launches instead of
+                                     one launch sharing a work queue (the results are the
+                                     same bits either way)                                 */
 #define FLCE_FLAG_DEBUG_STALL 0x100u /* testing only: the tensor-core forward GEMM leaves
                                      one pipeline stage unfilled so that its bounded waits
                                      run out; the call must then report FLCE_ERR_TIMEOUT */
@@ -108,7 +111,9 @@ typedef enum flce_stage {
   FLCE_STAGE_DW = 6,       /* dW GEMM (accumulating)                                    */
   FLCE_STAGE_REDUCE = 7,   /* mean/sum reductions (and, with FLCE_FLAG_DW_OVERWRITE,
                               the zeroing of dW / dbias when no row is labelled)         */
-  FLCE_STAGE_COUNT = 8
+  FLCE_STAGE_BWD = 8,      /* dX and dW GEMMs in one launch (tensor-core calls with both
+                              gradients and 4096-row or larger chunks), with the dX sum  */
+  FLCE_STAGE_COUNT = 9
 } flce_stage;
 
 /* Opaque profiler: when flce_args.profile is non-NULL, the call records a CUDA event pair

@@ -350,6 +350,17 @@ extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
     } else if (grads) {
       FLCE_TRY(staged(prof, FLCE_STAGE_GPASS, 1, s, [&] { return launch_gpass(a, k, s); }));
     }
+    if (tc && bwd_merged_supported(a)) {
+      // dX and dW in one launch (shared work queue), then the dX sum and scatter
+      FLCE_TRY(staged(prof, FLCE_STAGE_BWD, 2, s, [&] {
+        cudaError_t e = cudaMemsetAsync(a.w.dxacc, 0, 2 * (size_t)a.R * a.H * 4, s);
+        if (e != cudaSuccess) return e;
+        e = launch_bwd_tc(ar, k, s);
+        if (e != cudaSuccess) return e;
+        return launch_dx_store(a, k, s);
+      }));
+      continue;
+    }
     if (a.want_dX) {
       if (tc) {
         FLCE_TRY(staged(prof, FLCE_STAGE_DX, 2, s, [&] {

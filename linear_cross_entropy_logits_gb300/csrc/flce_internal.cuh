@@ -48,7 +48,7 @@ struct Ctrl {
   float cbar;     // uniform gradient factor: g/n_lab (mean), g (sum), 1 (none)
   float inv_n;    // 1/n_lab for mean (0 when n_lab == 0), 1 for sum
   int fb;         // row-reference mode: 1 when a row of the current chunk left the window
-  int pad;
+  int queue;      // work-item counter of the merged dX + dW launch (zeroed before it)
 };
 
 // Workspace layout for one call; every region is 256-byte aligned.
@@ -157,6 +157,10 @@ bool tc_supported(const CallArgs& a);
 cudaError_t launch_fwd_tc(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_dx_tc(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s);
+// dX and dW in one persistent launch with a device-wide work queue; for chunks whose dW
+// takes the 256 x 512 tile (bwd_merged_supported)
+bool bwd_merged_supported(const CallArgs& a);
+cudaError_t launch_bwd_tc(const CallArgs& a, int chunk, cudaStream_t s);
 cudaError_t launch_dx_store(const CallArgs& a, int chunk, cudaStream_t s);  // dxacc -> dX rows
 
 int num_sms();

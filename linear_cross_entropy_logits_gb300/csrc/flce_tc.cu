@@ -1124,6 +1124,363 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------ merged dX + dW launch
+// One persistent launch runs a chunk's dX items (256 x 512 tiles over K = V, split in up to
+// four K ranges as in the DX mode) and its dW tiles (256 x 512 over K = chunk rows). The
+// pairs take items from a device-wide queue, an atomic counter in the workspace's control
+// record, in index order: item g < n_dx is dX item g (split-major), item g >= n_dx the dW
+// tile g - n_dx. A pair that finishes its last dX item starts on dW tiles at once instead of
+// idling through dX's last partial wave, and the dW tiles in flight still walk the slab in
+// step. The leader CTA's producer draws each index and hands it to the other roles of both
+// CTAs through a ring of QD slots in shared memory (full / empty barriers per slot). Results
+// do not depend on which pair runs which item: a dX buffer element still receives at most two
+// adds onto zero, and each dW tile is added by the one pair that drew it.
+constexpr int QD = 4;
+constexpr int Q_CONSUMERS = 2 + 2 * 8;  // peer producer, MMA issuer, both CTAs' epilogue warps
+constexpr int NUM_BARS_BWD = NUM_BARS + 2 * QD;
+
+struct BwdSpace {
+  TileSpace dx, dw;
+  int S, ntx, n_dx, n_items;
+};
+__device__ __forceinline__ BwdSpace bwd_space(const CallArgs& a, int rows, int npairs) {
+  BwdSpace b;
+  b.dx = tile_space<DX, 2>(a, rows);
+  b.dw = tile_space<DW, 2>(a, rows);
+  b.ntx = b.dx.mt * b.dx.nt;
+  b.S = dx_splits(b.ntx, npairs, b.dx.nkb);
+  b.n_dx = b.S * b.ntx;
+  b.n_items = b.n_dx + b.dw.mt * b.dw.nt;
+  return b;
+}
+struct BwdItem {
+  int dw, m, n, k0, k1, split;
+};
+__device__ __forceinline__ BwdItem bwd_item(const BwdSpace& b, int g) {
+  BwdItem it;
+  if (g < b.n_dx) {
+    it.dw = 0;
+    it.split = g / b.ntx;
+    const int t = g - it.split * b.ntx;
+    it.n = t % b.dx.nt;  // n fastest: the pairs in flight share the slab rows
+    it.m = t / b.dx.nt;
+    it.k0 = (int)((int64_t)b.dx.nkb * it.split / b.S);
+    it.k1 = (int)((int64_t)b.dx.nkb * (it.split + 1) / b.S);
+  } else {
+    const int t = g - b.n_dx;
+    it.dw = 1;
+    it.split = 0;
+    it.n = t % b.dw.nt;  // n fastest: the pairs in flight share the slab columns
+    it.m = t / b.dw.nt;
+    it.k0 = 0;
+    it.k1 = b.dw.nkb;
+  }
+  return it;
+}
+
+// Bounded wait with cluster-scope acquire, for barriers that another CTA's release-arrive
+// completes together with data it stored into this CTA's shared memory (the queue slots).
+__device__ __noinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, const Abort& ab) {
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(50000u)
+        : "memory");
+    if (ok) return true;
+    if (*ab.flag) return false;
+    if (gtimer() - t0 > ab.timeout_ns) {
+      *ab.flag = 1;
+      st_cluster_u32(ab.peer_flag, 1u);
+      atomicOr(ab.status, ST_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_bwd(const __grid_constant__ CUtensorMap tmAx, const __grid_constant__ CUtensorMap tmBx,
+               const __grid_constant__ CUtensorMap tmCx, const __grid_constant__ CUtensorMap tmAw,
+               const __grid_constant__ CUtensorMap tmBw, const __grid_constant__ CUtensorMap tmCw,
+               const __grid_constant__ CallArgs a, const int chunk) {
+  constexpr int NB = 2;
+  constexpr int STAGES = stages_of<NB>();
+  constexpr int SBYTES = stage_bytes<NB>();
+  constexpr int NEPI = epi_warps_of<NB>();
+  constexpr int NBUF = epi_nbuf_of<NB>();
+  constexpr int HB = half_bufs_of<NB>();
+  int row0 = 0, rows = 0;
+  if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = (int)cluster_id_x(), npairs = (int)nclusters_x();
+  const BwdSpace bs = bwd_space(a, rows, npairs);
+  // both CTAs of a pair take the same decision; pairs beyond the item count never draw
+  if (bs.dx.nkb <= 0 || bs.dw.nkb <= 0 || pair >= bs.n_items) return;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* epi_stage = smem + STAGES * SBYTES;
+  uint64_t* bars = (uint64_t*)(smem + STAGES * SBYTES + epi_bytes_of<NB>());
+  uint32_t* tmem_slot = (uint32_t*)(bars + NUM_BARS_BWD);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  int* copies = (int*)(tmem_slot + 2);  // per stage: phases this CTA's producer filled / armed
+  int* qitem = copies + STAGES;         // the queue ring: item index per slot
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t tfull = bar0 + 8u * (2 * STAGES);
+  const uint32_t tempty = bar0 + 8u * (2 * STAGES + 2);
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto qfull_bar = [&](int q) { return bar0 + 8u * (NUM_BARS + q); };
+  auto qempty_bar = [&](int q) { return bar0 + 8u * (NUM_BARS + QD + q); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Abort ab{abort_flag, mapa(smem_u32((const void*)abort_flag), rank ^ 1u), a.w.status, a.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      copies[s] = 0;
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * NEPI);
+    mbar_init(drain_bar, 1);
+    for (int q = 0; q < QD; ++q) {
+      mbar_init(qfull_bar(q), 1);              // the leader's producer, locally or remotely
+      mbar_init(qempty_bar(q), Q_CONSUMERS);   // used in the leader CTA
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmAx) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmBx) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmAw) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmBw) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Next item of this pair from the queue ring (every role but the drawing one): false on
+  // abort. The slot is released on the leader's empty barrier once the index is read.
+  auto take = [&](int& slot, uint32_t& qph, int& g) -> bool {
+    if (!wait_bounded_cluster(qfull_bar(slot), qph, ab)) return false;
+    g = ((volatile int*)qitem)[slot];
+    return true;
+  };
+  auto release_slot = [&](int slot) {
+    if (leader) mbar_arrive(qempty_bar(slot));
+    else mbar_arrive_cluster(mapa(qempty_bar(slot), 0));
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs); the leader's also draws the items
+      int s = 0;
+      uint32_t ph = 0;
+      const int half = (int)rank * BM;
+      int slot = 0;
+      uint32_t qph = 0;
+      for (;;) {
+        int g;
+        if (leader) {
+          // the slot's previous index has been read by every role of both CTAs
+          if (!wait_bounded_cluster(qempty_bar(slot), qph ^ 1u, ab)) break;
+          g = atomicAdd(&a.w.ctrl->queue, 1);
+          qitem[slot] = g;
+          st_cluster_u32(mapa(smem_u32(&qitem[slot]), 1), (uint32_t)g);
+          mbar_arrive(qfull_bar(slot));
+          mbar_arrive_cluster(mapa(qfull_bar(slot), 1));
+        } else {
+          if (!take(slot, qph, g)) break;
+          release_slot(slot);
+        }
+        if (++slot == QD) {
+          slot = 0;
+          qph ^= 1u;
+        }
+        if (g >= bs.n_items) break;
+        const BwdItem it = bwd_item(bs, g);
+        int kb = it.k0;
+        for (; kb < it.k1; ++kb) {
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, ab, true)) break;
+          const uint32_t fb = leader ? full_bar(s) : mapa(full_bar(s), 0);
+          if (leader) mbar_expect_tx(full_bar(s), 2 * SBYTES);
+          const uint32_t adst = smem_u32(smem + s * SBYTES);
+          const uint32_t bdst = adst + A_BYTES;
+          if (it.dw) {
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+              tma_load_2d(adst + jj * BOX_BYTES, &tmAw, fb, it.m * 2 * BM + half + jj * 64, kb * BK);
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+#pragma unroll
+              for (int jj = 0; jj < 2; ++jj)
+                tma_load_2d(bdst + j * B_BYTES + jj * BOX_BYTES, &tmBw, fb,
+                            (it.n * NB + j) * BN + half + jj * 64, kb * BK);
+          } else {
+            tma_load_2d(adst, &tmAx, fb, kb * BK, it.m * 2 * BM + half);
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+#pragma unroll
+              for (int jj = 0; jj < 2; ++jj)
+                tma_load_2d(bdst + j * B_BYTES + jj * BOX_BYTES, &tmBx, fb,
+                            (it.n * NB + j) * BN + half + jj * 64, kb * BK);
+          }
+          copies[s] += 1;  // leader: phases armed; peer: phases filled
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (kb < it.k1) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (leader CTA)
+      constexpr uint32_t idesc_dx = make_idesc<DX, T>();
+      constexpr uint32_t idesc_dw = make_idesc<DW, T>();
+      int s = 0;
+      uint32_t ph = 0;
+      int slot = 0;
+      uint32_t qph = 0;
+      bool ok = true;
+      for (int n_it = 0; ok; ++n_it) {
+        int g;
+        if (!take(slot, qph, g)) break;
+        release_slot(slot);
+        if (++slot == QD) {
+          slot = 0;
+          qph ^= 1u;
+        }
+        if (g >= bs.n_items) break;
+        const BwdItem it = bwd_item(bs, g);
+        if (!wait_bounded(tempty, ((uint32_t)n_it & 1u) ^ 1u, ab, true)) break;
+        tc_fence_after();
+        const uint32_t idesc = it.dw ? idesc_dw : idesc_dx;
+        for (int kb = it.k0; kb < it.k1; ++kb) {
+          if (!wait_bounded(full_bar(s), ph, ab, true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t abase = smem_u32(smem + s * SBYTES);
+          const uint32_t bbase = abase + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // dX: A = slab K-major; dW: A = slab^T MN-major; B MN-major for both
+            const uint64_t ad = it.dw ? sdesc(abase + k * 2048, 8192, 1024) : sdesc(abase + k * 32, 16, 1024);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              const uint64_t bd = sdesc(bbase + j * B_BYTES + k * 2048, 8192, 1024);
+              mma_f16(tmem_base + (uint32_t)(j * BN), ad, bd, idesc, (kb != it.k0 || k != 0) ? 1u : 0u);
+            }
+          }
+          mma_commit_pair(empty_bar(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull);
+      }
+      mma_commit_local(drain_bar);
+      wait_bounded(drain_bar, 0u, ab, false);
+    }
+  } else if (warp - 2 < NEPI) {
+    // ---------------- epilogue warps (both CTAs): TMEM lane quadrant warp % 4 of 256-column
+    // sub-tile (warp - 2) / 4
+    const int q = warp & 3;
+    const int j = (warp - 2) >> 2;
+    const float cb = a.w.ctrl->cbar;
+    const float* rsc = (a.ref_mode && a.w.ctrl->fb == 0) ? a.w.rsc : nullptr;
+    const bool ovw = (a.flags & FLCE_FLAG_DW_OVERWRITE) && chunk == 0;
+    uint8_t* stg = epi_stage + (warp - 2) * epi_warp_bytes_of<NB>();
+    uint32_t epi_it = 0;
+    int slot = 0;
+    uint32_t qph = 0;
+    for (int n_it = 0;; ++n_it) {
+      int g;
+      bool ok = take(slot, qph, g);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      if (lane == 0) release_slot(slot);
+      if (++slot == QD) {
+        slot = 0;
+        qph ^= 1u;
+      }
+      if (g >= bs.n_items) break;
+      const BwdItem it = bwd_item(bs, g);
+      ok = wait_bounded(tfull, (uint32_t)n_it & 1u, ab, true);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int nsub = it.n * NB + j;
+      const int mrow = it.m * 2 * BM + (int)rank * BM;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * BN);
+      if (nsub < bs.dx.nsub) {
+        if (!it.dw)
+          epilogue_reduce<NBUF, true, float, HB>(a, &tmCx, stg, mrow, nsub, (int)a.R, (it.split >> 1) * (int)a.R,
+                                                 taddr, q, lane, cb, rsc, false, epi_it);
+        else if (a.dW_dt != FLCE_F32)
+          epilogue_reduce<NBUF, true, T, HB>(a, &tmCw, stg, mrow, nsub, (int)a.V, 0, taddr, q, lane, cb, nullptr, ovw,
+                                             epi_it);
+        else
+          epilogue_reduce<NBUF, true, float, HB>(a, &tmCw, stg, mrow, nsub, (int)a.V, 0, taddr, q, lane, cb, nullptr,
+                                                 ovw, epi_it);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty);
+        else mbar_arrive_cluster(mapa(tempty, 0));
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  // ---------------- teardown (as in k_gemm_tc)
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 0 && lane == 0 && leader) {
+    for (int s = 0; s < STAGES; ++s) {
+      const int mine = copies[s];
+      const int peer = (int)ld_cluster_u32(mapa(smem_u32(&copies[s]), 1));
+      int last = mine;
+      if (peer > mine) {
+        mbar_expect_tx(full_bar(s), SBYTES);
+        last = peer;
+      } else if (peer < mine) {
+        mbar_complete_tx(full_bar(s), SBYTES);
+      }
+      if (last > 0) wait_bounded(full_bar(s), (uint32_t)(last - 1) & 1u, ab, false);
+    }
+  }
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1277,6 +1634,79 @@ cudaError_t launch_dw_tc(const CallArgs& a, int chunk, cudaStream_t s) {
   const int64_t vt = (a.V + 255) / 256, ht = (a.H + 255) / 256;
   if (wide) return tc::launch_mode<tc::DW, 2>(a, chunk, s, A, B, C, vt * ((ht + 1) / 2));
   return tc::launch_mode<tc::DW, 1>(a, chunk, s, A, B, C, vt * ht);
+}
+
+bool bwd_merged_supported(const CallArgs& a) {
+  return a.want_dX && a.want_dW && a.R >= DW_WIDE_MIN_ROWS && !(a.flags & FLCE_FLAG_SEPARATE_BWD);
+}
+
+namespace tc {
+template <typename T>
+cudaError_t launch_bwd_t(const CallArgs& a, int chunk, cudaStream_t s, const CUtensorMap (&m)[6],
+                         int64_t items_max) {
+  auto kern = k_gemm_bwd<T>;
+  constexpr int smem = smem_bytes<DX, 2>();
+  static std::atomic<int> max_pairs[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_pairs[dev].load(std::memory_order_relaxed) == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (unsigned)(num_sms() / 2), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    max_pairs[dev].store(n, std::memory_order_relaxed);
+  }
+  const int mp = max_pairs[dev].load(std::memory_order_relaxed);
+  const int64_t pairs = items_max < mp ? items_max : mp;
+  if (pairs <= 0) return cudaSuccess;
+  // the queue counter starts at zero for every launch
+  e = cudaMemsetAsync(&a.w.ctrl->queue, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(2 * (unsigned)pairs, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, m[0], m[1], m[2], m[3], m[4], m[5], a, chunk);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+}  // namespace tc
+
+cudaError_t launch_bwd_tc(const CallArgs& a, int chunk, cudaStream_t s) {
+  CUtensorMap m[6];
+  const uint64_t esz = 2;
+  // dX: A = slab K-major, B = W MN-major, C = the two fp32 accumulator buffers [2R, H]
+  if (!tc::make_map(&m[0], a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 128)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&m[1], a.W, a.dt, a.H, a.V, a.H * esz, 64, 64)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&m[2], a.w.dxacc, FLCE_F32, a.H, 2 * a.R, a.H * 4, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  // dW: A = slab^T MN-major, B = Xc MN-major, C = dW (fp32 16-column or 16-bit 32-column boxes)
+  if (!tc::make_map(&m[3], a.w.slab, a.dt, a.V, a.R, a.Vp * esz, 64, 64)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&m[4], a.w.xc, a.dt, a.H, a.R, a.Hp * esz, 64, 64)) return cudaErrorInvalidValue;
+  if (a.dW_dt == FLCE_F32) {
+    if (!tc::make_map(&m[5], a.dW, FLCE_F32, a.H, a.V, a.H * 4, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!tc::make_map(&m[5], a.dW, a.dW_dt, a.H, a.V, a.H * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  }
+  const int64_t ht2 = ((a.H + 255) / 256 + 1) / 2;
+  const int64_t items = tc::DX_MAX_SPLITS * ((a.R + 255) / 256) * ht2 + ((a.V + 255) / 256) * ht2;
+  if (a.dt == FLCE_BF16) return tc::launch_bwd_t<__nv_bfloat16>(a, chunk, s, m, items);
+  return tc::launch_bwd_t<__half>(a, chunk, s, m, items);
 }
 
 }  // namespace flce

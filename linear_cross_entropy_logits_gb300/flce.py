@@ -23,6 +23,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 FLAG_FORCE_SIMT = 0x1
 FLAG_NO_ROW_REF = 0x2
 FLAG_DW_OVERWRITE = 0x4
+FLAG_SEPARATE_BWD = 0x8
 FLAG_DEBUG_STALL = 0x100
 EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_fwd_bwd_noalloc",
             "flce_get_status",
@@ -30,7 +31,7 @@ EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_fwd_
             "flce_profile_read", "flce_last_cuda_error", "flce_status_string", "flce_abi_version",
             "flce_jsd_workspace_size", "flce_fused_linear_jsd", "flce_scale_by",
             "flce_plan_describe")
-STAGES = ("prologue", "gather", "fwd", "finalize", "gpass", "dx", "dw", "reduce")
+STAGES = ("prologue", "gather", "fwd", "finalize", "gpass", "dx", "dw", "reduce", "bwd")
 
 
 class FlceArgs(ctypes.Structure):

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
     for name in _declared():
         assert name in exported, name
         assert hasattr(lib, name)
-    assert lib.flce_abi_version() == 1
+    assert lib.flce_abi_version() == 2
 
 
 @pytest.mark.parametrize("cls,cname", [(flce.FlceArgs, "flce_args"), (flce.FlceJsdArgs, "flce_jsd_args")])
