@@ -782,8 +782,8 @@ def run_jsd(args):
                "copies": "H2D of step k+1 on a copy stream overlapping step k (double-buffered)"}
     peaks, src = load_peaks()
     tflops = flops / (ms / 1000.0) / 1e12
-    dom = max(("fwd", "dx", "dw"), key=lambda k: stages[k][0])
-    dom_flops = 2.0 * n_lab * V * ((Hs + Ht) if dom == "fwd" else Hs)
+    dom = max(("fwd", "dx", "dw", "bwd"), key=lambda k: stages[k][0])
+    dom_flops = 2.0 * n_lab * V * {"fwd": Hs + Ht, "bwd": 2 * Hs}.get(dom, Hs)
     achieved = dom_flops / (stages[dom][0] / args.steps / 1000.0) / 1e12
     peak, peak_kind = peak_for_region(peaks, src, evs[0].elapsed_time(evs[-1]))
     line = {"op": "fused_linear_jsd", "metric": metric,

@@ -112,7 +112,7 @@ typedef enum flce_stage {
   FLCE_STAGE_REDUCE = 7,   /* mean/sum reductions (and, with FLCE_FLAG_DW_OVERWRITE,
                               the zeroing of dW / dbias when no row is labelled)         */
   FLCE_STAGE_BWD = 8,      /* dX and dW GEMMs in one launch (tensor-core calls with both
-                              gradients and 4096-row or larger chunks), with the dX sum  */
+                              gradients and 2048-row or larger chunks), with the dX sum  */
   FLCE_STAGE_COUNT = 9
 } flce_stage;
 

@@ -18,10 +18,10 @@ namespace flce {
 constexpr int VT = 256;
 constexpr int CHUNK_ALIGN = 128;   // row-chunk granularity (one tensor-core M tile)
 // Tile-shape thresholds of the tensor-core GEMMs (the reasons are at their use in
-// flce_tc.cu): the dW GEMM takes 256 x 512 pair tiles from chunks of this many rows on, the
-// forward from this hidden size on.
+// flce_tc.cu): the dW GEMM takes 256 x 512 pair tiles (and, with dX, the merged launch)
+// from chunks of this many rows on, the forward from this hidden size on.
 #ifndef FLCE_DW_WIDE_MIN_ROWS
-#define FLCE_DW_WIDE_MIN_ROWS 4096
+#define FLCE_DW_WIDE_MIN_ROWS 2048
 #endif
 #ifndef FLCE_FWD_WIDE_MIN_H
 #define FLCE_FWD_WIDE_MIN_H 4096

@@ -540,6 +540,15 @@ extern "C" int32_t flce_fused_linear_jsd(const flce_jsd_args* x, void* stream) {
       return cudaGetLastError();
     }));
     JSD_TRY(staged(prof, FLCE_STAGE_GPASS, 1, st, [&] { return jsd_rows(j, k, st, grads); }));
+    if (tc && bwd_merged_supported(s)) {
+      // the student's dX and dW in one launch (shared work queue), then the dX sum
+      JSD_TRY(staged(prof, FLCE_STAGE_BWD, 2, st, [&] {
+        cudaError_t e = cudaMemsetAsync(s.w.dxacc, 0, 2 * (size_t)p.R * s.H * 4, st);
+        if (e == cudaSuccess) e = launch_bwd_tc(s, k, st);
+        return e != cudaSuccess ? e : launch_dx_store(s, k, st);
+      }));
+      continue;
+    }
     if (s.want_dX) {
       if (tc) {
         JSD_TRY(staged(prof, FLCE_STAGE_DX, 2, st, [&] {

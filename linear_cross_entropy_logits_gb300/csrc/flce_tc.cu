@@ -65,7 +65,10 @@ enum Mode { FWD = 0, DX = 1, DW = 2 };
 // The forward takes NB = 2 when H >= FWD_WIDE_MIN_H and NB = 1 below (a short K cannot
 // hide the exposed epilogue of the single accumulator); dX takes NB = 2 (K = V, the
 // epilogue is negligible); dW takes NB = 2 when a chunk holds at least DW_WIDE_MIN_ROWS
-// rows (K long enough to amortise the exposed reduce-add epilogue) and NB = 1 below that.
+// rows and NB = 1 below that. At 2048 to 4096 rows the two dW shapes run at the same rate
+// (the wide tile's exposed reduce-add epilogue against the narrow one's operand feed), and
+// the wide one lets dW share the merged dX + dW launch (2.5% faster on the large-vocab
+// head at 2688-row chunks; outputs bit-identical).
 // DW_WIDE_MIN_ROWS, FWD_WIDE_MIN_H (flce_internal.cuh): the forward takes the wide tile
 // from H = 4096 on, where its K loop is long enough that the wide tile's smaller operand
 // traffic per FLOP outweighs its exposed epilogue (measured 1% faster at H = 4096, in short

@@ -1,5 +1,5 @@
 """The merged dX + dW launch (one persistent kernel over a device-wide work queue, used by
-tensor-core calls with both gradients whose chunks hold 4096 rows or more) against the
+tensor-core calls with both gradients whose chunks hold 2048 rows or more) against the
 float64 oracle, element by element, at sizes with ragged tails in every dimension; and bit
 for bit against the same call run as two launches (FLCE_FLAG_SEPARATE_BWD): which pair
 draws which work item must not change a single bit. The products are the grad_input and
@@ -35,10 +35,10 @@ def _chunk_rows(sp, budget):
 
 @pytest.mark.parametrize("reduction,z", [("mean", 1e-4), ("sum", 0.0)])
 def test_merged_matches_oracle_one_chunk(reduction, z):
-    # 4500 rows, 380 of them ignored at random: one chunk of 4608 rows (>= 4096: merged)
+    # 4500 rows, 380 of them ignored at random: one chunk of 4608 rows (>= 2048: merged)
     sp = I.spec("frozen_head", BT=4500, H=200, V=5000, w_std=0.1, bias_std=None, n_ignored=380,
                 reduction=reduction, grad_out=None, want_dW=True, z=z)
-    assert _chunk_rows(sp, 0) >= 4096
+    assert _chunk_rows(sp, 0) >= 2048
     inp = I.generate(sp, seed=61)
     compare_full(run_gpu(inp, sp), run_oracle(inp, sp), inp, sp)
 

@@ -7,9 +7,10 @@ Llama-3.1-8B and frozen-head workloads, in the launch configuration the benchmar
 (default workspace, gradients on; reduction "none" with the workload's per-token upstream
 gradient, or ones, so that every per-token loss is returned). Compared: lse and per-token
 loss of every row within the bf16 tolerance (2e-3 relative), the prediction bit exact
-outside the fp32 tie band, the ignored-row outputs bit exact, and the whole dX and dW
-within the 1e-2 relative-Frobenius tolerance. The large-vocab workload (3 x 92 TFLOP of
-float64) stays on sampled rows and vocabulary entries.
+outside the fp32 spread of the two competing logits (count printed and capped), the
+ignored-row outputs bit exact, and the whole dX and dW within the 1e-2 relative-Frobenius
+tolerance. The large-vocab workload has its own file (every row, dW on sampled vocabulary
+rows across all its chunks).
 """
 
 import numpy as np
@@ -20,7 +21,7 @@ from linear_cross_entropy_logits_gb300 import build as B
 from linear_cross_entropy_logits_gb300 import flce
 from linear_cross_entropy_logits_gb300 import inputs as I
 from oracle import flce_oracle as orc
-from parity_util import TOL, pred_ok, rel_fro
+from parity_util import TOL, max_argmax_mismatches, pred_ok, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -68,6 +69,7 @@ def test_every_output_full_size(base, ov):
     dX_ref = np.zeros((BT, H))
     dW_ref = np.zeros((V, H)) if dW_gpu is not None else None
     worst_lse = worst_loss = 0.0
+    n_mis = 0
     for k0 in range(0, rows.size, 1024):
         r = rows[k0:k0 + 1024]
         s = orc.logits_rows(X[r], W64, b)
@@ -82,7 +84,11 @@ def test_every_output_full_size(base, ov):
         worst_lse = max(worst_lse, float(np.max(np.abs(lse[r] - o_lse) / np.abs(o_lse))))
         worst_loss = max(worst_loss, float(np.max(np.abs(loss[r] - o_loss) / np.maximum(np.abs(o_loss), 1e-3))))
         ok, where = pred_ok(pred[r], o_pred, X, W64, b, r, mask[r])
-        assert ok, f"argmax mismatch outside the tie band at row {where}"
+        assert ok, f"argmax mismatch outside the fp32 spread at row {where}"
+        n_mis += where
+    print(f"{base}: lse rel {worst_lse:.2e}, loss rel {worst_loss:.2e}, argmax near-tie mismatches "
+          f"{n_mis} of {rows.size} rows")
+    assert n_mis <= max_argmax_mismatches(rows.size)
     assert worst_lse <= tol, f"lse rel err {worst_lse}"
     assert worst_loss <= tol, f"per-token loss rel err {worst_loss}"
     gtol = TOL[sp["dtype"]]["grad"]
