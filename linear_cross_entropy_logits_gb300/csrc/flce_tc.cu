@@ -376,6 +376,21 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "memory");
 }
 
+// N consecutive fp32 columns (N = 32 or 64), waited for.
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 64) tmem_ld64(taddr, r);
+  else tmem_ld32(taddr, r);
+}
+
+// Columns per TMEM load in the forward epilogue (32 or 64): the block over which a thread
+// keeps its row's logits in registers, takes a maximum and may search the argmax.
+#ifndef FLCE_FWD_COLS
+#define FLCE_FWD_COLS 64
+#endif
+constexpr int FC = FLCE_FWD_COLS;
+static_assert(FC == 32 || FC == 64, "forward epilogue block");
+
 // 2^x by the hardware approximation (ex2.approx.ftz: relative error about 2^-22, results
 // below 2^-126 flushed to zero), far finer than the 2^-9 rounding of the 16-bit slab the
 // values are stored in; the accurate library exp2f made the epilogue arithmetic-bound.
@@ -493,31 +508,32 @@ struct Items {
 };
 
 // ------------------------------------------------------------------ epilogues
-// The forward epilogues write the exp slab straight from registers: each thread holds 64
-// consecutive columns of its row as 16-bit values (128 bytes, one whole line) and stores
-// them with four 32-byte stores. Slab rows past R are skipped (the slab has R rows; rows
+// The forward epilogues write the exp slab straight from registers: each thread holds FC
+// consecutive columns of its row as 16-bit values (64 columns: 128 bytes, one whole line)
+// and stores them with 32-byte stores. Slab rows past R are skipped (the slab has R rows; rows
 // between the chunk's end and R hold values nothing reads, and the zero Xc rows there make
 // them finite).
 template <typename T>
-__device__ __forceinline__ void store_slab64(const CallArgs& a, int rr, int col, const uint32_t (&pk)[32]) {
+__device__ __forceinline__ void store_slab(const CallArgs& a, int rr, int col, const uint32_t (&pk)[FC / 2]) {
   if (rr >= (int)a.R) return;
   uint32_t* dst = (uint32_t*)((T*)a.w.slab + (int64_t)rr * a.Vp + col);  // 32-byte aligned
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int j = 0; j < FC / 16; ++j)
     asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 8 * j), "r"(pk[8 * j]),
                  "r"(pk[8 * j + 1]), "r"(pk[8 * j + 2]), "r"(pk[8 * j + 3]), "r"(pk[8 * j + 4]),
                  "r"(pk[8 * j + 5]), "r"(pk[8 * j + 6]), "r"(pk[8 * j + 7])
                  : "memory");
 }
 
-// r[idx] for a per-thread index 0 <= idx < 64 by a six-level select tree (indexing the
-// register array at run time would move it to local memory).
-__device__ __forceinline__ float select64(const uint32_t (&r)[64], int idx) {
-  float x[32];
+// r[idx] for a per-thread index 0 <= idx < N by a select tree (indexing the register
+// array at run time would move it to local memory).
+template <int N>
+__device__ __forceinline__ float select_n(const uint32_t (&r)[N], int idx) {
+  float x[N / 2];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) x[i] = __uint_as_float((idx & 1) ? r[2 * i + 1] : r[2 * i]);
+  for (int i = 0; i < N / 2; ++i) x[i] = __uint_as_float((idx & 1) ? r[2 * i + 1] : r[2 * i]);
 #pragma unroll
-  for (int w = 16, b = 2; w >= 1; w >>= 1, b <<= 1) {
+  for (int w = N / 4, b = 2; w >= 1; w >>= 1, b <<= 1) {
 #pragma unroll
     for (int i = 0; i < w; ++i) x[i] = (idx & b) ? x[2 * i + 1] : x[2 * i];
   }
@@ -535,15 +551,15 @@ __device__ __forceinline__ float logit_of(uint32_t acc, int v, float ls, const T
   return s;
 }
 
-// The target logit of a row whose target column lies in the 64 columns just loaded
-// (loc in [0, 64)). The warp picks it out only when one of its 32 rows has its target
+// The target logit of a row whose target column lies in the FC columns just loaded
+// (loc in [0, FC)). The warp picks it out only when one of its 32 rows has its target
 // there (about one 64-column block in 60 at V = 128256), so no per-column comparison runs.
 template <typename T, bool SCALE, bool BIAS>
-__device__ __forceinline__ void pick_target(const uint32_t (&r)[64], int loc, int v, float ls, const T* bias,
+__device__ __forceinline__ void pick_target(const uint32_t (&r)[FC], int loc, int v, float ls, const T* bias,
                                             float& tl) {
-  const bool mine = (unsigned)loc < 64u;
+  const bool mine = (unsigned)loc < (unsigned)FC;
   if (__any_sync(0xffffffffu, mine)) {
-    const float tv = select64(r, loc & 63);
+    const float tv = select_n<FC>(r, loc & (FC - 1));
     if (mine) tl = logit_of<T, SCALE, BIAS>(__float_as_uint(tv), v, ls, bias);
   }
 }
@@ -560,16 +576,16 @@ __device__ __forceinline__ void pick_target(const uint32_t (&r)[64], int loc, in
 //
 // Lowest column among the 64 just evaluated whose logit equals m (their maximum); s holds
 // the logits (columns past the vocabulary hold -inf, never equal to a searched maximum).
-__device__ __forceinline__ int find_max_col(const uint32_t (&s)[64], int vbase, float m) {
+__device__ __forceinline__ int find_max_col(const uint32_t (&s)[FC], int vbase, float m) {
   int j0 = 0;
 #pragma unroll
-  for (int j = 63; j >= 0; --j)
+  for (int j = FC - 1; j >= 0; --j)
     if (__uint_as_float(s[j]) == m) j0 = j;
   return vbase + j0;
 }
 
 // Argmax bookkeeping after a 64-column block of logits s with maximum bm (warp-collective).
-__device__ __forceinline__ void argmax_update(const uint32_t (&s)[64], int vbase, float bm, float thr, float& mx,
+__device__ __forceinline__ void argmax_update(const uint32_t (&s)[FC], int vbase, float bm, float thr, float& mx,
                                               int& ai) {
   const bool need = bm > mx && bm >= thr;
   if (__any_sync(0xffffffffu, need)) {
@@ -584,11 +600,11 @@ __device__ __forceinline__ void argmax_update(const uint32_t (&s)[64], int vbase
 // the vocabulary (all but the last tile), no column test; columns past the vocabulary count
 // as -inf (exp 0).
 template <typename T, bool FULL, bool SCALE, bool BIAS>
-__device__ __forceinline__ void fwd_ref_cols(uint32_t (&r)[64], int vbase, int V, float ls, const T* bias,
-                                             float& bm, float (&sum4)[4], uint32_t (&pk)[32]) {
+__device__ __forceinline__ void fwd_ref_cols(uint32_t (&r)[FC], int vbase, int V, float ls, const T* bias,
+                                             float& bm, float (&sum4)[4], uint32_t (&pk)[FC / 2]) {
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int jj = 0; jj < 64; jj += 2) {
+  for (int jj = 0; jj < FC; jj += 2) {
     const int v = vbase + jj;
     const int u = (jj >> 1) & 3;
     float s0 = -INFINITY, s1 = -INFINITY;
@@ -623,24 +639,42 @@ __device__ __forceinline__ void write_tile_stats(const CallArgs& a, int rr, int 
   if (want_arg && a.w.rmax != nullptr && mx > thr) atomicMax(a.w.rmax + rr, max_key(mx));
 }
 
+// The per-row values a forward epilogue thread needs for a tile: its row within the chunk,
+// the row's target (through the compaction index) and the running row maximum. Read before
+// the epilogue waits for its accumulator, so that the two dependent global loads and the
+// threshold load overlap the wait instead of starting the tile's work.
+struct FwdRow {
+  int rr;
+  bool valid;
+  int64_t tg;  // target column of the row (-1: none wanted or not a row of the chunk)
+  float thr;
+};
+__device__ __forceinline__ FwdRow fwd_row(const CallArgs& a, int row0, int rows, int mrow, int q, int lane) {
+  FwdRow f;
+  f.rr = mrow + q * 32 + lane;
+  f.valid = f.rr < rows;
+  f.tg = -1;
+  f.thr = -INFINITY;
+  if (f.valid && a.targets != nullptr) {  // the distillation op needs no argmax
+    f.tg = a.targets[a.w.idx[row0 + f.rr]];
+    f.thr = row_threshold(a, f.rr);
+  }
+  return f;
+}
+
 // Row-reference forward epilogue: exp(s) needs no tile max, so one pass over TMEM (64
 // columns per wait) gives the max / lowest-index argmax, the target logit and the exp
 // values, written to the slab.
 template <typename T, bool SCALE, bool BIAS>
-__device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, int row0, int rows, int mrow, int n,
-                                                 uint32_t taddr, int q, int lane) {
-  const int rr = mrow + q * 32 + lane;  // row within the chunk
-  const bool valid = rr < rows;
+__device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, const FwdRow& fr, int n, uint32_t taddr) {
+  const int rr = fr.rr;
+  const bool valid = fr.valid;
   const int v0 = n * VT;
   const int V = (int)a.V;
   const bool want_arg = a.targets != nullptr;  // the distillation op needs no argmax
-  int toff = -1;  // the target's column within this tile, or -1
-  float thr = -INFINITY;
-  if (valid && want_arg) {
-    const int64_t tg = a.targets[a.w.idx[row0 + rr]];
-    if (tg >= v0 && tg < v0 + BN) toff = (int)(tg - v0);
-    thr = row_threshold(a, rr);
-  }
+  const float thr = fr.thr;
+  // the target's column within this tile, or -1
+  const int toff = (fr.tg >= v0 && fr.tg < v0 + BN) ? (int)(fr.tg - v0) : -1;
   const float ls = a.logit_scale;
   const T* bias = (const T*)a.bias;
   const bool full = v0 + BN <= V;
@@ -648,12 +682,12 @@ __device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, int row0, in
   float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   int ai = v0;
 #pragma unroll 1
-  for (int c2 = 0; c2 < BN / 64; ++c2) {
-    uint32_t r[64];
-    tmem_ld64(taddr + c2 * 64, r);
-    const int vb = v0 + c2 * 64;
-    pick_target<T, SCALE, BIAS>(r, toff - c2 * 64, v0 + toff, ls, bias, tl);
-    uint32_t pk[32];
+  for (int c2 = 0; c2 < BN / FC; ++c2) {
+    uint32_t r[FC];
+    tmem_ldn<FC>(taddr + c2 * FC, r);
+    const int vb = v0 + c2 * FC;
+    pick_target<T, SCALE, BIAS>(r, toff - c2 * FC, v0 + toff, ls, bias, tl);
+    uint32_t pk[FC / 2];
     float bm;
     if (full) {
       fwd_ref_cols<T, true, SCALE, BIAS>(r, vb, V, ls, bias, bm, sum4, pk);
@@ -662,7 +696,7 @@ __device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, int row0, in
     }
     if (want_arg) argmax_update(r, vb, bm, thr, mx, ai);
     if (!want_arg) mx = fmaxf(mx, bm);
-    store_slab64<T>(a, rr, vb, pk);
+    store_slab<T>(a, rr, vb, pk);
   }
   if (valid) {
     write_tile_stats(a, rr, n, mx, (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]), ai, thr, want_arg);
@@ -673,10 +707,10 @@ __device__ __forceinline__ void epilogue_fwd_ref(const CallArgs& a, int row0, in
 // Per-tile forward epilogue, first pass over 64 columns: their maximum (four chains); the
 // accumulator values in r are replaced by the logits (-inf past the vocabulary).
 template <typename T, bool FULL, bool SCALE, bool BIAS>
-__device__ __forceinline__ float fwd_tile_max(uint32_t (&r)[64], int vbase, int V, float ls, const T* bias) {
+__device__ __forceinline__ float fwd_tile_max(uint32_t (&r)[FC], int vbase, int V, float ls, const T* bias) {
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int j = 0; j < 64; ++j) {
+  for (int j = 0; j < FC; ++j) {
     const int v = vbase + j;
     const float s = (FULL || v < V) ? logit_of<T, SCALE, BIAS>(r[j], v, ls, bias) : -INFINITY;
     r[j] = __float_as_uint(s);
@@ -688,10 +722,10 @@ __device__ __forceinline__ float fwd_tile_max(uint32_t (&r)[64], int vbase, int 
 // Per-tile forward epilogue, second pass over 64 columns: exp(s - max) (base 2, mxl =
 // max * log2 e) packed for the slab, and their sums (four partial sums).
 template <typename T, bool FULL, bool SCALE, bool BIAS>
-__device__ __forceinline__ void fwd_tile_exp(const uint32_t (&r)[64], int vbase, int V, float ls, const T* bias,
-                                             float mxl, float (&sum4)[4], uint32_t (&pk)[32]) {
+__device__ __forceinline__ void fwd_tile_exp(const uint32_t (&r)[FC], int vbase, int V, float ls, const T* bias,
+                                             float mxl, float (&sum4)[4], uint32_t (&pk)[FC / 2]) {
 #pragma unroll
-  for (int j = 0; j < 64; j += 2) {
+  for (int j = 0; j < FC; j += 2) {
     const int v = vbase + j;
     float e0 = 0.0f, e1 = 0.0f;
     if (FULL || v < V) e0 = ex2_fast(fmaf(logit_of<T, SCALE, BIAS>(r[j], v, ls, bias), LOG2E, -mxl));
@@ -705,31 +739,25 @@ __device__ __forceinline__ void fwd_tile_exp(const uint32_t (&r)[64], int vbase,
 // row-reference window): a first pass over TMEM for the max / argmax / target logit, a
 // second for exp(s - max) into the slab.
 template <typename T, bool SCALE, bool BIAS>
-__device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int rows, int mrow, int n,
-                                             uint32_t taddr, int q, int lane) {
-  const int rr = mrow + q * 32 + lane;  // row within the chunk
-  const bool valid = rr < rows;
+__device__ __forceinline__ void epilogue_fwd(const CallArgs& a, const FwdRow& fr, int n, uint32_t taddr) {
+  const int rr = fr.rr;
+  const bool valid = fr.valid;
   const int v0 = n * VT;
   const int V = (int)a.V;
   const bool want_arg = a.targets != nullptr;
-  int toff = -1;
-  float thr = -INFINITY;
-  if (valid && want_arg) {
-    const int64_t tg = a.targets[a.w.idx[row0 + rr]];
-    if (tg >= v0 && tg < v0 + BN) toff = (int)(tg - v0);
-    thr = row_threshold(a, rr);
-  }
+  const float thr = fr.thr;
+  const int toff = (fr.tg >= v0 && fr.tg < v0 + BN) ? (int)(fr.tg - v0) : -1;
   const float ls = a.logit_scale;
   const T* bias = (const T*)a.bias;
   const bool full = v0 + BN <= V;
   float mx = -INFINITY, tl = 0.0f;
   int ai = v0;
 #pragma unroll 1
-  for (int c2 = 0; c2 < BN / 64; ++c2) {
-    uint32_t r[64];
-    tmem_ld64(taddr + c2 * 64, r);
-    const int vb = v0 + c2 * 64;
-    pick_target<T, SCALE, BIAS>(r, toff - c2 * 64, v0 + toff, ls, bias, tl);
+  for (int c2 = 0; c2 < BN / FC; ++c2) {
+    uint32_t r[FC];
+    tmem_ldn<FC>(taddr + c2 * FC, r);
+    const int vb = v0 + c2 * FC;
+    pick_target<T, SCALE, BIAS>(r, toff - c2 * FC, v0 + toff, ls, bias, tl);
     const float bm = full ? fwd_tile_max<T, true, SCALE, BIAS>(r, vb, V, ls, bias)
                           : fwd_tile_max<T, false, SCALE, BIAS>(r, vb, V, ls, bias);
     if (want_arg) argmax_update(r, vb, bm, thr, mx, ai);
@@ -739,14 +767,14 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
   float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   const float mxl = a.ref_mode ? 0.0f : mx * LOG2E;  // row-reference mode stores exp(s)
 #pragma unroll 1
-  for (int c2 = 0; c2 < BN / 64; ++c2) {
-    uint32_t r[64];
-    tmem_ld64(taddr + c2 * 64, r);
-    uint32_t pk[32];
-    const int vb = v0 + c2 * 64;
+  for (int c2 = 0; c2 < BN / FC; ++c2) {
+    uint32_t r[FC];
+    tmem_ldn<FC>(taddr + c2 * FC, r);
+    uint32_t pk[FC / 2];
+    const int vb = v0 + c2 * FC;
     if (full) fwd_tile_exp<T, true, SCALE, BIAS>(r, vb, V, ls, bias, mxl, sum4, pk);
     else fwd_tile_exp<T, false, SCALE, BIAS>(r, vb, V, ls, bias, mxl, sum4, pk);
-    store_slab64<T>(a, rr, vb, pk);
+    store_slab<T>(a, rr, vb, pk);
   }
   if (valid) {
     write_tile_stats(a, rr, n, mx, (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]), ai, thr, want_arg);
@@ -756,25 +784,23 @@ __device__ __forceinline__ void epilogue_fwd(const CallArgs& a, int row0, int ro
 
 // Dispatch of the forward epilogues on the logit scale and the bias (warp-uniform).
 template <typename T, bool SCALE, bool BIAS>
-__device__ __forceinline__ void epilogue_fwd_any3(const CallArgs& a, int row0, int rows, int mrow, int n,
-                                                  uint32_t taddr, int q, int lane) {
-  if (a.ref_mode) epilogue_fwd_ref<T, SCALE, BIAS>(a, row0, rows, mrow, n, taddr, q, lane);
-  else epilogue_fwd<T, SCALE, BIAS>(a, row0, rows, mrow, n, taddr, q, lane);
+__device__ __forceinline__ void epilogue_fwd_any3(const CallArgs& a, const FwdRow& fr, int n, uint32_t taddr) {
+  if (a.ref_mode) epilogue_fwd_ref<T, SCALE, BIAS>(a, fr, n, taddr);
+  else epilogue_fwd<T, SCALE, BIAS>(a, fr, n, taddr);
 }
 // GEN: 0 for launches with no bias and a logit scale of 1 (the cross-entropy op without
 // bias), 1 with a bias and a scale of 1, 2 with another scale (the distillation op at
 // T != 1). Each is a kernel build of its own, so that the common ones keep all their values
 // in registers.
 template <typename T, int GEN>
-__device__ __forceinline__ void epilogue_fwd_any(const CallArgs& a, int row0, int rows, int mrow, int n,
-                                                 uint32_t taddr, int q, int lane) {
+__device__ __forceinline__ void epilogue_fwd_any(const CallArgs& a, const FwdRow& fr, int n, uint32_t taddr) {
   if constexpr (GEN == 0) {
-    epilogue_fwd_any3<T, false, false>(a, row0, rows, mrow, n, taddr, q, lane);
+    epilogue_fwd_any3<T, false, false>(a, fr, n, taddr);
   } else if constexpr (GEN == 1) {
-    epilogue_fwd_any3<T, false, true>(a, row0, rows, mrow, n, taddr, q, lane);
+    epilogue_fwd_any3<T, false, true>(a, fr, n, taddr);
   } else {
-    if (a.bias != nullptr) epilogue_fwd_any3<T, true, true>(a, row0, rows, mrow, n, taddr, q, lane);
-    else epilogue_fwd_any3<T, true, false>(a, row0, rows, mrow, n, taddr, q, lane);
+    if (a.bias != nullptr) epilogue_fwd_any3<T, true, true>(a, fr, n, taddr);
+    else epilogue_fwd_any3<T, true, false>(a, fr, n, taddr);
   }
 }
 
@@ -1066,18 +1092,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (; items.next(tile, k0, k1, split); ++it) {
       const int as = it % NACC;
       const uint32_t aph = (uint32_t)(it / NACC) & 1u;
-      bool ok = wait_bounded(tfull_bar(as), aph, ab, true);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
       int m, n;
       tile_coords<MODE>(ts, tile, m, n);
       const int nsub = n * NB + j;  // this warp's 256-column sub-tile of the output
       const int mrow = m * 2 * BM + (int)rank * BM;
+      FwdRow fr;
+      if (MODE == FWD) fr = fwd_row(a, row0, rows, mrow, q, lane);  // loads overlap the wait
+      bool ok = wait_bounded(tfull_bar(as), aph, ab, true);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((as * NB + j) * BN);
       if (nsub < ts.nsub) {
         if (MODE == FWD)
-          epilogue_fwd_any<T, GEN>(a, row0, rows, mrow, nsub, taddr, q, lane);
+          epilogue_fwd_any<T, GEN>(a, fr, nsub, taddr);
         else if (MODE == DW && a.dW_dt != FLCE_F32)
           epilogue_reduce<NBUF, (NB == 2), T, half_bufs_of<NB>()>(a, &tmC, stg, mrow, nsub, (int)a.V, 0, taddr, q, lane, cb,
                                               nullptr, ovw, epi_it);
