@@ -126,17 +126,13 @@ class FusedLinearCrossEntropy(torch.autograd.Function):
                         flce.scale_by(dW, g)
                         if ctx.has_bias:
                             flce.scale_by(db, g)
-                    ctx.versions = tuple(t._version for t in (dX, dW, db))
                 else:
                     # a later backward through a retained graph: the buffers were handed
                     # out scaled by the first upstream gradient, and whoever holds them
                     # (torch.autograd.grad's result, a hook) must keep what they got, so
-                    # the new gradients are fresh tensors scaled by the ratio
-                    if tuple(t._version for t in (dX, dW, db)) != ctx.versions:
-                        raise RuntimeError(
-                            "fused_linear_cross_entropy: the gradients returned by the first "
-                            "backward were modified in place, so a second backward through the "
-                            "retained graph cannot be formed from them")
+                    # the new gradients are fresh tensors scaled by the ratio (if the handed
+                    # out buffers were modified in place since, autograd's own check on the
+                    # saved tensors raises before this backward runs)
                     if float(prev) == 0.0:
                         raise RuntimeError(
                             "fused_linear_cross_entropy: a second backward through a retained "

@@ -138,7 +138,8 @@ def test_autograd_grad_twice_keeps_the_first_result():
 def test_second_backward_after_a_zero_upstream_gradient_raises():
     """A first backward with upstream gradient 0 leaves nothing to rescale from: a second
     backward through the retained graph raises instead of returning inf/NaN gradients; so
-    does one after the first gradients were modified in place."""
+    does one after the first gradients were modified in place (autograd's version check on
+    the saved buffers)."""
     from linear_cross_entropy_logits_gb300.torch_ops import fused_linear_cross_entropy
     sp = I.spec("llama1b", BT=200, H=128, V=2000, w_std=0.2)
     inp = I.generate(sp, seed=34)
@@ -153,5 +154,5 @@ def test_second_backward_after_a_zero_upstream_gradient_raises():
     # dX comes back in X's dtype, so autograd hands out the op's own buffer (the fp32 dW
     # is cast to W's dtype on the way out, a copy)
     gx.mul_(3.0)
-    with pytest.raises(RuntimeError, match="modified in place"):
+    with pytest.raises(RuntimeError, match="modified by an inplace operation"):
         torch.autograd.grad(loss, (X, W), retain_graph=True)
