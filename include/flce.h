@@ -97,6 +97,8 @@ typedef enum flce_dtype { FLCE_F32 = 0, FLCE_BF16 = 1, FLCE_F16 = 2 } flce_dtype
 #define FLCE_FLAG_DEBUG_STALL 0x100u /* testing only: the tensor-core forward GEMM leaves
                                      one pipeline stage unfilled so that its bounded waits
                                      run out; the call must then report FLCE_ERR_TIMEOUT */
+#define FLCE_FLAG_DEBUG_STALL_BWD 0x200u /* testing only: the same in the merged dX + dW
+                                     launch (its first work item)                          */
 
 /* Stages of one call, in launch order, for the optional profiler (flce_profile_*). */
 typedef enum flce_stage {

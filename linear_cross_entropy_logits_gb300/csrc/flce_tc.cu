@@ -1179,7 +1179,12 @@ __device__ __forceinline__ BwdSpace bwd_space(const CallArgs& a, int rows, int n
   b.dx = tile_space<DX, 2>(a, rows);
   b.dw = tile_space<DW, 2>(a, rows);
   b.ntx = b.dx.mt * b.dx.nt;
+#if defined(FLCE_BWD_DX_SPLITS) && FLCE_BWD_DX_SPLITS > 0
+  static_assert(FLCE_BWD_DX_SPLITS <= DX_MAX_SPLITS, "two dX buffers take at most four splits");
+  b.S = FLCE_BWD_DX_SPLITS < b.dx.nkb ? FLCE_BWD_DX_SPLITS : b.dx.nkb;
+#else
   b.S = dx_splits(b.ntx, npairs, b.dx.nkb);
+#endif
   b.n_dx = b.S * b.ntx;
   b.n_items = b.n_dx + b.dw.mt * b.dw.nt;
   return b;
@@ -1326,6 +1331,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int half = (int)rank * BM;
       int slot = 0;
       uint32_t qph = 0;
+      const bool stall = (a.flags & FLCE_FLAG_DEBUG_STALL_BWD) && leader;
+      bool first = true;
       for (;;) {
         int g;
         if (leader) {
@@ -1353,7 +1360,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (leader) mbar_expect_tx(full_bar(s), 2 * SBYTES);
           const uint32_t adst = smem_u32(smem + s * SBYTES);
           const uint32_t bdst = adst + A_BYTES;
-          if (it.dw) {
+          if (stall && first && kb == it.k1 - 1) {
+            // testing only: this stage is armed but never filled
+          } else if (it.dw) {
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj)
               tma_load_2d(adst + jj * BOX_BYTES, &tmAw, fb, it.m * 2 * BM + half + jj * 64, kb * BK);
@@ -1379,6 +1388,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (kb < it.k1) break;
+        first = false;
       }
     }
   } else if (warp == 1) {

@@ -25,6 +25,7 @@ FLAG_NO_ROW_REF = 0x2
 FLAG_DW_OVERWRITE = 0x4
 FLAG_SEPARATE_BWD = 0x8
 FLAG_DEBUG_STALL = 0x100
+FLAG_DEBUG_STALL_BWD = 0x200
 EXPORTED = ("flce_workspace_size", "flce_chunk_rows", "flce_fwd_bwd", "flce_fwd_bwd_noalloc",
             "flce_get_status",
             "flce_profile_create", "flce_profile_reset", "flce_profile_destroy",

@@ -39,3 +39,26 @@ def test_stalled_pipeline_reports_timeout_and_context_survives(H):
     assert after["status_code"] == flce.FLCE_OK
     for k in ("loss", "lse", "pred", "dX", "dW"):
         assert torch.equal(before[k], after[k]), k
+
+
+def test_stalled_merged_backward_reports_timeout_and_context_survives():
+    """The same for the merged dX + dW launch (a 2304-row chunk takes it): a stage of its
+    first work item is armed but never filled, every role of both CTAs leaves the work
+    queue through its bounded waits, and the next call is normal."""
+    sp = I.spec("llama1b", BT=2304, H=256, V=4000, w_std=0.2, ignore="random", n_ignored=100)
+    inp = I.generate(sp, seed=31)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    assert flce.chunk_rows(sp["BT"], sp["H"], sp["V"], torch.bfloat16,
+                           flce.workspace_size(sp["BT"], sp["H"], sp["V"], torch.bfloat16, 0)) >= 2048
+
+    def call(**kw):
+        return flce.fwd_bwd(d["X"], d["W"], d["targets"], None, reduction="mean", **kw)
+
+    before = call()
+    assert before["status_code"] == flce.FLCE_OK
+    stalled = call(flags=flce.FLAG_DEBUG_STALL_BWD, wait_timeout_ms=200)
+    assert stalled["status_code"] == flce.FLCE_ERR_TIMEOUT
+    after = call()
+    assert after["status_code"] == flce.FLCE_OK
+    for k in ("loss", "lse", "pred", "dX", "dW"):
+        assert torch.equal(before[k], after[k]), k
