@@ -249,10 +249,12 @@ extern "C" int64_t flce_plan_describe(int64_t BT, int64_t H, int64_t V, int32_t 
     const bool wide_dw = R >= DW_WIDE_MIN_ROWS;
     const bool wide_fwd = H >= FWD_WIDE_MIN_H;
     add("  GEMMs (tcgen05, CTA pairs) per full chunk: forward %lld tiles of %s; dX %lld tiles of "
-        "256x512 (K = V, up to 4 K splits); dW %lld tiles of %s\n",
+        "256x512 (K = V, up to 4 K splits); dW %lld tiles of %s; %s\n",
         (long long)(wide_fwd ? mt * ((p.nvt + 1) / 2) : mt * p.nvt), wide_fwd ? "256x512" : "256x256",
         (long long)(mt * ((ht + 1) / 2)), (long long)(wide_dw ? vt * ((ht + 1) / 2) : vt * ht),
-        wide_dw ? "256x512" : "256x256");
+        wide_dw ? "256x512" : "256x256",
+        wide_dw ? "dX and dW in one launch over a work queue (calls with both gradients)"
+                : "dX and dW in two launches");
   }
   const int64_t n = (int64_t)t.size();
   if (out_len > 0) {

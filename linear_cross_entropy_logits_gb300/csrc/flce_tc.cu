@@ -15,6 +15,9 @@
 //   DW:  dW += cbar * G^T Xc (K = chunk rows), added into the destination by TMA
 //        reduce-add from the single CTA pair that owns each tile (one add per element per
 //        launch: deterministic).
+//   BWD: the DX and DW work of a chunk in one persistent launch (k_gemm_bwd): the pairs
+//        draw work items (dX items first, then dW tiles) from a device-wide queue, so that
+//        dW fills dX's last wave; results bit-identical to two launches.
 // The three products are the logits, grad_input and grad_weight GEMMs that the pages'
 // op runs in its forward ("Liger-Kernel PR #1554: skip ignore_index rows", Summary); dW is
 // accumulated straight into the caller's buffer with no [V,H] temporary ("Reduce FLCE

@@ -186,7 +186,12 @@ def test_plan_describe(lib):
     assert f"forward {((R + 255) // 256) * 251} tiles of 256x512" in txt  # H >= 4096: wide tile
     t2 = flce.describe_plan(BT, 2048, V, torch.bfloat16)
     assert "forward " in t2 and "tiles of 256x256;" in t2
-    assert "dW 4008 tiles of 256x512" in txt
+    assert "dW 4008 tiles of 256x512" in txt and "dX and dW in one launch" in txt
+    # chunks under 2048 rows: dW on 256x256 tiles, two launches
+    small_ws = flce.workspace_size(BT, H, V, torch.bfloat16, 1 << 29)
+    t3 = flce.describe_plan(BT, H, V, torch.bfloat16, small_ws)
+    assert flce.chunk_rows(BT, H, V, torch.bfloat16, small_ws) < 2048
+    assert "dX and dW in two launches" in t3 and "tiles of 256x256; dX and dW" in t3
     assert "workspace slab   at" in txt and str(R * 128256 * 2) in txt
     n = lib.flce_plan_describe(BT, H, V, 1, wb, None, 0)
     assert n == len(txt.encode())
