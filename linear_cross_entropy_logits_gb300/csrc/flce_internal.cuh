@@ -17,6 +17,7 @@ namespace flce {
 // produces one (max, sum-exp, argmax) triple per row and per VT columns.
 constexpr int VT = 256;
 constexpr int CHUNK_ALIGN = 128;   // row-chunk granularity (one tensor-core M tile)
+constexpr int RED_BLOCKS = 128;   // blocks of the final mean / sum reduction (a fixed split: deterministic)
 // Tile-shape thresholds of the tensor-core GEMMs (the reasons are at their use in
 // flce_tc.cu): the dW GEMM takes 256 x 512 pair tiles (and, with dX, the merged launch)
 // from chunks of this many rows on, the forward from this hidden size on.
@@ -49,6 +50,8 @@ struct Ctrl {
   float inv_n;    // 1/n_lab for mean (0 when n_lab == 0), 1 for sum
   int fb;         // row-reference mode: 1 when a row of the current chunk left the window
   int queue;      // work-item counter of the merged dX + dW launch (zeroed before it)
+  int red_done;   // blocks of the final reduction that wrote their partial sums (zeroed by compaction)
+  double red[RED_BLOCKS][3];  // per-block partial sums of loss, z-loss and accuracy
 };
 
 // Workspace layout for one call; every region is 256-byte aligned.

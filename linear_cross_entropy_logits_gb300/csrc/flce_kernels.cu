@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(1024) k_compact(const __grid_constant__ CallAr
     const int nch = n > 0 ? (int)cdiv64(n, a.R) : 0;
     c->n_lab = n;
     c->n_chunks = nch;
+    c->red_done = 0;
     c->r_eff = n > 0 ? (int)rup64(cdiv64(n, nch), CHUNK_ALIGN) : 0;
     float g = 1.0f;
     if (a.reduction != FLCE_NONE && a.grad_out != nullptr) g = a.grad_out[0];
@@ -416,13 +417,19 @@ __global__ void __launch_bounds__(256) k_scale_by(T* x, int64_t n, const float* 
 
 // ---------------------------------------------------------------------------------------
 // Final reductions (mean/sum) of loss, z-loss and accuracy over the labelled rows, in a
-// fixed order (deterministic).
+// fixed order (deterministic): block b adds rows [b*per, (b+1)*per) in float64, and the
+// last block to finish adds the RED_BLOCKS partial sums in block order. float64 arithmetic
+// is slow on this GPU, so one block alone would take tens of microseconds.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) k_reduce(const __grid_constant__ CallArgs a) {
-  __shared__ double red[3][32];
-  const int n = a.w.ctrl->n_lab;
+__global__ void __launch_bounds__(256) k_reduce(const __grid_constant__ CallArgs a) {
+  __shared__ double red[3][8];
+  __shared__ bool last;
+  Ctrl* c = a.w.ctrl;
+  const int n = c->n_lab;
+  const int per = (n + RED_BLOCKS - 1) / RED_BLOCKS;
+  const int i0 = blockIdx.x * per, i1 = min(n, i0 + per);
   double s0 = 0.0, s1 = 0.0, s2 = 0.0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
     s0 += a.w.rloss[i];
     s1 += a.w.rz[i];
     s2 += a.w.racc[i];
@@ -440,24 +447,38 @@ __global__ void __launch_bounds__(1024) k_reduce(const __grid_constant__ CallArg
     red[2][wid] = s2;
   }
   __syncthreads();
-  if (wid == 0) {
-    s0 = red[0][lane];
-    s1 = red[1][lane];
-    s2 = red[2][lane];
+  if (threadIdx.x == 0) {
+    double q[3] = {0.0, 0.0, 0.0};
+    for (int w = 0; w < 8; ++w)
+      for (int k = 0; k < 3; ++k) q[k] += red[k][w];
+    for (int k = 0; k < 3; ++k) c->red[blockIdx.x][k] = q[k];
+    __threadfence();
+    last = atomicAdd(&c->red_done, 1) == RED_BLOCKS - 1;
+  }
+  __syncthreads();
+  if (!last || wid != 0) return;
+  // the last block to finish adds the partial sums in block order
+  __threadfence();
+  s0 = s1 = s2 = 0.0;
+  for (int b = lane; b < RED_BLOCKS; b += 32) {
+    s0 += __ldcg(&c->red[b][0]);
+    s1 += __ldcg(&c->red[b][1]);
+    s2 += __ldcg(&c->red[b][2]);
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      s0 += __shfl_down_sync(0xffffffffu, s0, o);
-      s1 += __shfl_down_sync(0xffffffffu, s1, o);
-      s2 += __shfl_down_sync(0xffffffffu, s2, o);
-    }
-    if (lane == 0) {
-      double d = 1.0;
-      if (a.reduction == FLCE_MEAN) d = n > 0 ? (double)n : 0.0;
-      const double q0 = d > 0.0 ? s0 / d : 0.0, q1 = d > 0.0 ? s1 / d : 0.0, q2 = d > 0.0 ? s2 / d : 0.0;
-      a.loss[0] = (float)q0;
-      if (a.z_loss) a.z_loss[0] = (float)q1;
-      if (a.acc) a.acc[0] = (float)q2;
-    }
+  for (int o = 16; o > 0; o >>= 1) {
+    s0 += __shfl_down_sync(0xffffffffu, s0, o);
+    s1 += __shfl_down_sync(0xffffffffu, s1, o);
+    s2 += __shfl_down_sync(0xffffffffu, s2, o);
+  }
+  if (lane == 0) {
+    double d = 1.0;
+    if (a.reduction == FLCE_MEAN) d = n > 0 ? (double)n : 0.0;
+    const double q0 = d > 0.0 ? s0 / d : 0.0, q1 = d > 0.0 ? s1 / d : 0.0, q2 = d > 0.0 ? s2 / d : 0.0;
+    a.loss[0] = (float)q0;
+    if (a.z_loss) a.z_loss[0] = (float)q1;
+    if (a.acc) a.acc[0] = (float)q2;
+    c->red_done = 0;
   }
 }
 
@@ -773,7 +794,7 @@ cudaError_t launch_dx_store(const CallArgs& a, int chunk, cudaStream_t s) {
 
 cudaError_t launch_epilogue(const CallArgs& a, cudaStream_t s) {
   if (a.reduction == FLCE_NONE) return cudaSuccess;
-  k_reduce<<<1, 1024, 0, s>>>(a);
+  k_reduce<<<RED_BLOCKS, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
