@@ -11,7 +11,7 @@
 // exp slab); k_jsd_finalize (both lse, per-tile log offsets); k_jsd_rows (per row: the
 // divergence terms and sum_v Q g in a fixed order, then dloss/dz into the student slab in
 // place, both passes over a row while it is still in L2); then the same dX / dW GEMMs as
-// the cross-entropy op. Nothing of [BT, V] reaches HBM.
+// the cross-entropy op. The only [R, V] data in HBM are the two per-chunk exp slabs.
 #include <math.h>
 #include <string.h>
 
@@ -225,19 +225,51 @@ constexpr int RU = 4;
 // per SM): pass 1 reads the row of both slabs and sums the divergence terms and Q g (g =
 // dloss/dQ up to a constant) with a fixed-order block reduction, giving loss_i and
 // S_i = sum_v Q_v g_v; pass 2 reads the row again, while it is still in L2 (one row per SM
-// in flight, about 0.5 MB each at V = 128256), and writes dS over the student slab. DRAM
-// moves each slab row once plus the dS write. The slab's pad columns (v >= V) hold exact
+// in flight, about 0.5 MB each at V = 128256), and writes dS over the student slab; over
+// the first JR_XTILES tiles it reads only the student row and the log ratio pass 1 kept in
+// shared memory (no log in pass 2 there). DRAM moves each slab row once plus the dS write. The slab's pad columns (v >= V) hold exact
 // zeros, whose terms vanish and whose dS is zero, so no column test is needed.
 constexpr int JR_THREADS = 512;
 constexpr int JR_WARPS = JR_THREADS / 32;
+// Pass 1 also keeps the log ratio x = log2(Q / R) of the row's first JR_XTILES tiles in
+// shared memory (fp16, 200 KB), R = M (0 < beta < 1) or P (beta = 1); pass 2 then forms
+// dS there from Q and x alone, without the teacher row and without a log. x <= log2(1 /
+// (1 - beta)) for 0 < beta < 1, and |x| < 256 for beta = 1 (both logs are clamped), so
+// fp16 keeps it to 2^-11 relative, below the 2^-9 rounding of the stored e.
+constexpr int JR_XTILES = 400;
+
+// 8 values <-> one 16-byte shared-memory word of fp16
+__device__ __forceinline__ void xs_store(uint32_t addr, const float (&x)[8]) {
+  uint32_t h[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __half2 v = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+    h[k] = *(uint32_t*)&v;
+  }
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+               : "memory");
+}
+__device__ __forceinline__ void xs_load(uint32_t addr, float (&x)[8]) {
+  uint32_t h[4];
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(addr)
+               : "memory");
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 v = __half22float2(*(__half2*)&h[k]);
+    x[2 * k] = v.x;
+    x[2 * k + 1] = v.y;
+  }
+}
 
 template <typename T>
 __global__ void __launch_bounds__(JR_THREADS, 1) k_jsd_rows(const __grid_constant__ JsdArgs j, int chunk,
-                                                           int grads) {
+                                                           int grads, int xt) {
   int row0, rows;
   if (!chunk_bounds(j.s.w.ctrl, chunk, row0, rows)) return;
   __shared__ float red_t[JR_WARPS], red_g[JR_WARPS];
   __shared__ float row_S;
+  extern __shared__ __align__(16) uint8_t xs_raw[];  // xt tiles x 256 fp16 values
+  const uint32_t xs0 = (uint32_t)__cvta_generic_to_shared(xs_raw);
   const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
   const int rlim = grads ? (int)rup64(rows, 64) : rows;
   const int nvt = (int)j.s.nvt;
@@ -273,6 +305,7 @@ __global__ void __launch_bounds__(JR_THREADS, 1) k_jsd_rows(const __grid_constan
           Load8<T>::cvt(rt[u], et);
           const float qm = expf(lqo[u]), pm = expf(lpo[u]);
           const float lq2 = lqo[u] * LOG2E, lp2 = lpo[u] * LOG2E;
+          float xr[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const float Q = es[k] * qm, P = et[k] * pm;
@@ -280,16 +313,20 @@ __global__ void __launch_bounds__(JR_THREADS, 1) k_jsd_rows(const __grid_constan
             if (beta == 0.0f) {
               tm = fmaf(P, lP - lQ, tm);
             } else if (beta == 1.0f) {
-              const float x = Q * (lQ - lP);
+              xr[k] = lQ - lP;
+              const float x = Q * xr[k];
               tm += x;
               g += x;
             } else {
               const float lM = lg2_clamped(fmaf(beta, P, omb * Q));
-              const float qpart = omb * Q * (lQ - lM);
+              xr[k] = lQ - lM;
+              const float qpart = omb * Q * xr[k];
               tm = fmaf(beta * P, lP - lM, tm + qpart);
               g += qpart;
             }
           }
+          const int t = t0 + u * JR_WARPS;
+          if (t < xt) xs_store(xs0 + (uint32_t)(t * VT + lane * 8) * 2u, xr);
         }
       }
 #pragma unroll
@@ -335,9 +372,11 @@ __global__ void __launch_bounds__(JR_THREADS, 1) k_jsd_rows(const __grid_constan
           for (int u = 0; u < RUJ; ++u) {
             const int t = t0 + u * JR_WARPS < nvt ? t0 + u * JR_WARPS : t0;
             lqo[u] = soff[t];
-            lpo[u] = toff[t];
             rs[u] = Load8<T>::load(s_row + (int64_t)t * VT + lane * 8);
-            rt[u] = Load8<T>::load(t_row + (int64_t)t * VT + lane * 8);
+            if (t >= xt) {
+              lpo[u] = toff[t];
+              rt[u] = Load8<T>::load(t_row + (int64_t)t * VT + lane * 8);
+            }
           }
         }
 #pragma unroll
@@ -345,7 +384,14 @@ __global__ void __launch_bounds__(JR_THREADS, 1) k_jsd_rows(const __grid_constan
           const int t = t0 + u * JR_WARPS;
           if (t >= nvt) continue;
           float out[8];
-          if (live) {
+          if (live && t < xt) {
+            float es[8], xr[8];
+            Load8<T>::cvt(rs[u], es);
+            xs_load(xs0 + (uint32_t)(t * VT + lane * 8) * 2u, xr);
+            const float qm = expf(lqo[u]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) out[k] = f * ((es[k] * qm) * fmaf(cg, xr[k], -S));
+          } else if (live) {
             float es[8], et[8];
             Load8<T>::cvt(rs[u], es);
             Load8<T>::cvt(rt[u], et);
@@ -381,7 +427,15 @@ template <typename T>
 cudaError_t launch_jsd_rows(const JsdArgs& j, int chunk, cudaStream_t s, bool grads) {
   int g = num_sms();
   if (g > j.s.R) g = (int)j.s.R;
-  k_jsd_rows<T><<<(unsigned)g, JR_THREADS, 0, s>>>(j, chunk, grads ? 1 : 0);
+  // x is kept for 16-bit slabs with gradients and beta > 0 (beta = 0 needs P, not a log)
+  int xt = 0;
+  if (grads && sizeof(T) == 2 && j.beta > 0.0f) xt = j.s.nvt < JR_XTILES ? (int)j.s.nvt : JR_XTILES;
+  const size_t smem = (size_t)xt * VT * 2;
+  if (smem > 0) {  // per device and cheap: set on every launch
+    const cudaError_t e = cudaFuncSetAttribute(k_jsd_rows<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k_jsd_rows<T><<<(unsigned)g, JR_THREADS, smem, s>>>(j, chunk, grads ? 1 : 0, xt);
   return cudaGetLastError();
 }
 
