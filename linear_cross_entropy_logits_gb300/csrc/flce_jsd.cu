@@ -219,7 +219,12 @@ template <> struct Load8<float> {
 
 // Eight slab columns per lane; a warp covers one 256-column tile, and each warp keeps
 // RU tiles' loads in flight so that enough bytes are outstanding to cover DRAM latency.
-constexpr int RU = 4;
+// 24 warps x 2 tiles (768 threads, 80 registers) ran faster than 16 x 4, 32 x 1 or 8 x 8:
+// the kernel needs both the bytes in flight and the warps to hide its arithmetic.
+#ifndef FLCE_JR_RU
+#define FLCE_JR_RU 2
+#endif
+constexpr int RU = FLCE_JR_RU;
 
 // Both elementwise passes in one kernel, one row at a time per CTA (persistent, one CTA
 // per SM): pass 1 reads the row of both slabs and sums the divergence terms and Q g (g =
@@ -229,7 +234,10 @@ constexpr int RU = 4;
 // the first JR_XTILES tiles it reads only the student row and the log ratio pass 1 kept in
 // shared memory (no log in pass 2 there). DRAM moves each slab row once plus the dS write. The slab's pad columns (v >= V) hold exact
 // zeros, whose terms vanish and whose dS is zero, so no column test is needed.
-constexpr int JR_THREADS = 512;
+#ifndef FLCE_JR_THREADS
+#define FLCE_JR_THREADS 768
+#endif
+constexpr int JR_THREADS = FLCE_JR_THREADS;
 constexpr int JR_WARPS = JR_THREADS / 32;
 // Pass 1 also keeps the log ratio x = log2(Q / R) of the row's first JR_XTILES tiles in
 // shared memory (fp16, 200 KB), R = M (0 < beta < 1) or P (beta = 1); pass 2 then forms
@@ -275,7 +283,7 @@ __global__ void __launch_bounds__(JR_THREADS, 1) k_jsd_rows(const __grid_constan
   const int nvt = (int)j.s.nvt;
   const float beta = j.beta, omb = 1.0f - beta;
   const float cg = (beta == 1.0f ? 1.0f : omb) * LN2;
-  constexpr int RUJ = sizeof(T) == 4 ? 2 : RU;  // tiles in flight per warp (fp32 rows are twice the bytes)
+  constexpr int RUJ = sizeof(T) == 4 ? (RU > 1 ? RU / 2 : 1) : RU;  // tiles in flight per warp (fp32 rows are twice the bytes)
   for (int r = blockIdx.x; r < rlim; r += gridDim.x) {
     const bool live = r < rows;
     const T* s_row = (const T*)j.s.w.slab + (int64_t)r * j.s.Vp;
@@ -305,30 +313,32 @@ __global__ void __launch_bounds__(JR_THREADS, 1) k_jsd_rows(const __grid_constan
           Load8<T>::cvt(rt[u], et);
           const float qm = expf(lqo[u]), pm = expf(lpo[u]);
           const float lq2 = lqo[u] * LOG2E, lp2 = lpo[u] * LOG2E;
+          // 0 < beta < 1: (1 - beta) Q and beta P straight from the stored e
+          const float qmo = omb * qm, pmb = beta * pm;
           float xr[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const float Q = es[k] * qm, P = et[k] * pm;
             const float lQ = lg2_clamped(es[k]) + lq2, lP = lg2_clamped(et[k]) + lp2;
             if (beta == 0.0f) {
-              tm = fmaf(P, lP - lQ, tm);
+              tm = fmaf(et[k] * pm, lP - lQ, tm);
             } else if (beta == 1.0f) {
               xr[k] = lQ - lP;
-              const float x = Q * xr[k];
+              const float x = (es[k] * qm) * xr[k];
               tm += x;
               g += x;
             } else {
-              const float lM = lg2_clamped(fmaf(beta, P, omb * Q));
+              const float Qo = es[k] * qmo, Pb = et[k] * pmb;
+              const float lM = lg2_clamped(Qo + Pb);
               xr[k] = lQ - lM;
-              const float qpart = omb * Q * xr[k];
-              tm = fmaf(beta * P, lP - lM, tm + qpart);
-              g += qpart;
+              g = fmaf(Qo, xr[k], g);       // (1 - beta) Q log(Q / M)
+              tm = fmaf(Pb, lP - lM, tm);   // beta P log(P / M); the Q part is added below
             }
           }
           const int t = t0 + u * JR_WARPS;
           if (t < xt) xs_store(xs0 + (uint32_t)(t * VT + lane * 8) * 2u, xr);
         }
       }
+      if (beta != 0.0f && beta != 1.0f) tm += g;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         tm += __shfl_xor_sync(0xffffffffu, tm, o);
@@ -406,7 +416,7 @@ __global__ void __launch_bounds__(JR_THREADS, 1) k_jsd_rows(const __grid_constan
               } else {
                 const float lQ = lg2_clamped(es[k]) + lq2;
                 const float lR = beta == 1.0f ? lg2_clamped(et[k]) + lp2
-                                              : lg2_clamped(fmaf(beta, P, omb * Q));
+                                              : lg2_clamped(es[k] * (omb * qm) + et[k] * (beta * pm));
                 dz = Q * fmaf(cg, lQ - lR, -S);
               }
               out[k] = f * dz;
