@@ -349,3 +349,26 @@ def test_tiny_shapes_fp32(BT, H, V):
     sp = I.spec("tiny_fp32", BT=BT, H=H, V=V, ignore="none" if BT < 10 else "random", n_ignored=5)
     inp = I.generate(sp, seed=28 + BT)
     compare_full(run_gpu(inp, sp), run_oracle(inp, sp), inp, sp)
+
+
+@pytest.mark.parametrize("n_lab", [1, 127, 128, 129, 1000, 20000])
+def test_mean_and_sum_equal_the_sum_of_per_token_values(n_lab):
+    """The mean / sum outputs are the float64 sum of the per-token loss, z-loss and
+    accuracy that reduction "none" returns for the same rows (the rows' values do not depend
+    on the reduction), rounded once to fp32: checked at labelled counts around the final
+    reduction's 128-block split (one row, one row per block, a ragged last block, many rows
+    per block)."""
+    BT = n_lab + 7
+    base = dict(BT=BT, H=64, V=500, w_std=0.3, z=1e-3, ignore="random", n_ignored=7, want_dW=False)
+    none = run_gpu(I.generate(I.spec("llama1b", reduction="none", **base), seed=11),
+                   I.spec("llama1b", reduction="none", **base))
+    lab = I.generate(I.spec("llama1b", reduction="none", **base), seed=11)["targets"].numpy() != I.IGNORE_INDEX
+    assert int(lab.sum()) == n_lab
+    for red in ("sum", "mean"):
+        sp = I.spec("llama1b", reduction=red, **base)
+        g = run_gpu(I.generate(sp, seed=11), sp)
+        d = 1.0 if red == "sum" else float(n_lab)
+        for k in ("loss", "z_loss", "acc"):
+            want = np.float32(np.sum(none[k][lab].astype(np.float64)) / d)
+            got = np.float32(g[k][0])
+            assert abs(got - want) <= 2 * np.spacing(np.abs(want)) + 1e-30, (red, k, got, want)
