@@ -44,6 +44,7 @@ WORKLOAD_TITLES = {
     "llama8b": "Llama-3.1-8B-shaped head",
     "large_vocab": "large-vocab long-context head",
     "frozen_head": "frozen-head (LoRA) variant",
+    "llama2_7b": "32000-token head (H=4096)",
 }
 
 
@@ -55,7 +56,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--op", default="flce", choices=["flce", "jsd"])
     p.add_argument("--workload", default="llama8b", choices=list(I.WORKLOADS))
-    p.add_argument("--dtype", default=None, choices=["bf16", "f16"],
+    p.add_argument("--dtype", default=None, choices=["bf16", "f16", "f32"],
                    help="override the workload's input dtype")
     p.add_argument("--dw-dtype", default="f32", choices=["f32", "same"],
                    help="dW / dbias accumulation dtype: fp32, or the input dtype")
@@ -329,14 +330,18 @@ def cpu_threads():
     return os.cpu_count()
 
 
-def traffic_record():
-    """ncu DRAM bytes of the dominant kernel, if taken with the current kernel sources."""
+def traffic_record(run):
+    """ncu DRAM bytes per GEMM launch, if taken with the current kernel sources on the
+    configuration of this run (the record's "config": workload, BT, labelled rows, input and
+    dW dtypes, chunk rows); None otherwise."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
     if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    if any(run.get(k) != v for k, v in rec.get("config", {"unmatched": True}).items()):
         return None
     return rec
 
@@ -587,7 +592,8 @@ def run_ours(args):
     per_step_dom_ms = dom_ms / args.steps
     stage_summary = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                      for k, v in stages.items() if v[1] > 0}
-    rec = traffic_record()
+    rec = traffic_record({"workload": args.workload, "BT": BT, "n_labelled": n_lab, "dtype": sp["dtype"],
+                          "dW_dtype": "f32" if args.dw_dtype == "f32" else sp["dtype"], "chunk_rows": R})
     if args.api == "torch":
         # the autograd op takes no profiler: whole-step numbers only
         roof = None

@@ -483,116 +483,230 @@ __global__ void __launch_bounds__(256) k_reduce(const __grid_constant__ CallArgs
 }
 
 // ---------------------------------------------------------------------------------------
-// SIMT forward: a 16-row x 256-column logit tile per block, fp32 FMA over H, then the
-// same per-tile statistics and stored exp(s - tile max) as the tensor-core forward.
+// SIMT GEMM core (fp32 FMA; the fp32-input path, and 16-bit inputs whose H is not a
+// multiple of 8 or that force it): one block computes a (16 TM) x (16 TN) tile of
+// C = A B over K. 256 threads as 16 x 16; thread (ty, tx) keeps TM x TN accumulators for
+// rows ty*4 + 64*(i/4) + i%4 and columns tx*4 + 64*(j/4) + j%4, so that its shared-memory
+// reads are float4 and a warp's reads hit distinct banks (or broadcast). The operands
+// pass through shared memory SK = 16 k at a time, in two buffers: the next step's elements
+// are loaded into registers while the current step is multiplied.
+// KC: the operand's K index is the contiguous one (element (e, k) at p[e * ld + k]);
+// otherwise its row index e is (p[k * ld + e]). Elements outside the extents read as 0.
+// ---------------------------------------------------------------------------------------
+constexpr int SK = 16;
+
+template <typename T, int E, bool KC>
+struct SimtOperand {
+  static constexpr int PER = E * SK / 256;  // elements per thread per step
+  static constexpr int PITCH = E + 4;       // shared-memory row pitch (floats, 16-byte rows)
+  float r[PER];
+  __device__ __forceinline__ void load(const T* p, int64_t ld, int64_t e0, int64_t ext, int64_t k0, int64_t K,
+                                       int tid) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      int e, k;
+      if (KC) {
+        k = tid % SK;
+        e = tid / SK + (256 / SK) * i;
+      } else {
+        e = tid % E;
+        k = tid / E + (256 / E) * i;
+      }
+      const int64_t ge = e0 + e, gk = k0 + k;
+      r[i] = (ge < ext && gk < K) ? to_f<T>(KC ? p[ge * ld + gk] : p[gk * ld + ge]) : 0.0f;
+    }
+  }
+  __device__ __forceinline__ void store(float* s, int tid) const {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      int e, k;
+      if (KC) {
+        k = tid % SK;
+        e = tid / SK + (256 / SK) * i;
+      } else {
+        e = tid % E;
+        k = tid / E + (256 / E) * i;
+      }
+      s[k * PITCH + e] = r[i];
+    }
+  }
+};
+
+template <int TM, int TN>
+__device__ __forceinline__ void simt_step(const float* as, const float* bs, float (&acc)[TM][TN], int ty, int tx) {
+  constexpr int PA = 16 * TM + 4, PB = 16 * TN + 4;
+#pragma unroll
+  for (int k = 0; k < SK; ++k) {
+    float av[TM], bv[TN];
+#pragma unroll
+    for (int g = 0; g < TM / 4; ++g) {
+      const float4 v = *(const float4*)&as[k * PA + g * 64 + ty * 4];
+      av[4 * g] = v.x;
+      av[4 * g + 1] = v.y;
+      av[4 * g + 2] = v.z;
+      av[4 * g + 3] = v.w;
+    }
+#pragma unroll
+    for (int g = 0; g < TN / 4; ++g) {
+      const float4 v = *(const float4*)&bs[k * PB + g * 64 + tx * 4];
+      bv[4 * g] = v.x;
+      bv[4 * g + 1] = v.y;
+      bv[4 * g + 2] = v.z;
+      bv[4 * g + 3] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+  }
+}
+
+// Shared memory of one block tile: two buffers of each operand's 16-k slice.
+template <int TM, int TN>
+__host__ __device__ constexpr int simt_smem_floats() {
+  return 2 * SK * ((16 * TM + 4) + (16 * TN + 4));
+}
+
+// acc = A[m0 : m0 + 16 TM, 0 : K] B[0 : K, n0 : n0 + 16 TN] (rows past M / columns past N
+// and k past K count as zero). Every thread of the block calls it.
+template <typename T, int TM, int TN, bool AKC, bool BKC>
+__device__ __forceinline__ void simt_gemm_tile(const T* A, int64_t lda, int64_t m0, int64_t M, const T* B,
+                                               int64_t ldb, int64_t n0, int64_t N, int64_t K, float* smem,
+                                               float (&acc)[TM][TN]) {
+  constexpr int BM = 16 * TM, BN = 16 * TN;
+  constexpr int SA = SK * (BM + 4), SB = SK * (BN + 4);
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+  const int64_t nk = (K + SK - 1) / SK;
+  if (nk == 0) return;
+  SimtOperand<T, BM, AKC> oa;
+  SimtOperand<T, BN, BKC> ob;
+  oa.load(A, lda, m0, M, 0, K, tid);
+  ob.load(B, ldb, n0, N, 0, K, tid);
+  oa.store(smem, tid);
+  ob.store(smem + 2 * SA, tid);
+  __syncthreads();
+  for (int64_t kt = 0; kt < nk; ++kt) {
+    const int cur = (int)(kt & 1), nxt = cur ^ 1;
+    const bool more = kt + 1 < nk;
+    if (more) {
+      oa.load(A, lda, m0, M, (kt + 1) * SK, K, tid);
+      ob.load(B, ldb, n0, N, (kt + 1) * SK, K, tid);
+    }
+    simt_step<TM, TN>(smem + cur * SA, smem + 2 * SA + cur * SB, acc, ty, tx);
+    if (more) {
+      oa.store(smem + nxt * SA, tid);
+      ob.store(smem + 2 * SA + nxt * SB, tid);
+    }
+    __syncthreads();
+  }
+}
+
+// Row / column of accumulator (i, j) of thread (ty, tx) within the block tile.
+__device__ __forceinline__ int simt_row(int i, int ty) { return (i >> 2) * 64 + ty * 4 + (i & 3); }
+__device__ __forceinline__ int simt_col(int j, int tx) { return (j >> 2) * 64 + tx * 4 + (j & 3); }
+
+// ---------------------------------------------------------------------------------------
+// SIMT forward: a 64-row x 256-column logit tile per block (one vocabulary tile), then the
+// same per-tile statistics and stored exp(s - tile max) as the tensor-core forward. The
+// tile is staged in shared memory 32 rows at a time for the row statistics.
 // ---------------------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(256) k_fwd_simt(const __grid_constant__ CallArgs a, int chunk) {
+__global__ void __launch_bounds__(256, 2) k_fwd_simt(const __grid_constant__ CallArgs a, int chunk) {
   int row0, rows;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
   const int mb = blockIdx.x;
-  if (mb * 16 >= rows) return;
+  if (mb * 64 >= rows) return;
   const int t = blockIdx.y;
-  __shared__ float As[16][33];
-  __shared__ float Bs[VT * 33];
-  const int tid = threadIdx.x;
-  const T* xc = (const T*)a.w.xc;
-  const T* W = (const T*)a.W;
-  const int64_t H = a.H, V = a.V;
-  float acc[16];
+  __shared__ __align__(16) float smem[simt_smem_floats<4, 16>()];
+  static_assert(simt_smem_floats<4, 16>() >= 32 * 257, "row staging");
+  float acc[4][16];
+  simt_gemm_tile<T, 4, 16, true, true>((const T*)a.w.xc, a.Hp, (int64_t)mb * 64, rows, (const T*)a.W, a.H,
+                                       (int64_t)t * VT, a.V, a.H, smem, acc);
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int64_t V = a.V;
+  float bj[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-  for (int64_t k0 = 0; k0 < H; k0 += 32) {
-    for (int e = tid; e < 16 * 32; e += 256) {
-      const int rr = e >> 5, kk = e & 31;
-      const int64_t gk = k0 + kk;
-      As[rr][kk] = gk < H ? to_f<T>(xc[(int64_t)(mb * 16 + rr) * a.Hp + gk]) : 0.0f;
-    }
-    for (int e = tid; e < VT * 32; e += 256) {
-      const int nn = e >> 5, kk = e & 31;
-      const int64_t v = (int64_t)t * VT + nn, gk = k0 + kk;
-      Bs[nn * 33 + kk] = (v < V && gk < H) ? to_f<T>(W[v * H + gk]) : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < 32; ++kk) {
-      const float b = Bs[tid * 33 + kk];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] = fmaf(As[i][kk], b, acc[i]);
-    }
-    __syncthreads();
+  for (int j = 0; j < 16; ++j) {
+    const int64_t v = (int64_t)t * VT + simt_col(j, tx);
+    bj[j] = (a.bias != nullptr && v < V) ? to_f<T>(((const T*)a.bias)[v]) : 0.0f;
   }
-  // stage the tile (with bias) in shared memory: Ss[i][j] at Bs[i * 257 + j]
-  float* Ss = Bs;
-  {
-    const int64_t v = (int64_t)t * VT + tid;
-    float b = 0.0f;
-    if (a.bias != nullptr && v < V) b = to_f<T>(((const T*)a.bias)[v]);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) Ss[i * 257 + tid] = fmaf(acc[i], a.logit_scale, b);
-  }
-  __syncthreads();
+  float* Ss = smem;  // Ss[r * 257 + c], 32 rows
   const int lane = tid & 31, warp = tid >> 5;
   T* slab = (T*)a.w.slab;
-  for (int i = warp; i < 16; i += 8) {
-    const int rr = mb * 16 + i;
-    if (rr >= rows) continue;
-    const int64_t tg = a.targets ? a.targets[a.w.idx[row0 + rr]] : -1;
-    float mx = -INFINITY;
-    int ai = t * VT;
-    float tl = 0.0f;
-    bool ht = false;
-    for (int j = lane; j < VT; j += 32) {
-      const int64_t v = (int64_t)t * VT + j;
-      if (v < V) {
-        const float s = Ss[i * 257 + j];
-        if (s > mx) {
-          mx = s;
-          ai = (int)v;
-        }
-        if (v == tg) {
-          tl = s;
-          ht = true;
+  for (int h = 0; h < 2; ++h) {
+    if ((ty >> 3) == h) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          Ss[(ty * 4 + i - 32 * h) * 257 + simt_col(j, tx)] = fmaf(acc[i][j], a.logit_scale, bj[j]);
+    }
+    __syncthreads();
+    for (int il = warp; il < 32; il += 8) {
+      const int rr = mb * 64 + 32 * h + il;
+      if (rr >= rows) continue;
+      const int64_t tg = a.targets ? a.targets[a.w.idx[row0 + rr]] : -1;
+      float mx = -INFINITY;
+      int ai = t * VT;
+      float tl = 0.0f;
+      bool ht = false;
+      for (int j = lane; j < VT; j += 32) {
+        const int64_t v = (int64_t)t * VT + j;
+        if (v < V) {
+          const float s = Ss[il * 257 + j];
+          if (s > mx) {
+            mx = s;
+            ai = (int)v;
+          }
+          if (v == tg) {
+            tl = s;
+            ht = true;
+          }
         }
       }
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float om = __shfl_xor_sync(0xffffffffu, mx, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, ai, o);
-      if (om > mx || (om == mx && oi < ai)) {
-        mx = om;
-        ai = oi;
+      for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, ai, o);
+        if (om > mx || (om == mx && oi < ai)) {
+          mx = om;
+          ai = oi;
+        }
+      }
+      float sum = 0.0f;
+      for (int j = lane; j < VT; j += 32) {
+        const int64_t v = (int64_t)t * VT + j;
+        const float e = v < V ? expf(Ss[il * 257 + j] - mx) : 0.0f;
+        sum += e;
+        slab[(int64_t)rr * a.Vp + v] = from_f<T>(e);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      const unsigned hb = __ballot_sync(0xffffffffu, ht);
+      if (hb) tl = __shfl_sync(0xffffffffu, tl, __ffs(hb) - 1);
+      if (lane == 0) {
+        const int64_t o = (int64_t)rr * a.nvt + t;
+        a.w.stm[o] = mx;
+        a.w.sts[o] = sum;
+        a.w.sti[o] = ai;
+        if (hb) a.w.tgt[rr] = tl;
       }
     }
-    float sum = 0.0f;
-    for (int j = lane; j < VT; j += 32) {
-      const int64_t v = (int64_t)t * VT + j;
-      const float e = v < V ? expf(Ss[i * 257 + j] - mx) : 0.0f;
-      sum += e;
-      slab[(int64_t)rr * a.Vp + v] = from_f<T>(e);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const unsigned hb = __ballot_sync(0xffffffffu, ht);
-    if (hb) tl = __shfl_sync(0xffffffffu, tl, __ffs(hb) - 1);
-    if (lane == 0) {
-      const int64_t o = (int64_t)rr * a.nvt + t;
-      a.w.stm[o] = mx;
-      a.w.sts[o] = sum;
-      a.w.sti[o] = ai;
-      if (hb) a.w.tgt[rr] = tl;
-    }
+    __syncthreads();  // the staging rows are rewritten by the next half
   }
 }
 
 // ---------------------------------------------------------------------------------------
-// SIMT GEMMs of the backward, 64x64 output tiles, fp32 FMA.
+// SIMT GEMMs of the backward, 128x128 output tiles on the core above.
 //   MODE 0 (dX): dX[idx[r]] = cbar * sum_v G[r, v] W[v, :]        (M = rows, K = V)
 //   MODE 1 (dW): dW[v]     += cbar * sum_r G[r, v] Xc[r, :]       (M = V, K = rows)
 // ---------------------------------------------------------------------------------------
 template <typename T, int MODE>
-__global__ void __launch_bounds__(256) k_gemm_simt(const __grid_constant__ CallArgs a, int chunk) {
+__global__ void __launch_bounds__(256, 2) k_gemm_simt(const __grid_constant__ CallArgs a, int chunk) {
   int row0, rows;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
   // dW overwrite: the first chunk stores, later chunks accumulate
@@ -600,62 +714,24 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const __grid_constant__ CallA
   const int64_t M = MODE == 0 ? rows : a.V;
   const int64_t N = a.H;
   const int64_t K = MODE == 0 ? a.V : rows;
-  const int64_t m0 = (int64_t)blockIdx.y * 64, n0 = (int64_t)blockIdx.x * 64;
+  const int64_t m0 = (int64_t)blockIdx.y * 128, n0 = (int64_t)blockIdx.x * 128;
   if (m0 >= M) return;
-  __shared__ float As[16][68];
-  __shared__ float Bs[16][68];
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  __shared__ __align__(16) float smem[simt_smem_floats<8, 8>()];
+  float acc[8][8];
   const T* G = (const T*)a.w.slab;
-  const T* Bsrc = MODE == 0 ? (const T*)a.W : (const T*)a.w.xc;
-  const int64_t ldb = MODE == 0 ? a.H : a.Hp;
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-  for (int64_t k0 = 0; k0 < K; k0 += 16) {
-    for (int e = tid; e < 1024; e += 256) {
-      int mm, kk;
-      if (MODE == 0) {
-        mm = e >> 4;
-        kk = e & 15;
-      } else {
-        kk = e >> 6;
-        mm = e & 63;
-      }
-      const int64_t gm = m0 + mm, gk = k0 + kk;
-      float v = 0.0f;
-      if (gm < M && gk < K) v = MODE == 0 ? to_f<T>(G[gm * a.Vp + gk]) : to_f<T>(G[gk * a.Vp + gm]);
-      As[kk][mm] = v;
-    }
-    for (int e = tid; e < 1024; e += 256) {
-      const int kk = e >> 6, nn = e & 63;
-      const int64_t gk = k0 + kk, gn = n0 + nn;
-      Bs[kk][nn] = (gk < K && gn < N) ? to_f<T>(Bsrc[gk * ldb + gn]) : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      float av[4], bv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
+  if constexpr (MODE == 0)
+    simt_gemm_tile<T, 8, 8, true, false>(G, a.Vp, m0, M, (const T*)a.W, a.H, n0, N, K, smem, acc);
+  else
+    simt_gemm_tile<T, 8, 8, false, false>(G, a.Vp, m0, M, (const T*)a.w.xc, a.Hp, n0, N, K, smem, acc);
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const float cb = a.w.ctrl->cbar;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t m = m0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int64_t m = m0 + simt_row(i, ty);
     if (m >= M) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t n = n0 + tx * 4 + j;
+    for (int j = 0; j < 8; ++j) {
+      const int64_t n = n0 + simt_col(j, tx);
       if (n >= N) continue;
       if (MODE == 0) {
         const int64_t orow = a.w.idx[row0 + m];
@@ -756,7 +832,7 @@ cudaError_t launch_gpass(const CallArgs& a, int chunk, cudaStream_t s) {
 }
 
 cudaError_t launch_fwd_simt(const CallArgs& a, int chunk, cudaStream_t s) {
-  dim3 grid((unsigned)cdiv64(a.R, 16), (unsigned)a.nvt);
+  dim3 grid((unsigned)cdiv64(a.R, 64), (unsigned)a.nvt);
   switch (a.dt) {
     case FLCE_BF16: k_fwd_simt<__nv_bfloat16><<<grid, 256, 0, s>>>(a, chunk); break;
     case FLCE_F16: k_fwd_simt<__half><<<grid, 256, 0, s>>>(a, chunk); break;
@@ -766,7 +842,7 @@ cudaError_t launch_fwd_simt(const CallArgs& a, int chunk, cudaStream_t s) {
 }
 
 cudaError_t launch_dx_simt(const CallArgs& a, int chunk, cudaStream_t s) {
-  dim3 grid((unsigned)cdiv64(a.H, 64), (unsigned)cdiv64(a.R, 64));
+  dim3 grid((unsigned)cdiv64(a.H, 128), (unsigned)cdiv64(a.R, 128));
   switch (a.dt) {
     case FLCE_BF16: k_gemm_simt<__nv_bfloat16, 0><<<grid, 256, 0, s>>>(a, chunk); break;
     case FLCE_F16: k_gemm_simt<__half, 0><<<grid, 256, 0, s>>>(a, chunk); break;
@@ -776,7 +852,7 @@ cudaError_t launch_dx_simt(const CallArgs& a, int chunk, cudaStream_t s) {
 }
 
 cudaError_t launch_dw_simt(const CallArgs& a, int chunk, cudaStream_t s) {
-  dim3 grid((unsigned)cdiv64(a.H, 64), (unsigned)cdiv64(a.V, 64));
+  dim3 grid((unsigned)cdiv64(a.H, 128), (unsigned)cdiv64(a.V, 128));
   switch (a.dt) {
     case FLCE_BF16: k_gemm_simt<__nv_bfloat16, 1><<<grid, 256, 0, s>>>(a, chunk); break;
     case FLCE_F16: k_gemm_simt<__half, 1><<<grid, 256, 0, s>>>(a, chunk); break;

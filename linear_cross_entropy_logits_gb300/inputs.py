@@ -21,6 +21,9 @@ Workloads (shapes after the pages' model heads):
                     k maps to token k-1), sum, dX and fp32 dW.
   * ``frozen_head`` BT=16384, H=4096, V=151936, bf16, bias~N(0,0.01^2), 8192 rows ignored at
                     random, none with a per-token upstream gradient ~U(0.5,1.5), dX only.
+  * ``llama2_7b``   a 32000-token head: BT=16384, H=4096, V=32000, bf16 (or fp32 / fp16 by
+                    override), W~N(0,0.02^2), all rows labelled, uniform targets, mean, dX and
+                    fp32 dW.
   * ``distill``     fused linear JSD distillation: student Llama-3.2-1B-shaped head (Hs=2048)
                     against a Llama-3.1-8B-shaped teacher head (Ht=4096), V=128256,
                     BT=8192, bf16, W~N(0,0.02^2), all rows labelled, beta=0.5, T=1, mean,
@@ -54,6 +57,9 @@ WORKLOADS = {
     "frozen_head": dict(BT=16384, H=4096, V=151936, dtype="bf16", x_std=1.0, w_std=0.02,
                         bias_std=0.01, targets="uniform", ignore="random", n_ignored=8192,
                         reduction="none", grad_out="uniform", z=0.0, want_dW=False),
+    "llama2_7b": dict(BT=16384, H=4096, V=32000, dtype="bf16", x_std=1.0, w_std=0.02,
+                      bias_std=None, targets="uniform", ignore="none", reduction="mean",
+                      z=0.0, want_dW=True),
 }
 
 DISTILL = dict(name="distill", BT=8192, Hs=2048, Ht=4096, V=128256, dtype="bf16", x_std=1.0,
