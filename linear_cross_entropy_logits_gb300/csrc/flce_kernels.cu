@@ -701,11 +701,13 @@ __global__ void __launch_bounds__(256, 2) k_fwd_simt(const __grid_constant__ Cal
 }
 
 // ---------------------------------------------------------------------------------------
-// SIMT GEMMs of the backward, 128x128 output tiles on the core above.
+// SIMT GEMMs of the backward, (16 TL) x (16 TL) output tiles on the core above (TL = 8;
+// 4 when the 128 x 128 grid would leave most SMs idle: every output still sums its k in
+// the same order, so the two tile sizes give the same bits).
 //   MODE 0 (dX): dX[idx[r]] = cbar * sum_v G[r, v] W[v, :]        (M = rows, K = V)
 //   MODE 1 (dW): dW[v]     += cbar * sum_r G[r, v] Xc[r, :]       (M = V, K = rows)
 // ---------------------------------------------------------------------------------------
-template <typename T, int MODE>
+template <typename T, int MODE, int TL>
 __global__ void __launch_bounds__(256, 2) k_gemm_simt(const __grid_constant__ CallArgs a, int chunk) {
   int row0, rows;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
@@ -714,23 +716,23 @@ __global__ void __launch_bounds__(256, 2) k_gemm_simt(const __grid_constant__ Ca
   const int64_t M = MODE == 0 ? rows : a.V;
   const int64_t N = a.H;
   const int64_t K = MODE == 0 ? a.V : rows;
-  const int64_t m0 = (int64_t)blockIdx.y * 128, n0 = (int64_t)blockIdx.x * 128;
+  const int64_t m0 = (int64_t)blockIdx.y * (16 * TL), n0 = (int64_t)blockIdx.x * (16 * TL);
   if (m0 >= M) return;
-  __shared__ __align__(16) float smem[simt_smem_floats<8, 8>()];
-  float acc[8][8];
+  __shared__ __align__(16) float smem[simt_smem_floats<TL, TL>()];
+  float acc[TL][TL];
   const T* G = (const T*)a.w.slab;
   if constexpr (MODE == 0)
-    simt_gemm_tile<T, 8, 8, true, false>(G, a.Vp, m0, M, (const T*)a.W, a.H, n0, N, K, smem, acc);
+    simt_gemm_tile<T, TL, TL, true, false>(G, a.Vp, m0, M, (const T*)a.W, a.H, n0, N, K, smem, acc);
   else
-    simt_gemm_tile<T, 8, 8, false, false>(G, a.Vp, m0, M, (const T*)a.w.xc, a.Hp, n0, N, K, smem, acc);
+    simt_gemm_tile<T, TL, TL, false, false>(G, a.Vp, m0, M, (const T*)a.w.xc, a.Hp, n0, N, K, smem, acc);
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const float cb = a.w.ctrl->cbar;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < TL; ++i) {
     const int64_t m = m0 + simt_row(i, ty);
     if (m >= M) continue;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < TL; ++j) {
       const int64_t n = n0 + simt_col(j, tx);
       if (n >= N) continue;
       if (MODE == 0) {
@@ -842,11 +844,20 @@ cudaError_t launch_fwd_simt(const CallArgs& a, int chunk, cudaStream_t s) {
 }
 
 cudaError_t launch_dx_simt(const CallArgs& a, int chunk, cudaStream_t s) {
+  if (cdiv64(a.H, 128) * cdiv64(a.R, 128) < num_sms()) {  // few output tiles: 64 x 64
+    dim3 grid((unsigned)cdiv64(a.H, 64), (unsigned)cdiv64(a.R, 64));
+    switch (a.dt) {
+      case FLCE_BF16: k_gemm_simt<__nv_bfloat16, 0, 4><<<grid, 256, 0, s>>>(a, chunk); break;
+      case FLCE_F16: k_gemm_simt<__half, 0, 4><<<grid, 256, 0, s>>>(a, chunk); break;
+      default: k_gemm_simt<float, 0, 4><<<grid, 256, 0, s>>>(a, chunk); break;
+    }
+    return cudaGetLastError();
+  }
   dim3 grid((unsigned)cdiv64(a.H, 128), (unsigned)cdiv64(a.R, 128));
   switch (a.dt) {
-    case FLCE_BF16: k_gemm_simt<__nv_bfloat16, 0><<<grid, 256, 0, s>>>(a, chunk); break;
-    case FLCE_F16: k_gemm_simt<__half, 0><<<grid, 256, 0, s>>>(a, chunk); break;
-    default: k_gemm_simt<float, 0><<<grid, 256, 0, s>>>(a, chunk); break;
+    case FLCE_BF16: k_gemm_simt<__nv_bfloat16, 0, 8><<<grid, 256, 0, s>>>(a, chunk); break;
+    case FLCE_F16: k_gemm_simt<__half, 0, 8><<<grid, 256, 0, s>>>(a, chunk); break;
+    default: k_gemm_simt<float, 0, 8><<<grid, 256, 0, s>>>(a, chunk); break;
   }
   return cudaGetLastError();
 }
@@ -854,9 +865,9 @@ cudaError_t launch_dx_simt(const CallArgs& a, int chunk, cudaStream_t s) {
 cudaError_t launch_dw_simt(const CallArgs& a, int chunk, cudaStream_t s) {
   dim3 grid((unsigned)cdiv64(a.H, 128), (unsigned)cdiv64(a.V, 128));
   switch (a.dt) {
-    case FLCE_BF16: k_gemm_simt<__nv_bfloat16, 1><<<grid, 256, 0, s>>>(a, chunk); break;
-    case FLCE_F16: k_gemm_simt<__half, 1><<<grid, 256, 0, s>>>(a, chunk); break;
-    default: k_gemm_simt<float, 1><<<grid, 256, 0, s>>>(a, chunk); break;
+    case FLCE_BF16: k_gemm_simt<__nv_bfloat16, 1, 8><<<grid, 256, 0, s>>>(a, chunk); break;
+    case FLCE_F16: k_gemm_simt<__half, 1, 8><<<grid, 256, 0, s>>>(a, chunk); break;
+    default: k_gemm_simt<float, 1, 8><<<grid, 256, 0, s>>>(a, chunk); break;
   }
   return cudaGetLastError();
 }

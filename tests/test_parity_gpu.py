@@ -372,3 +372,20 @@ def test_mean_and_sum_equal_the_sum_of_per_token_values(n_lab):
             want = np.float32(np.sum(none[k][lab].astype(np.float64)) / d)
             got = np.float32(g[k][0])
             assert abs(got - want) <= 2 * np.spacing(np.abs(want)) + 1e-30, (red, k, got, want)
+
+
+def test_simt_dx_tile_sizes_give_the_same_bits():
+    """fp32 inputs: one 2432-row chunk runs the SIMT dX GEMM on 128x128 tiles (8 x 19 of
+    them), 128-row chunks on 64x64 tiles (few output tiles); every dX element sums its k in
+    the same order either way, so dX, lse and the per-token loss are bit-identical, and both
+    match the oracle."""
+    sp = I.spec("tiny_fp32", BT=2432, H=1024, V=500, reduction="none", want_dW=False,
+                n_ignored=0)
+    inp = I.generate(sp, seed=12)
+    wb = _ws_for_rows(sp["BT"], sp["H"], sp["V"], torch.float32, 128)
+    assert flce.chunk_rows(sp["BT"], sp["H"], sp["V"], torch.float32, wb) == 128
+    one = run_gpu(inp, sp)
+    many = run_gpu(inp, sp, workspace_bytes=wb)
+    for k in ("dX", "lse", "loss", "pred"):
+        assert np.array_equal(one[k], many[k]), k
+    compare_full(one, run_oracle(inp, sp), inp, sp)
