@@ -493,6 +493,23 @@ __global__ void __launch_bounds__(256) k_reduce(const __grid_constant__ CallArgs
 // KC: the operand's K index is the contiguous one (element (e, k) at p[e * ld + k]);
 // otherwise its row index e is (p[k * ld + e]). Elements outside the extents read as 0.
 // ---------------------------------------------------------------------------------------
+// Row / column of accumulator (i, j) of thread (ty, tx) within the block tile.
+__device__ __forceinline__ int simt_row(int i, int ty) { return (i >> 2) * 64 + ty * 4 + (i & 3); }
+__device__ __forceinline__ int simt_col(int j, int tx) { return (j >> 2) * 64 + tx * 4 + (j & 3); }
+// Thread coordinates in the 16 x 16 grid. The index that keeps more accumulators per thread
+// runs slower across a warp, so a warp's reads of that operand are two float4 broadcasts
+// (the forward's 4 x 16 accumulators per thread: 6 shared-memory wavefronts per k, not 9).
+template <int TM, int TN>
+__device__ __forceinline__ void simt_txy(int tid, int& tx, int& ty) {
+  if (TN > TM) {
+    ty = tid & 15;
+    tx = tid >> 4;
+  } else {
+    tx = tid & 15;
+    ty = tid >> 4;
+  }
+}
+
 constexpr int SK = 16;
 
 template <typename T, int E, bool KC>
@@ -575,7 +592,9 @@ __device__ __forceinline__ void simt_gemm_tile(const T* A, int64_t lda, int64_t 
                                                float (&acc)[TM][TN]) {
   constexpr int BM = 16 * TM, BN = 16 * TN;
   constexpr int SA = SK * (BM + 4), SB = SK * (BN + 4);
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int tid = threadIdx.x;
+  int tx, ty;
+  simt_txy<TM, TN>(tid, tx, ty);
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -605,9 +624,6 @@ __device__ __forceinline__ void simt_gemm_tile(const T* A, int64_t lda, int64_t 
   }
 }
 
-// Row / column of accumulator (i, j) of thread (ty, tx) within the block tile.
-__device__ __forceinline__ int simt_row(int i, int ty) { return (i >> 2) * 64 + ty * 4 + (i & 3); }
-__device__ __forceinline__ int simt_col(int j, int tx) { return (j >> 2) * 64 + tx * 4 + (j & 3); }
 
 // ---------------------------------------------------------------------------------------
 // SIMT forward: a 64-row x 256-column logit tile per block (one vocabulary tile), then the
@@ -626,7 +642,9 @@ __global__ void __launch_bounds__(256, 2) k_fwd_simt(const __grid_constant__ Cal
   float acc[4][16];
   simt_gemm_tile<T, 4, 16, true, true>((const T*)a.w.xc, a.Hp, (int64_t)mb * 64, rows, (const T*)a.W, a.H,
                                        (int64_t)t * VT, a.V, a.H, smem, acc);
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int tid = threadIdx.x;
+  int tx, ty;
+  simt_txy<4, 16>(tid, tx, ty);
   const int64_t V = a.V;
   float bj[16];
 #pragma unroll
@@ -725,7 +743,9 @@ __global__ void __launch_bounds__(256, 2) k_gemm_simt(const __grid_constant__ Ca
     simt_gemm_tile<T, TL, TL, true, false>(G, a.Vp, m0, M, (const T*)a.W, a.H, n0, N, K, smem, acc);
   else
     simt_gemm_tile<T, TL, TL, false, false>(G, a.Vp, m0, M, (const T*)a.w.xc, a.Hp, n0, N, K, smem, acc);
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int tid = threadIdx.x;
+  int tx, ty;
+  simt_txy<TL, TL>(tid, tx, ty);
   const float cb = a.w.ctrl->cbar;
 #pragma unroll
   for (int i = 0; i < TL; ++i) {
