@@ -15,6 +15,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "flce_internal.cuh"
 
 namespace flce {
@@ -441,9 +443,18 @@ cudaError_t launch_jsd_rows(const JsdArgs& j, int chunk, cudaStream_t s, bool gr
   int xt = 0;
   if (grads && sizeof(T) == 2 && j.beta > 0.0f) xt = j.s.nvt < JR_XTILES ? (int)j.s.nvt : JR_XTILES;
   const size_t smem = (size_t)xt * VT * 2;
-  if (smem > 0) {  // per device and cheap: set on every launch
-    const cudaError_t e = cudaFuncSetAttribute(k_jsd_rows<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the shared-memory limit (the largest any launch asks for) is set on a device's first
+  // launch and persists, so later launches, including ones captured into a CUDA graph,
+  // enqueue the kernel only; concurrent first launches may both set it
+  static std::atomic<int> attr_set[64];
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (smem > 0 && (dev < 0 || dev >= 64 || attr_set[dev].load(std::memory_order_relaxed) == 0)) {
+    e = cudaFuncSetAttribute(k_jsd_rows<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)((size_t)JR_XTILES * VT * 2));
     if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(1, std::memory_order_relaxed);
   }
   k_jsd_rows<T><<<(unsigned)g, JR_THREADS, smem, s>>>(j, chunk, grads ? 1 : 0, xt);
   return cudaGetLastError();
