@@ -418,8 +418,8 @@ __global__ void __launch_bounds__(256) k_scale_by(T* x, int64_t n, const float* 
 // ---------------------------------------------------------------------------------------
 // Final reductions (mean/sum) of loss, z-loss and accuracy over the labelled rows, in a
 // fixed order (deterministic): block b adds rows [b*per, (b+1)*per) in float64, and the
-// last block to finish adds the RED_BLOCKS partial sums in block order. float64 arithmetic
-// is slow on this GPU, so one block alone would take tens of microseconds.
+// last block to finish adds the RED_BLOCKS partial sums in block order. GB300 runs float64
+// at a small fraction of its fp32 rate, so one block alone would take tens of microseconds.
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_reduce(const __grid_constant__ CallArgs a) {
   __shared__ double red[3][8];
