@@ -11,6 +11,7 @@
 #include <atomic>
 #include <mutex>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 #include <string>
 #include <vector>
@@ -265,6 +266,32 @@ extern "C" int64_t flce_plan_describe(int64_t BT, int64_t H, int64_t V, int32_t 
   return n;
 }
 
+// FLCE_TRACE (environment, read once; any value but empty or "0"): every call prints its
+// plan (flce_plan_describe) and the path it takes to stderr, before it enqueues any work.
+static bool trace_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("FLCE_TRACE");
+    return e != nullptr && e[0] != '\0' && strcmp(e, "0") != 0;
+  }();
+  return on;
+}
+
+static void trace_call(const flce_args* x, bool tc, bool ref, const char* bwd) {
+  const int64_t n = flce_plan_describe(x->BT, x->H, x->V, x->in_dtype, x->workspace_bytes, nullptr, 0);
+  if (n > 0) {
+    std::string t((size_t)n + 1, '\0');
+    flce_plan_describe(x->BT, x->H, x->V, x->in_dtype, x->workspace_bytes, &t[0], t.size());
+    fputs(t.c_str(), stderr);
+  }
+  static const char* const red[3] = {"mean", "sum", "none"};
+  fprintf(stderr,
+          "  call: reduction=%s z=%g dX=%d dW=%d bias=%d flags=0x%x; GEMMs on %s; gradient form %s; %s\n",
+          red[x->reduction], (double)x->z_loss_scale, x->want_dX ? 1 : 0, x->want_dW ? 1 : 0,
+          x->bias != nullptr ? 1 : 0, (unsigned)x->flags, tc ? "tcgen05" : "SIMT fp32 FMA",
+          ref ? "row-reference (exp(s) slab)" : "per-tile (exp(s - tile max) slab)",
+          bwd);
+}
+
 extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
   const int32_t v = validate(x);
   if (v != FLCE_OK) return v;
@@ -323,15 +350,20 @@ extern "C" int32_t flce_fwd_bwd(const flce_args* x, void* stream) {
     }                                     \
   } while (0)
 
-  flce_profile* prof = x->profile;
-  FLCE_TRY(cudaMemsetAsync(a.w.status, 0, sizeof(int), s));
-  FLCE_TRY(staged(prof, FLCE_STAGE_PROLOGUE, 2, s, [&] { return launch_prologue(a, s); }));
   // Row-reference mode (bf16 tensor-core calls with gradients and no dbias): the forward
   // stores exp(s), finalize turns it into G up to one scale per row, and the gradient pass
   // over the slab is skipped. A chunk with a row outside the window is redone per tile by
   // three launches that do nothing otherwise (run_if = the chunk's flag).
   const bool ref = tc && grads && a.dt == FLCE_BF16 && a.dbias == nullptr &&
                    !(x->flags & FLCE_FLAG_NO_ROW_REF);
+  if (trace_enabled())
+    trace_call(x, tc, ref,
+               !grads ? "no backward"
+               : (tc && bwd_merged_supported(a)) ? "dX and dW in one launch"
+                                                 : "backward GEMMs in separate launches");
+  flce_profile* prof = x->profile;
+  FLCE_TRY(cudaMemsetAsync(a.w.status, 0, sizeof(int), s));
+  FLCE_TRY(staged(prof, FLCE_STAGE_PROLOGUE, 2, s, [&] { return launch_prologue(a, s); }));
   CallArgs ar = a;
   ar.ref_mode = ref ? 1 : 0;
   CallArgs afb = a;

@@ -7,6 +7,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 import tempfile
 
 import pytest
@@ -220,3 +221,31 @@ def test_noalloc_host_rejections(lib, kw, code):
     a = _args(**kw)
     assert lib.flce_fwd_bwd_noalloc(ctypes.byref(a), None) == code
     assert lib.flce_fwd_bwd_noalloc(None, None) == flce.FLCE_ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+def test_trace_prints_the_plan_of_each_call(tmp_path):
+    """FLCE_TRACE=1: a real call prints its plan and path to stderr (a child process, so the
+    switch is read fresh); without it nothing is printed."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    code = (
+        "import torch\n"
+        "from linear_cross_entropy_logits_gb300 import flce\n"
+        "flce.load()\n"
+        "X = torch.randn(256, 128, device='cuda').bfloat16()\n"
+        "W = (0.05 * torch.randn(1000, 128, device='cuda')).bfloat16()\n"
+        "t = torch.randint(0, 1000, (256,), device='cuda')\n"
+        "o = flce.fwd_bwd(X, W, t, None)\n"
+        "torch.cuda.synchronize()\n"
+        "assert o['status_code'] == flce.FLCE_OK\n")
+    env = dict(os.environ, PYTHONPATH=ROOT + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    on = subprocess.run([sys.executable, "-c", code], env=dict(env, FLCE_TRACE="1"), capture_output=True,
+                        text=True, timeout=600)
+    assert on.returncode == 0, on.stderr
+    assert "flce plan: BT=256 H=128 V=1000 dtype=bf16" in on.stderr
+    assert "GEMMs on tcgen05; gradient form row-reference" in on.stderr
+    off = subprocess.run([sys.executable, "-c", code], env=dict(env, FLCE_TRACE="0"), capture_output=True,
+                         text=True, timeout=600)
+    assert off.returncode == 0, off.stderr
+    assert "flce plan:" not in off.stderr
