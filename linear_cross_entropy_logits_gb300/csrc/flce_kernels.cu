@@ -134,22 +134,34 @@ __global__ void __launch_bounds__(256) k_gather(const __grid_constant__ CallArgs
   const int lim = (int)rup64(rows, CHUNK_ALIGN);
   const int esz = a.dt == FLCE_F32 ? 4 : 2;
   const int64_t src_bytes = a.H * esz, dst_bytes = a.Hp * esz;
-  for (int r = blockIdx.x; r < lim; r += gridDim.x) {
-    if (threadIdx.x == 0 && a.w.rmax != nullptr) a.w.rmax[r] = MAX_KEY_NEG_INF;
+  // 64 threads per row, four rows per block at a time; each thread keeps up to eight 16-byte
+  // loads in flight before it stores them
+  const int grp = threadIdx.x >> 6, lt = threadIdx.x & 63;
+  for (int r = blockIdx.x * 4 + grp; r < lim; r += gridDim.x * 4) {
+    if (lt == 0 && a.w.rmax != nullptr) a.w.rmax[r] = MAX_KEY_NEG_INF;
     char* dst = (char*)a.w.xc + (int64_t)r * dst_bytes;
     if (r < rows) {
       const char* src = (const char*)a.X + (int64_t)a.w.idx[row0 + r] * src_bytes;
       if ((src_bytes & 15) == 0) {
         const uint4* s4 = (const uint4*)src;
         uint4* d4 = (uint4*)dst;
-        for (int64_t j = threadIdx.x; j < src_bytes / 16; j += blockDim.x) d4[j] = s4[j];
+        const int64_t n16 = src_bytes / 16;
+        for (int64_t j0 = lt; j0 < n16; j0 += 64 * 8) {
+          uint4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (j0 + 64 * u < n16) v[u] = s4[j0 + 64 * u];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (j0 + 64 * u < n16) d4[j0 + 64 * u] = v[u];
+        }
       } else {
-        for (int64_t j = threadIdx.x; j < src_bytes; j += blockDim.x) dst[j] = src[j];
+        for (int64_t j = lt; j < src_bytes; j += 64) dst[j] = src[j];
       }
-      for (int64_t j = src_bytes + threadIdx.x; j < dst_bytes; j += blockDim.x) dst[j] = 0;
+      for (int64_t j = src_bytes + lt; j < dst_bytes; j += 64) dst[j] = 0;
     } else {
       uint4* d4 = (uint4*)dst;
-      for (int64_t j = threadIdx.x; j < dst_bytes / 16; j += blockDim.x) d4[j] = make_uint4(0, 0, 0, 0);
+      for (int64_t j = lt; j < dst_bytes / 16; j += 64) d4[j] = make_uint4(0, 0, 0, 0);
     }
   }
 }
@@ -373,19 +385,35 @@ __global__ void __launch_bounds__(256) k_gpass(const __grid_constant__ CallArgs 
 
 // ---------------------------------------------------------------------------------------
 // Row-reference mode: Xc rows *= rsc (bf16, in place) for the dW GEMM, unless the chunk
-// left the window (then Xc stays as gathered for the per-tile redo). One block per row.
+// left the window (then Xc stays as gathered for the per-tile redo).
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_scale_x(const __grid_constant__ CallArgs a, int chunk) {
   int row0, rows;
   if (!chunk_bounds(a.w.ctrl, chunk, row0, rows)) return;
   if (a.w.ctrl->fb) return;
-  __nv_bfloat162* x = (__nv_bfloat162*)a.w.xc;
-  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+  // 64 threads per row (a row is Hp / 8 16-byte units; the pad columns hold zeros, which
+  // stay zero), up to eight units in flight per thread
+  const int grp = threadIdx.x >> 6, lt = threadIdx.x & 63;
+  const int64_t n16 = a.Hp / 8;
+  for (int r = blockIdx.x * 4 + grp; r < rows; r += gridDim.x * 4) {
     const float sc = a.w.rsc[r];
-    __nv_bfloat162* xr = x + (int64_t)r * (a.Hp / 2);
-    for (int64_t j = threadIdx.x; j < (a.H + 1) / 2; j += blockDim.x) {  // pad column is 0
-      const float2 v = __bfloat1622float2(xr[j]);
-      xr[j] = __floats2bfloat162_rn(v.x * sc, v.y * sc);
+    uint4* xr = (uint4*)((__nv_bfloat16*)a.w.xc + (int64_t)r * a.Hp);
+    for (int64_t j0 = lt; j0 < n16; j0 += 64 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (j0 + 64 * u < n16) v[u] = xr[j0 + 64 * u];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + 64 * u >= n16) continue;
+        __nv_bfloat162* h = (__nv_bfloat162*)&v[u];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(h[k]);
+          h[k] = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+        }
+        xr[j0 + 64 * u] = v[u];
+      }
     }
   }
 }
@@ -814,7 +842,7 @@ cudaError_t launch_prologue(const CallArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_gather(const CallArgs& a, int chunk, cudaStream_t s) {
-  const int64_t blocks = a.R < 4LL * num_sms() ? a.R : 4LL * num_sms();
+  const int64_t blocks = cdiv64(a.R, 4) < 4LL * num_sms() ? cdiv64(a.R, 4) : 4LL * num_sms();
   k_gather<<<(unsigned)blocks, 256, 0, s>>>(a, chunk);
   return cudaGetLastError();
 }
@@ -835,7 +863,7 @@ cudaError_t launch_scale_by(void* x, int64_t n, int dtype, const float* g, cudaS
 }
 
 cudaError_t launch_scale_x(const CallArgs& a, int chunk, cudaStream_t s) {
-  const int64_t blocks = a.R < 4096 ? a.R : 4096;
+  const int64_t blocks = cdiv64(a.R, 4) < 4LL * num_sms() ? cdiv64(a.R, 4) : 4LL * num_sms();
   k_scale_x<<<(unsigned)blocks, 256, 0, s>>>(a, chunk);
   return cudaGetLastError();
 }
