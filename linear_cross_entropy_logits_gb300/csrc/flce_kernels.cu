@@ -204,7 +204,21 @@ __global__ void __launch_bounds__(256) k_finalize(const __grid_constant__ CallAr
   float M = -INFINITY, S = 0.0f;
   int am = 0x7fffffff;
   if (a.ref_mode) {
-    for (int t = lane; t < nvt; t += 32) ref_combine(M, S, am, stm[t], sts[t], sti[t]);
+    // eight tiles' loads per lane in flight, merged in the same order as one at a time
+    int t = lane;
+    for (; t + 32 * 7 < nvt; t += 32 * 8) {
+      float m8[8], s8[8];
+      int i8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        m8[u] = stm[t + 32 * u];
+        s8[u] = sts[t + 32 * u];
+        i8[u] = sti[t + 32 * u];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ref_combine(M, S, am, m8[u], s8[u], i8[u]);
+    }
+    for (; t < nvt; t += 32) ref_combine(M, S, am, stm[t], sts[t], sti[t]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
