@@ -240,6 +240,8 @@ constexpr int RU = FLCE_JR_RU;
 #define FLCE_JR_THREADS 768
 #endif
 constexpr int JR_THREADS = FLCE_JR_THREADS;
+static_assert(JR_THREADS % 32 == 0 && JR_THREADS >= 64 && JR_THREADS <= 1024, "whole warps, one CTA");
+static_assert(RU >= 1, "at least one tile in flight per warp");
 constexpr int JR_WARPS = JR_THREADS / 32;
 // Pass 1 also keeps the log ratio x = log2(Q / R) of the row's first JR_XTILES tiles in
 // shared memory (fp16, 200 KB), R = M (0 < beta < 1) or P (beta = 1); pass 2 then forms
