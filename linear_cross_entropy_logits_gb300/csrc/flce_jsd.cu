@@ -250,14 +250,14 @@ constexpr int JR_WARPS = JR_THREADS / 32;
 // fp16 keeps it to 2^-11 relative, below the 2^-9 rounding of the stored e.
 constexpr int JR_XTILES = 400;
 
-// 8 values <-> one 16-byte shared-memory word of fp16
+// 8 values <-> one 16-byte shared-memory word of fp16. The conversion saturates at the
+// largest finite fp16 (|x| past 65504 needs logit gaps beyond ~45000 after the temperature;
+// there Q underflows to 0, and a finite x keeps Q * x at 0 instead of NaN).
 __device__ __forceinline__ void xs_store(uint32_t addr, const float (&x)[8]) {
   uint32_t h[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    __half2 v = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
-    h[k] = *(uint32_t*)&v;
-  }
+  for (int k = 0; k < 4; ++k)  // upper half <- the odd column, lower half <- the even one
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "f"(x[2 * k + 1]), "f"(x[2 * k]));
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
                : "memory");
 }

@@ -198,3 +198,16 @@ def test_jsd_dw_modes(dw):
 
 def test_jsd_reverse_kl_sum_tc():
     _check("bf16", 1.0, 1.3, "sum", "tc", BT=333, Hs=200, Ht=136, V=2600, seed=69)
+
+
+@pytest.mark.parametrize("beta", [0.5, 1.0])
+def test_extreme_logit_gaps_stay_finite(beta):
+    """Logit gaps of ~1e5 after the temperature (T = 1e-3, logits of std ~16): the log ratio
+    kept in fp16 for the second pass saturates instead of overflowing, so the loss and the
+    gradients stay finite (a token whose Q underflows contributes 0, not 0 * inf)."""
+    Xs, Ws, Xt, Wt, labels, _ = _problem(256, 256, 256, 3000, "bf16", 61, 10, w_std=1.0)
+    out = flce.fused_linear_jsd(Xs.cuda(), Ws.cuda(), Xt.cuda(), Wt.cuda(), labels.cuda(), beta=beta,
+                                temperature=1e-3, reduction="mean")
+    assert out["status_code"] == flce.FLCE_OK
+    for k in ("loss", "dX", "dW"):
+        assert torch.isfinite(out[k].float()).all(), k
