@@ -187,8 +187,9 @@ FLCE_API int64_t flce_chunk_rows(int64_t BT, int64_t H, int64_t V, int32_t in_dt
  * balances the rows it actually finds over cdiv(N, R) chunks). Writes at most `out_len`
  * bytes including the terminating NUL into `out` (which may be NULL when out_len is 0) and
  * returns the length of the full text, like snprintf, or -1 for invalid sizes or dtype or
- * a workspace too small for one 128-row chunk. Host-only; touches no GPU. This is the tile
- * plan trace of the design, offered as a call rather than an environment switch. */
+ * a workspace too small for one 128-row chunk. Host-only; touches no GPU. The same text is
+ * printed to stderr by every flce_fwd_bwd call, with the path the call takes, when the
+ * environment variable FLCE_TRACE is set to a value other than "" or "0" (read once). */
 FLCE_API int64_t flce_plan_describe(int64_t BT, int64_t H, int64_t V, int32_t in_dtype,
                                     size_t workspace_bytes, char* out, size_t out_len);
 
